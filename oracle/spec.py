@@ -33,6 +33,15 @@ import numpy as np
 from .philox import uniform, PURPOSE_ACCEPT, PURPOSE_RESAMPLE, PURPOSE_DRAFT
 
 NEAR_TIE = 1e-5
+# Band of the top-p threshold decision (relative to the kept mass): the GPU's
+# cumulative masses at the crossing are fp32 sums of the few head bins above it,
+# accurate to a few 1e-7; a 1e-5 band would flag most rows of a large flat
+# nucleus, where single tokens carry ~1e-5 of the mass.
+THRESH_NEAR = 2e-6
+# Absolute floor of the KL comparison band in the mentor bisection: the fp32
+# rounding of a prefix sum of ~3e4 terms q ln(q/p) of size <= 1 (hierarchical
+# summation, about 1e-6) with margin.
+KL_ABS_TOL = 2e-6
 STATUS_OK = 0
 STATUS_EDATA = 4
 
@@ -58,8 +67,9 @@ def transformed_probs(z, temperature, top_k=0, top_p=1.0):
 
     z: [R, V] logits. Returns (probs [R, V] fp64, near_tie [R] bool). The
     near-tie flag marks rows whose top-p threshold is decided by a cumulative
-    mass within NEAR_TIE of top_p (at the kept crossing value or at the next
-    larger value), where fp32 and fp64 may legitimately choose differently.
+    mass within THRESH_NEAR of top_p (at the kept crossing value or at the
+    next larger value), where fp32 and fp64 may legitimately choose
+    differently.
     """
     z = _f64(z)
     R, V = z.shape
@@ -91,8 +101,8 @@ def transformed_probs(z, temperature, top_k=0, top_p=1.0):
             prev_last = np.full((R, V), -1)
             prev_last[:, 1:] = np.maximum.accumulate(idx, axis=1)[:, :-1]
             jp = prev_last[rows, j]
-            near = (frac[rows, j] - top_p) <= NEAR_TIE
-            near |= (jp >= 0) & ((top_p - frac[rows, np.maximum(jp, 0)]) <= NEAR_TIE)
+            near = (frac[rows, j] - top_p) <= THRESH_NEAR
+            near |= (jp >= 0) & ((top_p - frac[rows, np.maximum(jp, 0)]) <= THRESH_NEAR)
             keep &= z >= tau[:, None]
             e = e * keep
         q = e / e.sum(axis=1, keepdims=True)
@@ -117,7 +127,7 @@ def accept_test(u, q_x, p_x):
     return u < thr, rho, np.abs(u - thr) <= NEAR_TIE
 
 
-def inverse_cdf(u, w):
+def inverse_cdf(u, w, with_alt=False):
     """Index sampled from weights w [R, V] >= 0 with uniform u [R].
 
     The smallest i with C_i > u * W (C the inclusive prefix sum in index
@@ -125,7 +135,11 @@ def inverse_cdf(u, w):
     This is the draw x ~ (f)_+ of [SpS] "改进的拒绝采样" once the weights are
     max(0, q - p), and the ordinary draw from q for the bonus token.
     Returns (index [R], near_tie [R]) with near_tie when u*W lies within
-    NEAR_TIE * W of the boundary that decided the index.
+    NEAR_TIE * W of the boundary that decided the index. With with_alt=True
+    also returns alt [R]: where exactly one of the two boundaries of the
+    chosen interval is that close, the positive-weight neighbour across it
+    (the other admissible answer); -1 where there is no near boundary, -2
+    where both are near (ambiguous beyond one neighbour).
     """
     w = np.asarray(w, dtype=np.float64)
     u = np.asarray(u, dtype=np.float64)
@@ -136,11 +150,24 @@ def inverse_cdf(u, w):
     gt = C > t[:, None]
     rows = np.arange(R)
     has = gt.any(axis=1)
-    last_pos = V - 1 - np.argmax((w > 0)[:, ::-1], axis=1)
+    pos = w > 0
+    last_pos = V - 1 - np.argmax(pos[:, ::-1], axis=1)
     i = np.where(has, np.argmax(gt, axis=1), last_pos)
     lower = np.where(i > 0, C[rows, np.maximum(i - 1, 0)], -np.inf)
-    near = ((C[rows, i] - t) <= NEAR_TIE * W) | ((t - lower) <= NEAR_TIE * W) | ~has
-    return i, near
+    near_hi = (C[rows, i] - t) <= NEAR_TIE * W
+    near_lo = (t - lower) <= NEAR_TIE * W
+    near = near_hi | near_lo | ~has
+    if not with_alt:
+        return i, near
+    idx = np.arange(V)[None, :]
+    prev_pos = np.where(pos & (idx < i[:, None]), idx, -1).max(axis=1)
+    nxt = np.where(pos & (idx > i[:, None]), idx, V).min(axis=1)
+    alt = np.full(R, -1, dtype=np.int64)
+    alt = np.where(near_lo & ~near_hi & (prev_pos >= 0), prev_pos, alt)
+    alt = np.where(near_hi & ~near_lo & (nxt < V), nxt, alt)
+    alt = np.where((near_lo & near_hi) | ~has, -2, alt)
+    alt = np.where(near & (alt == -1), -2, alt)   # near, but no neighbour to offer
+    return i, near, alt
 
 
 def _emit(x, n, token):
@@ -181,9 +208,12 @@ def verify(target, draft, draft_tokens, temperature=1.0, top_p=1.0, top_k=0,
     n, RESAMPLE); ``uniform_fn(rows, pos, purpose)`` may replace them.
 
     Returns a dict: accepted [B], tokens [B, gamma+1] (-1 padded),
-    next_token [B], status [B], near_tie [B], q_x / p_x [B, gamma] (the
-    probabilities of each draft token), prob_near [B, gamma] (top-p threshold
-    near-tie in either row at that position).
+    next_token [B], status [B], near_tie [B] (a decision within the near-tie
+    band: the row is excluded from exact comparison), alt_token [B] (where
+    the final draw's uniform sits within the band of one CDF boundary, the
+    neighbouring token across it, equally admissible; -1 otherwise),
+    q_x / p_x [B, gamma] (the probabilities of each draft token), prob_near
+    [B, gamma] (top-p threshold near-tie in either row at that position).
     """
     zt = _f64(target)
     B, G1, V = zt.shape
@@ -202,6 +232,7 @@ def verify(target, draft, draft_tokens, temperature=1.0, top_p=1.0, top_k=0,
 
     n = np.full(B, gamma, dtype=np.int64)
     token = np.full(B, -1, dtype=np.int64)
+    alt = np.full(B, -1, dtype=np.int64)
     near = np.zeros(B, dtype=bool)
     q_x = np.full((B, gamma), np.nan)
     p_x = np.full((B, gamma), np.nan)
@@ -230,16 +261,18 @@ def verify(target, draft, draft_tokens, temperature=1.0, top_p=1.0, top_k=0,
                 w = np.maximum(0.0, q[rej] - p[rej])
                 zero = w.sum(axis=1) == 0
                 w[zero] = q[rej][zero]
-                tok, near_cdf = inverse_cdf(U(rows[rej], k, PURPOSE_RESAMPLE), w)
+                tok, _, a = inverse_cdf(U(rows[rej], k, PURPOSE_RESAMPLE), w, with_alt=True)
                 token[rej] = tok
-                near[rej] |= near_cdf
+                alt[rej] = np.maximum(a, -1)
+                near[rej] |= a == -2
                 n[rej] = k
         allacc = n == gamma
         if allacc.any():
             q, nq = transformed_probs(zt[allacc, gamma], temperature, top_k, top_p)
-            tok, near_cdf = inverse_cdf(U(rows[allacc], gamma, PURPOSE_RESAMPLE), q)
+            tok, _, a = inverse_cdf(U(rows[allacc], gamma, PURPOSE_RESAMPLE), q, with_alt=True)
             token[allacc] = tok
-            near[allacc] |= near_cdf | nq
+            alt[allacc] = np.maximum(a, -1)
+            near[allacc] |= (a == -2) | nq
 
     tokens = _emit(x, n, token)
     accepted = n.copy()
@@ -248,8 +281,9 @@ def verify(target, draft, draft_tokens, temperature=1.0, top_p=1.0, top_k=0,
     tokens[bad] = -1
     token[bad] = -1
     near[bad] = False
+    alt[bad | near] = -1
     return dict(accepted=accepted, tokens=tokens, next_token=token, status=status,
-                near_tie=near, q_x=q_x, p_x=p_x, prob_near=prob_near)
+                near_tie=near, alt_token=alt, q_x=q_x, p_x=p_x, prob_near=prob_near)
 
 
 def sample(logits, temperature=1.0, top_p=1.0, top_k=0, seed=0, offset=0,
@@ -259,28 +293,33 @@ def sample(logits, temperature=1.0, top_p=1.0, top_k=0, seed=0, offset=0,
     The ordinary sampler that [SpS] Algorithm 1 (ArS) and the drafting step
     use, with the transforms of [SpS] "与标准采样方法的兼容性". logits
     [B, P, V]; token[b, j] uses U(seed, offset+b, pos0+j, purpose) and the
-    inverse CDF in index order (temperature 0: argmax). Returns dict with
-    tokens [B, P], near_tie [B, P], status [B].
+    inverse CDF in index order (temperature 0: argmax). A bad row (NaN,
+    +inf, all -inf) gets token -1 and marks its sequence with status 4.
+    Returns dict with tokens [B, P], near_tie [B, P], status [B].
     """
     z = _f64(logits)
     B, P, V = z.shape
     U = _uniform_fn(seed, uniform_fn)
     rows = np.uint64(offset) + np.arange(B, dtype=np.uint64)
     tokens = np.full((B, P), -1, dtype=np.int64)
+    alt = np.full((B, P), -1, dtype=np.int64)
     near = np.zeros((B, P), dtype=bool)
-    bad = _bad_rows(z).any(axis=1)
+    bad = _bad_rows(z)
     for j in range(P):
         q, nq = transformed_probs(z[:, j], temperature, top_k, top_p)
         if temperature == 0:
             tokens[:, j] = np.argmax(q, axis=1)
             continue
         with np.errstate(invalid="ignore"):
-            tok, near_cdf = inverse_cdf(U(rows, pos0 + j, purpose), np.nan_to_num(q))
+            tok, _, a = inverse_cdf(U(rows, pos0 + j, purpose), np.nan_to_num(q), with_alt=True)
         tokens[:, j] = tok
-        near[:, j] = nq | near_cdf
+        alt[:, j] = np.maximum(a, -1)
+        near[:, j] = nq | (a == -2)
     tokens[bad] = -1
     near[bad] = False
-    return dict(tokens=tokens, near_tie=near, status=np.where(bad, STATUS_EDATA, STATUS_OK))
+    alt[bad | near] = -1
+    return dict(tokens=tokens, near_tie=near, alt_token=alt,
+                status=np.where(bad.any(axis=1), STATUS_EDATA, STATUS_OK))
 
 
 # ---------------------------------------------------------------------------
@@ -400,18 +439,24 @@ def mentor_solve(q, p, kl_bound, iters=30):
     (KL(mid) <= D -> hi = mid), return alpha = hi. alpha = 1 gives beta = 1
     exactly (standard speculative sampling); D = 0 gives alpha = 1 directly.
 
-    Returns dict(alpha, beta, kl0, shortcut, near): shortcut when
-    KL(q || p) <= D (fast path of the same section: accept directly);
-    near when KL(q||p) or any KL(mid) lies within NEAR_TIE * D of D.
+    Returns dict(alpha, beta, alpha_lo, beta_lo, alpha_hi, beta_hi, kl0,
+    shortcut, near): shortcut when KL(q || p) <= D (fast path of the same
+    section: accept directly); near when KL(q||p) lies within
+    band = NEAR_TIE * D + KL_ABS_TOL of D. [alpha_lo, alpha_hi] are the
+    bisection results for the bounds D + band and D - band: every result a
+    bisection can reach when each KL evaluation is off by at most band (the
+    last steps of a bisection always sit inside the band, so the admissible
+    answers form this range rather than one value).
     """
     q = np.asarray(q, dtype=np.float64)
     p = np.asarray(p, dtype=np.float64)
     D = float(kl_bound)
+    band = NEAR_TIE * D + KL_ABS_TOL
     with np.errstate(divide="ignore", invalid="ignore"):
         rho = np.where(p > 0, q / np.where(p > 0, p, 1.0), np.where(q > 0, np.inf, 0.0))
         qlr = np.where(q > 0, q * np.log(np.where(q > 0, rho, 1.0)), 0.0)
     kl0 = float(qlr.sum())
-    near = abs(kl0 - D) <= NEAR_TIE * D
+    near = abs(kl0 - D) <= band
     if kl0 <= D:
         return dict(alpha=0.0, beta=np.inf, kl0=kl0, shortcut=True, near=near)
     order = np.argsort(rho, kind="stable")
@@ -442,20 +487,26 @@ def mentor_solve(q, p, kl_bound, iters=30):
         # KL(alpha) > 0 for every alpha < 1 once KL(q||p) > 0, so D = 0 admits
         # alpha = 1 only; KL(1 - eps) ~ eps^2 sinks below fp64 rounding for
         # eps < 1e-7, so the bisection could not resolve this limit itself.
-        return dict(alpha=1.0, beta=1.0, kl0=kl0, shortcut=False, near=near)
-    lo, hi = 0.0, 1.0
-    for _ in range(iters):
-        mid = 0.5 * (lo + hi)
-        kl, _ = at(mid)
-        if abs(kl - D) <= NEAR_TIE * D:
-            near = True
-        if kl <= D:
-            hi = mid
-        else:
-            lo = mid
-    alpha = hi
-    beta = 1.0 if alpha == 1.0 else at(alpha)[1]
-    return dict(alpha=alpha, beta=beta, kl0=kl0, shortcut=False, near=near)
+        return dict(alpha=1.0, beta=1.0, alpha_lo=1.0, beta_lo=1.0, alpha_hi=1.0, beta_hi=1.0,
+                    kl0=kl0, shortcut=False, near=near)
+    def bisect(bound):
+        lo, hi = 0.0, 1.0
+        for _ in range(iters):
+            mid = 0.5 * (lo + hi)
+            if at(mid)[0] <= bound:
+                hi = mid
+            else:
+                lo = mid
+        return hi
+
+    def beta_of(a):
+        return 1.0 if a == 1.0 else at(a)[1]
+
+    alpha = bisect(D)
+    # the results a bisection reaches when every KL(mid) may be off by +-band
+    alpha_lo, alpha_hi = bisect(D + band), bisect(D - band)
+    return dict(alpha=alpha, beta=beta_of(alpha), alpha_lo=alpha_lo, beta_lo=beta_of(alpha_lo),
+                alpha_hi=alpha_hi, beta_hi=beta_of(alpha_hi), kl0=kl0, shortcut=False, near=near)
 
 
 def verify_mentor(target, draft, draft_tokens, temperature=1.0, kl_bound=0.0,
@@ -474,7 +525,9 @@ def verify_mentor(target, draft, draft_tokens, temperature=1.0, kl_bound=0.0,
 
     Returns the ``verify`` dict plus alpha [B, gamma] and beta [B, gamma] for
     the decided positions k <= accepted: -1 where the standard test accepted,
-    0 for the KL(q||p) <= D shortcut, the bisection result otherwise.
+    0 for the KL(q||p) <= D shortcut, the bisection result otherwise; and
+    alpha_lo / alpha_hi, the range of admissible bisection results (see
+    mentor_solve). A decision that differs across that range is a near-tie.
     """
     zt = _f64(target)
     B, G1, V = zt.shape
@@ -489,9 +542,12 @@ def verify_mentor(target, draft, draft_tokens, temperature=1.0, kl_bound=0.0,
     xs = np.clip(x, 0, V - 1)
     n = np.full(B, gamma, dtype=np.int64)
     token = np.full(B, -1, dtype=np.int64)
+    alt_tok = np.full(B, -1, dtype=np.int64)
     near = np.zeros(B, dtype=bool)
     alpha = np.full((B, gamma), np.nan)
     beta = np.full((B, gamma), np.nan)
+    alpha_lo = np.full((B, gamma), np.nan)
+    alpha_hi = np.full((B, gamma), np.nan)
     q_x = np.full((B, gamma), np.nan)
     p_x = np.full((B, gamma), np.nan)
     brange = np.arange(B)
@@ -516,31 +572,42 @@ def verify_mentor(target, draft, draft_tokens, temperature=1.0, kl_bound=0.0,
             a, be = sol["alpha"], sol["beta"]
             alpha[b, k] = a
             beta[b, k] = be
+            alpha_lo[b, k], alpha_hi[b, k] = sol["alpha_lo"], sol["alpha_hi"]
             thr = min(1.0, rho[b] / a)
             near[b] |= abs(u[b] - thr) <= NEAR_TIE
+            near[b] |= (u[b] < min(1.0, rho[b] / sol["alpha_lo"])) != (u[b] < min(1.0, rho[b] / sol["alpha_hi"]))
             if u[b] < thr:
                 continue
-            w = np.maximum(0.0, q[b] / be - p[b])
-            if w.sum() == 0:
-                w = q[b]
-            tok, near_cdf = inverse_cdf(U(rows[b:b + 1], k, PURPOSE_RESAMPLE), w[None, :])
+            u2 = U(rows[b:b + 1], k, PURPOSE_RESAMPLE)
+
+            def draw(bb):
+                w = np.maximum(0.0, q[b] / bb - p[b])
+                if w.sum() == 0:
+                    w = q[b]
+                return inverse_cdf(u2, w[None, :], with_alt=True)
+
+            tok, _, a_alt = draw(be)
+            others = {int(draw(sol["beta_lo"])[0][0]), int(draw(sol["beta_hi"])[0][0])}
             token[b] = tok[0]
-            near[b] |= near_cdf[0]
+            alt_tok[b] = max(int(a_alt[0]), -1)
+            near[b] |= (a_alt[0] == -2) or bool(others - {int(tok[0]), alt_tok[b]})
             n[b] = k
     allacc = (n == gamma) & ~bad
     if allacc.any():
         q, _ = transformed_probs(zt[allacc, gamma], temperature)
-        tok, near_cdf = inverse_cdf(U(rows[allacc], gamma, PURPOSE_RESAMPLE), q)
+        tok, _, a = inverse_cdf(U(rows[allacc], gamma, PURPOSE_RESAMPLE), q, with_alt=True)
         token[allacc] = tok
-        near[allacc] |= near_cdf
+        alt_tok[allacc] = np.maximum(a, -1)
+        near[allacc] |= a == -2
     tokens = _emit(x, n, token)
     tokens[bad] = -1
     accepted = np.where(bad, -1, n)
     token[bad] = -1
     near[bad] = False
+    alt_tok[bad | near] = -1
     return dict(accepted=accepted, tokens=tokens, next_token=token,
-                status=np.where(bad, STATUS_EDATA, STATUS_OK), near_tie=near,
-                alpha=alpha, beta=beta, q_x=q_x, p_x=p_x)
+                status=np.where(bad, STATUS_EDATA, STATUS_OK), near_tie=near, alt_token=alt_tok,
+                alpha=alpha, beta=beta, alpha_lo=alpha_lo, alpha_hi=alpha_hi, q_x=q_x, p_x=p_x)
 
 
 # ---------------------------------------------------------------------------

@@ -113,5 +113,6 @@ def test_nucleus_near_tie_flag():
     # masses 0.5, 0.3, 0.2 -> mass of the top two is exactly 0.8
     z = np.log(np.array([[0.5, 0.3, 0.2]]))
     assert transformed_probs(z, 1.0, top_p=0.8)[1][0]
-    assert transformed_probs(z, 1.0, top_p=0.8 + 5e-6)[1][0]
+    assert transformed_probs(z, 1.0, top_p=0.8 + 1e-6)[1][0]
+    assert not transformed_probs(z, 1.0, top_p=0.8 + 5e-6)[1][0]
     assert not transformed_probs(z, 1.0, top_p=0.79)[1][0]
