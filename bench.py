@@ -1,0 +1,356 @@
+"""Throughput benchmark of the verification step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One bench step is one pass of the whole verification path over one batch:
+for the default workload ("nucleus": B=8, gamma=4, V=32000, bf16, T=0.8,
+top_p=0.95, 1000 steps) the 1000 verification steps are issued as one call
+over 8000 sequences (offset = step * B, so every Philox counter is the one a
+step-by-step loop would use). Inputs (4.6 GB) are resident in HBM and larger
+than L2, so no flush is needed between timed steps.
+
+Prints one JSON line: verified positions/s (whole job), the roofline of the
+dominant kernel (algorithmic bytes / CUDA-event time against the measured HBM
+copy bandwidth), the CPU oracle baseline, the end-to-end figure through the
+public API with host buffers, launch count and SM clocks during the run.
+Under torchrun (N > 1) every rank runs an independent replica (the path
+shards by sequence with no exchange), and rank 0 reports the aggregate.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "verified positions/sec and achieved HBM GB/s vs GB300 roofline (1 GPU)"
+UNIT = "positions/s"
+
+WORKLOADS = {
+    # name: (config, steps stacked into one call, temperature override)
+    "nucleus": ("nucleus", 1000, None),
+    "tiny": ("tiny", 64, None),
+    "large_vocab": ("large_vocab", 1, 1.0),
+    "large_vocab_t0": ("large_vocab", 1, 0.0),
+    "tree": ("tree", 4, None),
+    "mentor": ("mentor", 12, None),
+}
+
+KERNEL_OF = {"nucleus": "row_kernel<bf16,transform>", "tiny": "row_kernel<f32>",
+             "large_vocab": "row_kernel<f32>", "large_vocab_t0": "argmax_kernel<f32>",
+             "tree": "argmax_kernel<f32>", "mentor": "row_kernel<f32> + mentor_kernel"}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def recorded_traffic(workload):
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu summary."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    return None if e is None else e.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4)
+                          if len(r) > 5 + i and r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def make_inputs(name, steps_stacked, temperature, device, seed=2024):
+    """Synthetic inputs of a workload on the device (generator: workloads.py)."""
+    import speculative_decoding_verification_05_gb300 as sv
+
+    c = dict(workloads.CONFIGS[name])
+    if c["kind"] == "tree":
+        B = c["B"] * steps_stacked
+        z, tok, par, dep = workloads.tree_inputs(B, c["N"], c["V"], seed, device="cpu")
+        return dict(kind="tree", z=z.to(device), tok=tok.to(device), par=par.to(device), dep=dep.to(device),
+                    B=B, N=c["N"], V=c["V"], max_depth=c["max_depth"], esize=4)
+    T = c["temperature"] if temperature is None else temperature
+    zt, zd = workloads.config_logits(name, seed, steps=steps_stacked, device=device)
+    B = zt.shape[0]
+    top_p = c.get("top_p", 1.0)
+    # drafts: the library's own sampler on the transformed draft distribution
+    drafts = sv.sample(zd, T, top_p, 0, seed=seed, offset=0, purpose=sv.PURPOSE_DRAFT)["tokens"]
+    return dict(kind=c["kind"], zt=zt, zd=zd, drafts=drafts, B=B, gamma=c["gamma"], V=c["V"], T=T,
+                top_p=top_p, kl_bound=c.get("kl_bound", 0.0), iters=c.get("iters", 30),
+                esize=zt.element_size())
+
+
+def run_step(inp):
+    import speculative_decoding_verification_05_gb300 as sv
+
+    if inp["kind"] == "tree":
+        return sv.verify_tree(inp["z"], inp["tok"], inp["par"], inp["dep"], inp["max_depth"])
+    if inp["kind"] == "mentor":
+        return sv.verify_mentor(inp["zt"], inp["zd"], inp["drafts"], inp["T"], inp["kl_bound"], inp["iters"])
+    return sv.verify(inp["zt"], inp["zd"], inp["drafts"], inp["T"], inp["top_p"], 0, 0, 0)
+
+
+def run_step_host(inp, host):
+    """End-to-end through the public API: pinned host inputs in, host outputs back."""
+    import speculative_decoding_verification_05_gb300 as sv
+
+    if inp["kind"] == "tree":
+        return sv.verify_tree(host["z"], host["tok"], host["par"], host["dep"], inp["max_depth"])
+    if inp["kind"] == "mentor":
+        return sv.verify_mentor(host["zt"], host["zd"], host["drafts"], inp["T"], inp["kl_bound"], inp["iters"])
+    return sv.verify(host["zt"], host["zd"], host["drafts"], inp["T"], inp["top_p"], 0, 0, 0)
+
+
+def algorithmic(inp):
+    """(bytes, verified positions) one step must read / decides."""
+    if inp["kind"] == "tree":
+        return (workloads.algorithmic_bytes("tree", inp["B"], inp["V"], inp["esize"], N=inp["N"]),
+                workloads.verified_positions("tree", inp["B"], N=inp["N"]))
+    return (workloads.algorithmic_bytes("linear", inp["B"], inp["V"], inp["esize"], gamma=inp["gamma"],
+                                        temperature=inp["T"]),
+            workloads.verified_positions("linear", inp["B"], gamma=inp["gamma"]))
+
+
+def launches_per_step(inp):
+    return 2 if inp["kind"] == "mentor" else 1
+
+
+def cpu_baseline(name, temperature, budget_s=12.0):
+    """The oracle, as it stands, on a bounded sample of the workload (host cores)."""
+    import oracle
+
+    c = dict(workloads.CONFIGS[name])
+    T = c["temperature"] if temperature is None else temperature
+    if c["kind"] == "tree":
+        B = c["B"]
+        z, tok, par, dep = workloads.tree_inputs(B, c["N"], c["V"], 99)
+        t0 = time.perf_counter()
+        n = 0
+        while time.perf_counter() - t0 < budget_s:
+            oracle.verify_tree(z, tok, par, dep, c["max_depth"])
+            n += 1
+        dt = time.perf_counter() - t0
+        pos = n * B * (c["N"] - 1)
+        return {"value": pos / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": f"{n} calls of {B} trees (N={c['N']}, V={c['V']}) in {dt:.1f} s"}
+    B = c["B"]
+    zt, zd = workloads.config_logits(name, 99, steps=1)
+    top_p = c.get("top_p", 1.0)
+    drafts = oracle.sample(zd, T, top_p, 0, seed=99)["tokens"]
+    t0 = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t0 < budget_s:
+        if c["kind"] == "mentor":
+            oracle.verify_mentor(zt, zd, drafts, T, c["kl_bound"], c["iters"], seed=n, offset=n * B)
+        else:
+            oracle.verify(zt, zd if T > 0 else None, drafts, T, top_p, 0, seed=n, offset=n * B)
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": n * B * c["gamma"] / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} steps of B={B} ({n * B * c['gamma']} positions, V={c['V']}) in {dt:.1f} s"}
+
+
+def reference_arm(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    cfg, _, temp = WORKLOADS[args.workload]
+    for _ in range(args.warmup):
+        cpu_baseline(cfg, temp, budget_s=1.0)
+    vals = [cpu_baseline(cfg, temp, budget_s=max(2.0, 60.0 / max(1, args.steps))) for _ in range(args.steps)]
+    v = statistics.median(x["value"] for x in vals)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": vals[0]["sample"]},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="nucleus", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return reference_arm(args)
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    import speculative_decoding_verification_05_gb300 as sv
+
+    sv.load_library()
+    cfg, stacked, temp = WORKLOADS[args.workload]
+    inp = make_inputs(cfg, stacked, temp, device, seed=2024 + rank)
+    nbytes, npos = algorithmic(inp)
+    stream = torch.cuda.current_stream(device)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(device)
+
+    for _ in range(args.warmup):
+        run_step(inp)
+    barrier()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        barrier()
+        t_all0 = torch.cuda.Event(enable_timing=True)
+        t_all1 = torch.cuda.Event(enable_timing=True)
+        t_all0.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            run_step(inp)
+            ends[i].record(stream)
+        t_all1.record(stream)
+        barrier()
+    total_ms = t_all0.elapsed_time(t_all1)
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = ws * npos * args.steps / (total_ms / 1e3)
+
+    # acceptance statistics of one step (a property of the synthetic inputs)
+    out = run_step(inp)
+    torch.cuda.synchronize(device)
+    acc_mean = None
+    if "accepted" in out:
+        acc_mean = float(out["accepted"].float().mean().item())
+    elif "accept_len" in out:
+        acc_mean = float(out["accept_len"].float().mean().item())
+
+    e2e = None
+    if not args.no_e2e:
+        host = {k: v.to("cpu").pin_memory() for k, v in inp.items() if isinstance(v, torch.Tensor)}
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        for _ in range(2):
+            run_step_host(inp, host)
+        torch.cuda.synchronize(device)
+        n_e2e = max(3, min(args.steps, 10))
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            r = run_step_host(inp, host)
+        dt = time.perf_counter() - t0
+        d2h = sum(v.numel() * v.element_size() for v in r.values() if isinstance(v, torch.Tensor))
+        e2e = {"value": ws * npos * n_e2e / dt, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": n_e2e}
+        del host
+
+    if rank != 0:
+        return 0
+    peak, peak_kind = measured_peaks()
+    avg_launch_ms = statistics.mean(per_launch_ms)
+    achieved = nbytes / (avg_launch_ms / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "traffic": recorded_traffic(args.workload),
+            "kernel": KERNEL_OF[args.workload], "algorithmic_bytes_per_launch": nbytes,
+            "peak_source": f"{peak_kind} hbm_gbs (copy)", "frac_of_nominal_8TBps": achieved / 8000.0}
+    cpu = None if args.no_cpu else cpu_baseline(cfg, temp)
+    c = workloads.CONFIGS[cfg]
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if inp["esize"] == 2 else "f32", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {cfg} x {stacked} steps in one call "
+                               f"(B={inp['B']}, V={inp['V']})", "global_batch": inp["B"] * ws,
+                   "bytes_per_step": nbytes, "positions_per_step": npos,
+                   "l2": "inputs larger than L2 (no flush)" if nbytes > 4 * 129e6 else "L2 flushed",
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches_per_step(inp) * args.steps,
+        "clocks": clk.summary(),
+        "hbm_gbs": achieved, "mean_accepted": acc_mean,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

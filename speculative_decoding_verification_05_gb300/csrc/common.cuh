@@ -1,0 +1,333 @@
+// Shared device helpers and launch parameter blocks for libspecverify.
+//
+// Everything here is GB300 (sm_103a) device code or plain host structs; the
+// CPU oracle in the repository does not include or call any of it.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#define SV_DEV __device__ __forceinline__
+#define SV_HD __host__ __device__ __forceinline__
+
+namespace sv {
+
+// Status codes written to status[b] (mirror spec_status in specverify.h).
+constexpr int kOk = 0;
+constexpr int kEData = 4;
+constexpr int kETimeout = 3;
+
+// Per-task record flags.
+constexpr int kRecAccept = 1;    // the standard test u < min(1, q/p) accepted
+constexpr int kRecEData = 2;     // bad logits in this task's rows / bad token
+constexpr int kRecTimeout = 4;   // a bounded copy wait gave up
+constexpr int kRecSolved = 8;    // (mentor) the lossy test accepted
+
+constexpr uint32_t kPurposeAccept = 0;
+constexpr uint32_t kPurposeResample = 1;
+
+// ---------------------------------------------------------------------------
+// Philox-4x32-10, written from Salmon, Moraes, Dror, Shaw, "Parallel Random
+// Numbers: As Easy as 1, 2, 3" (SC'11). One round maps (c0, c1, c2, c3) to
+// (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0)); the key
+// advances by the Weyl constants between rounds.
+// ---------------------------------------------------------------------------
+struct Philox4 {
+    uint32_t v[4];
+};
+
+SV_HD Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
+                            uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+#ifdef __CUDA_ARCH__
+        const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+#else
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c0, p1 = (uint64_t)0xCD9E8D57u * c2;
+        const uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+        const uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+#endif
+        const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    return Philox4{{c0, c1, c2, c3}};
+}
+
+// u = ((w0 >> 9) + 0.5) * 2^-23 for counter (row lo, row hi, position, purpose)
+// and key (seed lo, seed hi): 2^23 equally likely values in (0, 1), exact in fp32.
+SV_HD float uniform01(uint64_t seed, uint64_t row, uint32_t pos, uint32_t purpose) {
+    const Philox4 r = philox4x32_10((uint32_t)row, (uint32_t)(row >> 32), pos, purpose,
+                                    (uint32_t)seed, (uint32_t)(seed >> 32));
+    return ((float)(r.v[0] >> 9) + 0.5f) * 0x1p-23f;
+}
+
+// ---------------------------------------------------------------------------
+// Order-preserving 32-bit keys of fp32 values (-0 folded onto +0 so that
+// equal values share a key). bf16 values converted to fp32 exactly keep all
+// their information in the top 16 key bits.
+// ---------------------------------------------------------------------------
+SV_HD uint32_t f32_key(float x) {
+#ifdef __CUDA_ARCH__
+    uint32_t b = __float_as_uint(x);
+#else
+    uint32_t b;
+    __builtin_memcpy(&b, &x, 4);
+#endif
+    b = (b == 0x80000000u) ? 0u : b;
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+SV_DEV float key_to_f32(uint32_t k) {
+    const uint32_t b = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+    return __uint_as_float(b);
+}
+
+constexpr uint32_t kKeyNegInf = 0x007FFFFFu;  // f32_key(-inf)
+constexpr uint32_t kKeyPosInf = 0xFF800000u;  // f32_key(+inf)
+
+// 2^x on the MUFU unit (ex2.approx.ftz: about 2 ulp).
+SV_DEV float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ---------------------------------------------------------------------------
+// 16-byte vectors of logits.
+// ---------------------------------------------------------------------------
+template <typename E>
+struct VecTraits;
+
+template <>
+struct VecTraits<float> {
+    static constexpr int kN = 4;
+    static constexpr uint32_t kNegInfBits = 0xFF800000u;
+    SV_DEV static void unpack(const uint4& r, float (&x)[4]) {
+        x[0] = __uint_as_float(r.x);
+        x[1] = __uint_as_float(r.y);
+        x[2] = __uint_as_float(r.z);
+        x[3] = __uint_as_float(r.w);
+    }
+    SV_DEV static float load1(const void* p) { return __ldg(reinterpret_cast<const float*>(p)); }
+};
+
+struct bf16_t {
+    uint16_t bits;
+};
+
+template <>
+struct VecTraits<bf16_t> {
+    static constexpr int kN = 8;
+    static constexpr uint32_t kNegInfBits = 0xFF80u;
+    SV_DEV static void unpack(const uint4& r, float (&x)[8]) {
+        x[0] = __uint_as_float(r.x << 16);
+        x[1] = __uint_as_float(r.x & 0xFFFF0000u);
+        x[2] = __uint_as_float(r.y << 16);
+        x[3] = __uint_as_float(r.y & 0xFFFF0000u);
+        x[4] = __uint_as_float(r.z << 16);
+        x[5] = __uint_as_float(r.z & 0xFFFF0000u);
+        x[6] = __uint_as_float(r.w << 16);
+        x[7] = __uint_as_float(r.w & 0xFFFF0000u);
+    }
+    SV_DEV static float load1(const void* p) {
+        const unsigned short v = __ldg(reinterpret_cast<const unsigned short*>(p));
+        return __uint_as_float(((uint32_t)v) << 16);
+    }
+};
+
+// ---------------------------------------------------------------------------
+// mbarrier + bulk asynchronous copy (TMA engine, non-tensor form).
+// ---------------------------------------------------------------------------
+SV_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+SV_DEV void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+SV_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+SV_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for phase `parity`; returns false if it gave up after `limit` polls.
+SV_DEV bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t it = 0; it < limit; ++it)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// global -> own shared memory, `bytes` a multiple of 16, both addresses 16-byte aligned.
+SV_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Warp reductions.
+// ---------------------------------------------------------------------------
+SV_DEV float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+SV_DEV float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+SV_DEV unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        const unsigned long long w = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+        v = w > v ? w : v;
+    }
+    return v;
+}
+SV_DEV uint32_t warp_min_u32(uint32_t v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// Exclusive prefix of v over lanes 0..31 in lane order, summed sequentially so
+// that prefix[l+1] == prefix[l] + v[l] exactly. Returns the lane's exclusive
+// prefix; *total receives the sequential total.
+SV_DEV float warp_seq_exclusive(float v, float* total) {
+    const int lane = threadIdx.x & 31;
+    float acc = 0.f, mine = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        if (j == lane) mine = acc;
+        acc += __shfl_sync(0xFFFFFFFFu, v, j);
+    }
+    *total = acc;
+    return mine;
+}
+
+// ---------------------------------------------------------------------------
+// Launch parameter blocks (host and device).
+// ---------------------------------------------------------------------------
+enum RowMode : int { kModeVerify = 0, kModeMentor = 1, kModeSample = 2 };
+enum Transform : int { kXfTopK = 1, kXfTopP = 2 };
+
+// One record per (b, k) task, written by the task's cluster.
+struct TaskRec {
+    int32_t flags;  // kRec* bits
+    int32_t token;  // resampled (rejected) or bonus (k = gamma) token, -1 if none
+    float q_x, p_x; // probabilities of the draft token
+    float m_t, s_t; // target row max and sum of exp2((z - m) log2e / T)
+    float m_d, s_d; // draft row max and sum
+};
+
+struct RowParams {
+    const void* target;
+    const void* draft;
+    const int32_t* draft_tokens;
+    int B, gamma, V;
+    int C;            // CTAs per cluster (vocab split)
+    int L;            // elements per CTA slice (multiple of 16)
+    int rows_per_b;   // gamma + 1 (verify / mentor) or P (sample)
+    int mode;         // RowMode
+    int transform;    // Transform bits
+    int top_k;
+    float top_p;
+    float c2;         // log2(e) / T
+    uint64_t seed, offset;
+    uint32_t pos0, purpose;  // sample mode
+    unsigned int wait_limit;
+    int32_t* accepted;
+    int32_t* tokens;
+    int32_t* next_token;
+    int32_t* status;
+    float* probs_dbg;
+    int32_t* sample_out;
+    TaskRec* recs;
+    unsigned int* cnt;
+};
+
+enum ArgmaxMode : int { kArgVerify = 0, kArgTree = 1, kArgSample = 2 };
+
+struct ArgmaxParams {
+    const void* logits;
+    int B, rows_per_b, V;
+    int mode;          // ArgmaxMode
+    int chunk;         // elements per CTA (flattened [rows, V] range)
+    int max_depth;     // tree
+    const int32_t* draft_tokens;  // verify: [B, rows_per_b - 1]
+    const int32_t* node_tokens;   // tree: [B, N]
+    const int32_t* parent;
+    const int32_t* depth;
+    int32_t* out0;  // verify: accepted; tree: accept_len; sample: tokens_out
+    int32_t* out1;  // verify: tokens;   tree: path_nodes
+    int32_t* out2;  // verify: next;     tree: tokens
+    int32_t* out3;  // tree: bonus
+    float* probs_dbg;  // verify: [B, gamma, 2] (q(x), p(x)) of greedy verification
+    int32_t* status;
+    unsigned long long* rowbest;  // [rows] packed (key << 32) | ~index
+    unsigned int* rowbad;         // [rows]
+    unsigned long long* cnt;      // [B] elements processed
+};
+
+struct MentorParams {
+    const void* target;
+    const void* draft;
+    const int32_t* draft_tokens;
+    int B, gamma, V;
+    int bf16;            // logits are bf16 (else fp32)
+    float c2;            // log2(e) / T
+    float inv_t;         // 1 / T
+    float kl_bound;
+    int iters;
+    uint64_t seed, offset;
+    const TaskRec* recs;  // from the row kernel (mentor mode)
+    int32_t* m_flags;     // [B * gamma] lossy decision per task
+    int32_t* m_token;     // [B * gamma] lossy resample per task
+    unsigned int* cnt;    // [B] arrivals
+    uint32_t* keys;       // scratch per slot: [2][V] keys
+    uint32_t* idx;        // scratch per slot: [2][V] indices
+    float* arr;           // scratch per slot: [7][V] sorted arrays
+    int32_t* accepted;
+    int32_t* tokens;
+    int32_t* next_token;
+    int32_t* status;
+    float* alpha_out;
+    float* beta_out;
+    float* probs_dbg;
+};
+
+// Host launchers (defined in the .cu files).
+cudaError_t launch_rows(const RowParams& p, int dtype, int num_tasks, size_t smem,
+                        cudaStream_t stream);
+size_t rows_smem_bytes(int dtype, int L, bool two_rows);
+cudaError_t launch_argmax(const ArgmaxParams& p, int dtype, int grid, cudaStream_t stream);
+cudaError_t launch_mentor(const MentorParams& p, int grid, cudaStream_t stream);
+
+}  // namespace sv
