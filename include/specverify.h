@@ -218,6 +218,34 @@ spec_status spec_sample(const void* logits, spec_dtype dtype, int B, int P, int 
 spec_status spec_philox_uniform(uint64_t seed, uint64_t row0, uint32_t position, uint32_t purpose,
                                 int n, float* out, spec_stream stream);
 
+/* ------------------------------------------------------------------------
+ * spec_verify_noalloc - spec_verify without a workspace argument, for
+ * callers that cannot allocate device memory when they verify (an engine
+ * plugin whose framework owns all device allocations, a server with a
+ * device memory budget fixed at start-up, a C caller without a device
+ * allocator). The pages have no counterpart: this is a deployment variant of
+ * spec_verify, with the same arguments (minus workspace / ws_bytes), the
+ * same kernels and the same outputs.
+ *
+ * Its scratch memory is a fixed array of SPEC_NOALLOC_SCRATCH_BYTES in the
+ * library's device image, held by every GPU that loads the library until the
+ * process exits. Returns SPEC_EINVAL when the call would need more scratch
+ * than that (spec_verify_workspace_size(B, gamma, V, dtype) >
+ * SPEC_NOALLOC_SCRATCH_BYTES). It never calls cudaMalloc, cudaFree or any
+ * allocating routine. The first call on a device looks the array's device
+ * address up (cudaGetSymbolAddress) and should be made before any stream
+ * capture. All calls share the array and it keeps the last call's contents
+ * (each call clears what must start at zero); calls that overlap on the GPU
+ * race on it.
+ * ---------------------------------------------------------------------- */
+enum { SPEC_NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024 };
+
+spec_status spec_verify_noalloc(const void* target, const void* draft, spec_dtype dtype,
+                                const int32_t* draft_tokens, int B, int gamma, int V,
+                                spec_sampling sampling, uint64_t seed, uint64_t offset,
+                                int32_t* accepted, int32_t* tokens, int32_t* next_token,
+                                int32_t* status, float* probs_dbg, spec_stream stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* spec_status_string(spec_status s);
 

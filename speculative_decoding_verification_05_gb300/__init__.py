@@ -34,7 +34,8 @@ EXPORTED = [
     "spec_verify_tree_workspace_size", "spec_verify_tree",
     "spec_verify_mentor_workspace_size", "spec_verify_mentor",
     "spec_sample_workspace_size", "spec_sample",
-    "spec_philox_uniform", "spec_status_string", "spec_last_cuda_error", "spec_version",
+    "spec_philox_uniform", "spec_verify_noalloc", "spec_status_string", "spec_last_cuda_error",
+    "spec_version",
 ]
 
 
@@ -83,6 +84,9 @@ def load_library(path=LIB_PATH):
         lib.spec_sample.argtypes = [_P, _I, _I, _I, _I, SpecSampling, _U64, _U64, ctypes.c_uint32,
                                     ctypes.c_uint32, _P, _P, _P, _SZ, _P]
         lib.spec_sample.restype = _I
+        lib.spec_verify_noalloc.argtypes = [_P, _P, _I, _P, _I, _I, _I, SpecSampling, _U64, _U64,
+                                            _P, _P, _P, _P, _P, _P]
+        lib.spec_verify_noalloc.restype = _I
         lib.spec_philox_uniform.argtypes = [_U64, _U64, ctypes.c_uint32, ctypes.c_uint32, _I, _P, _P]
         lib.spec_philox_uniform.restype = _I
         lib.spec_status_string.argtypes = [_I]

@@ -12,6 +12,7 @@
 
 namespace sv {
 size_t mentor_smem_bytes(int V);
+spec_status note_cuda_error(cudaError_t e);
 }
 
 namespace {
@@ -186,6 +187,9 @@ __global__ void philox_uniform_kernel(uint64_t seed, uint64_t row0, uint32_t pos
 }
 
 }  // namespace
+
+// Records a CUDA error for spec_last_cuda_error (used by other translation units).
+spec_status sv::note_cuda_error(cudaError_t e) { return cuda_fail(e); }
 
 extern "C" {
 
