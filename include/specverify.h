@@ -171,11 +171,14 @@ spec_status spec_verify_tree(const void* target, spec_dtype dtype,
  * Arguments as spec_verify, with temperature > 0 and no top-k / top-p, plus:
  *   kl_bound      D >= 0: bound on KL(q || pi) for the result law pi
  *   bisect_iters  bisection steps on alpha in ]0, 1] (1..SPEC_MAX_BISECT)
- *   alpha_out     [B, gamma] (NULL allowed): -1 where the standard test
- *                 u < min(1, q/p) accepted, 0 where KL(q||p) <= D accepted
- *                 directly, otherwise the bisection's alpha. Computed for
- *                 every position, also after the first rejection.
- *   beta_out      [B, gamma] (NULL allowed): beta for solved positions, else 0
+ *   alpha_out     [B, gamma] (NULL allowed): for the decided positions
+ *                 k <= accepted[b]: -1 where the standard test u < min(1, q/p)
+ *                 accepted, 0 where KL(q||p) <= D accepted directly,
+ *                 otherwise the bisection's alpha. NaN after the first
+ *                 rejection and for sequences with status SPEC_EDATA (those
+ *                 positions are never decided, so nothing is solved there).
+ *   beta_out      [B, gamma] (NULL allowed): beta for solved positions, 0 for
+ *                 the two acceptance codes, NaN where alpha_out is NaN
  * A position that fails the standard test is accepted iff
  * u < min(1, q(x)/(alpha p(x))) with the same u; on rejection the token is
  * drawn from max(0, q/beta - p). The bonus token comes from q_gamma.

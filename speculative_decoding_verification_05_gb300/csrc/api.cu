@@ -2,6 +2,7 @@
 // configuration. Every entry point checks its arguments on the host before
 // touching CUDA, so invalid calls return SPEC_EINVAL with nothing enqueued.
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -11,7 +12,6 @@
 #include "specverify.h"
 
 namespace sv {
-size_t mentor_smem_bytes(int V);
 spec_status note_cuda_error(cudaError_t e);
 }
 
@@ -20,7 +20,6 @@ namespace {
 thread_local char g_cuda_err[256] = "";
 
 constexpr size_t kAlign = 256;
-constexpr int kMentorSlots = 128;
 
 size_t al(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
@@ -54,55 +53,81 @@ bool dtype_ok(spec_dtype d) { return d == SPEC_F32 || d == SPEC_BF16; }
 
 // ---- workspace layouts -----------------------------------------------------
 
+// Segments per row for the row kernel: long rows are split so that a step
+// has about kUnitsWanted work units (dynamic scheduling then balances the SMs),
+// each at least kMinSeg elements and a multiple of 16 elements. Rows with a
+// top-k / top-p transform stay whole (their threshold comes from the whole
+// row in one CTA). Depends only on the shape, so results do not depend on the
+// device's SM count.
+constexpr long long kUnitsWanted = 4096;
+constexpr int kMinSeg = 4096;
+
+void seg_plan(long long rows, int V, bool xf, int* nseg, int* seg_len) {
+    long long n = 1;
+    if (!xf) n = std::max(1LL, std::min((kUnitsWanted + rows - 1) / rows, (long long)(V / kMinSeg)));
+    long long len = ((V + n - 1) / n + 15) & ~15LL;
+    *seg_len = (int)len;
+    *nseg = (int)((V + len - 1) / len);
+}
+
 // Every layout starts with the control region that must be zero when the
-// kernels start (arrival counters, packed per-row argmaxes); each call clears
-// it with one memset, so the workspace may hold anything on entry. Records and
-// scratch follow and are always written before they are read.
-struct LinearWs {
-    size_t cnt, cnt64, rowbest, rowbad, zero_end, recs, total;
+// kernels start (work counters, arrival counters, packed per-row argmaxes);
+// each call clears the part it uses with one memset, so the workspace may
+// hold anything on entry. Records and scratch follow and are always written
+// before they are read.
+struct Ws {
+    size_t work, seq_cnt, row_cnt, row_zero_end;  // row kernel control
+    size_t cnt64, rowbest, rowbad, arg_end;         // argmax control
+    size_t rows, segs, total;
+    int nseg_max;
 };
 
-LinearWs linear_ws(int B, int rows_per_b) {
-    LinearWs w;
+Ws ws_layout(int B, int R, int V) {
+    Ws w;
     size_t o = 0;
-    const size_t rows = (size_t)B * rows_per_b;
-    w.cnt = o;
+    const size_t rows = (size_t)B * R;
+    int seg_len;
+    seg_plan((long long)rows, V, false, &w.nseg_max, &seg_len);
+    w.work = o;
+    o = al(o + 2 * sizeof(unsigned int));
+    w.seq_cnt = o;
     o = al(o + (size_t)B * sizeof(unsigned int));
+    w.row_cnt = o;
+    o = al(o + rows * sizeof(unsigned int));
+    w.row_zero_end = o;
     w.cnt64 = o;
     o = al(o + (size_t)B * sizeof(unsigned long long));
     w.rowbest = o;
     o = al(o + rows * sizeof(unsigned long long));
     w.rowbad = o;
     o = al(o + rows * sizeof(unsigned int));
-    w.zero_end = o;
-    w.recs = o;
-    o = al(o + rows * sizeof(sv::TaskRec));
+    w.arg_end = o;
+    w.rows = o;
+    o = al(o + rows * sizeof(sv::RowRec));
+    w.segs = o;
+    if (w.nseg_max > 1) o = al(o + rows * w.nseg_max * sizeof(sv::SegRec));
     w.total = o;
     return w;
 }
 
-spec_status clear_control(void* ws, const LinearWs& w, cudaStream_t st) {
-    const cudaError_t e = cudaMemsetAsync(ws, 0, w.zero_end, st);
+spec_status clear(void* ws, size_t from, size_t to, cudaStream_t st) {
+    const cudaError_t e = cudaMemsetAsync(reinterpret_cast<char*>(ws) + from, 0, to - from, st);
     return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
 }
 
+constexpr int kMentorSlots = 152;
+
 struct MentorWs {
-    LinearWs lin;
-    size_t mflags, mtok, mcnt, keys, idx, arr, total;
+    Ws lin;
+    size_t keys, idx, arr, total;
     int slots;
 };
 
 MentorWs mentor_ws(int B, int gamma, int V) {
     MentorWs w;
-    w.lin = linear_ws(B, gamma + 1);
+    w.lin = ws_layout(B, 2 * gamma + 1, V);
     size_t o = w.lin.total;
-    const size_t t = (size_t)B * gamma;
-    w.slots = (int)std::min<size_t>(t, kMentorSlots);
-    w.mcnt = w.lin.cnt;  // the row kernel leaves cnt alone in mentor mode
-    w.mflags = o;
-    o = al(o + t * 4);
-    w.mtok = o;
-    o = al(o + t * 4);
+    w.slots = std::min(B, kMentorSlots);
     w.keys = o;
     o = al(o + (size_t)w.slots * 2 * V * 4);
     w.idx = o;
@@ -120,40 +145,26 @@ T* at(void* ws, size_t off) {
 
 // ---- launch configuration ---------------------------------------------------
 
-// Cluster size C and slice length L for the row kernel: the smallest C whose
-// per-CTA shared memory stays within 72 KB (three CTAs per SM), else the
-// smallest C within 200 KB; 0 if V is too large.
-int pick_cluster(int dtype, int V, bool two_rows, int* L, size_t* smem) {
-    for (int pass = 0; pass < 2; ++pass) {
-        const size_t cap = pass == 0 ? 72 * 1024 : 200 * 1024;
-        for (int C = 1; C <= 16; C *= 2) {
-            const int l = (((V + C - 1) / C) + 15) & ~15;
-            if ((long long)l * (C - 1) >= V && C > 1) break;  // last CTA would be empty
-            const size_t sm = sv::rows_smem_bytes(dtype, l, two_rows);
-            if (sm <= cap) {
-                *L = l;
-                *smem = sm;
-                return C;
-            }
-        }
-    }
-    return 0;
-}
-
-spec_status launch_rows_checked(sv::RowParams& p, int dtype, int num_tasks, bool two_rows,
-                                cudaStream_t st) {
-    int L;
-    size_t smem;
-    const int C = pick_cluster(dtype, p.V, two_rows, &L, &smem);
-    if (!C) return SPEC_EINVAL;
-    if ((long long)num_tasks * C > 0x7FFFFFFFLL) return SPEC_EINVAL;
-    p.C = C;
-    p.L = L;
-    const cudaError_t e = sv::launch_rows(p, dtype, num_tasks, smem, st);
+// Fills the row kernel's workspace pointers and segment plan, clears its
+// control region and launches it.
+spec_status run_rows(sv::RowParams& p, int dtype, void* ws, const Ws& w, cudaStream_t st) {
+    seg_plan((long long)p.B * p.rows_per_b, p.V, p.transform != 0, &p.nseg, &p.seg_len);
+    if (p.nseg > w.nseg_max) return SPEC_EINVAL;
+    p.rows = at<sv::RowRec>(ws, w.rows);
+    p.segs = at<sv::SegRec>(ws, w.segs);
+    p.row_cnt = at<unsigned int>(ws, w.row_cnt);
+    p.seq_cnt = at<unsigned int>(ws, w.seq_cnt);
+    p.work = at<unsigned int>(ws, w.work);
+    if (spec_status c = clear(ws, 0, w.row_zero_end, st)) return c;
+    const cudaError_t e = sv::launch_rows(p, dtype, device_sms(), st);
     return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
 }
 
-spec_status launch_argmax_checked(sv::ArgmaxParams& p, int dtype, cudaStream_t st) {
+spec_status launch_argmax_checked(sv::ArgmaxParams& p, int dtype, void* ws, const Ws& w, cudaStream_t st) {
+    p.rowbest = at<unsigned long long>(ws, w.rowbest);
+    p.rowbad = at<unsigned int>(ws, w.rowbad);
+    p.cnt = at<unsigned long long>(ws, w.cnt64);
+    if (spec_status c = clear(ws, w.cnt64, w.arg_end, st)) return c;
     const long long total = (long long)p.B * p.rows_per_b * p.V;
     long long grid = std::min<long long>((long long)device_sms() * 4, (total + 8191) / 8192);
     if (grid < 1) grid = 1;
@@ -209,10 +220,9 @@ const char* spec_status_string(spec_status s) {
 const char* spec_last_cuda_error(void) { return g_cuda_err; }
 
 size_t spec_verify_workspace_size(int B, int gamma, int V, spec_dtype dtype) {
-    (void)V;
     (void)dtype;
-    if (B < 1 || gamma < 1) return 0;
-    return linear_ws(B, gamma + 1).total;
+    if (B < 1 || gamma < 1 || V < 1) return 0;
+    return ws_layout(B, 2 * gamma + 1, V).total;
 }
 
 spec_status spec_verify(const void* target, const void* draft, spec_dtype dtype,
@@ -230,10 +240,10 @@ spec_status spec_verify(const void* target, const void* draft, spec_dtype dtype,
     const int es = esize(dtype);
     if (!aligned(target, es) || (draft && !aligned(draft, es)) || !aligned(workspace, kAlign))
         return SPEC_EINVAL;
-    const LinearWs w = linear_ws(B, gamma + 1);
+    const Ws w = ws_layout(B, 2 * gamma + 1, V);
     if (ws_bytes < w.total) return SPEC_EINVAL;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (spec_status c = clear_control(workspace, w, st)) return c;
+    const int dt = dtype == SPEC_F32 ? 0 : 1;
 
     if (greedy) {
         sv::ArgmaxParams p = {};
@@ -248,10 +258,7 @@ spec_status spec_verify(const void* target, const void* draft, spec_dtype dtype,
         p.out2 = next_token;
         p.probs_dbg = probs_dbg;
         p.status = status;
-        p.rowbest = at<unsigned long long>(workspace, w.rowbest);
-        p.rowbad = at<unsigned int>(workspace, w.rowbad);
-        p.cnt = at<unsigned long long>(workspace, w.cnt64);
-        return launch_argmax_checked(p, dtype == SPEC_F32 ? 0 : 1, st);
+        return launch_argmax_checked(p, dt, workspace, w, st);
     }
     sv::RowParams p = {};
     p.target = target;
@@ -260,7 +267,7 @@ spec_status spec_verify(const void* target, const void* draft, spec_dtype dtype,
     p.B = B;
     p.gamma = gamma;
     p.V = V;
-    p.rows_per_b = gamma + 1;
+    p.rows_per_b = 2 * gamma + 1;
     p.mode = sv::kModeVerify;
     p.transform = transform_bits(sampling, V);
     p.top_k = sampling.top_k;
@@ -268,23 +275,19 @@ spec_status spec_verify(const void* target, const void* draft, spec_dtype dtype,
     p.c2 = kLog2e / sampling.temperature;
     p.seed = seed;
     p.offset = offset;
-    p.wait_limit = 1u << 26;
     p.accepted = accepted;
     p.tokens = tokens;
     p.next_token = next_token;
     p.status = status;
     p.probs_dbg = probs_dbg;
-    p.recs = at<sv::TaskRec>(workspace, w.recs);
-    p.cnt = at<unsigned int>(workspace, w.cnt);
     if (!std::isfinite(p.c2)) return SPEC_EINVAL;
-    return launch_rows_checked(p, dtype == SPEC_F32 ? 0 : 1, B * (gamma + 1), true, st);
+    return run_rows(p, dt, workspace, w, st);
 }
 
 size_t spec_verify_tree_workspace_size(int B, int N, int V, spec_dtype dtype) {
-    (void)V;
     (void)dtype;
-    if (B < 1 || N < 1) return 0;
-    return linear_ws(B, N).total;
+    if (B < 1 || N < 1 || V < 1) return 0;
+    return ws_layout(B, N, V).total;
 }
 
 spec_status spec_verify_tree(const void* target, spec_dtype dtype, const int32_t* node_tokens,
@@ -300,9 +303,8 @@ spec_status spec_verify_tree(const void* target, spec_dtype dtype, const int32_t
         !bonus || !workspace)
         return SPEC_EINVAL;
     if (!aligned(target, esize(dtype)) || !aligned(workspace, kAlign)) return SPEC_EINVAL;
-    const LinearWs w = linear_ws(B, N);
+    const Ws w = ws_layout(B, N, V);
     if (ws_bytes < w.total) return SPEC_EINVAL;
-    if (spec_status c = clear_control(workspace, w, reinterpret_cast<cudaStream_t>(stream))) return c;
     sv::ArgmaxParams p = {};
     p.logits = target;
     p.B = B;
@@ -318,10 +320,8 @@ spec_status spec_verify_tree(const void* target, spec_dtype dtype, const int32_t
     p.out2 = tokens;
     p.out3 = bonus;
     p.status = status;
-    p.rowbest = at<unsigned long long>(workspace, w.rowbest);
-    p.rowbad = at<unsigned int>(workspace, w.rowbad);
-    p.cnt = at<unsigned long long>(workspace, w.cnt64);
-    return launch_argmax_checked(p, dtype == SPEC_F32 ? 0 : 1, reinterpret_cast<cudaStream_t>(stream));
+    return launch_argmax_checked(p, dtype == SPEC_F32 ? 0 : 1, workspace, w,
+                                 reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t spec_verify_mentor_workspace_size(int B, int gamma, int V, spec_dtype dtype) {
@@ -353,7 +353,7 @@ spec_status spec_verify_mentor(const void* target, const void* draft, spec_dtype
     const float c2 = kLog2e / temperature;
     if (!std::isfinite(c2)) return SPEC_EINVAL;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (spec_status c = clear_control(workspace, w.lin, st)) return c;
+    const int dt = dtype == SPEC_F32 ? 0 : 1;
 
     sv::RowParams p = {};
     p.target = target;
@@ -362,24 +362,19 @@ spec_status spec_verify_mentor(const void* target, const void* draft, spec_dtype
     p.B = B;
     p.gamma = gamma;
     p.V = V;
-    p.rows_per_b = gamma + 1;
+    p.rows_per_b = 2 * gamma + 1;
     p.mode = sv::kModeMentor;
     p.transform = 0;
     p.top_p = 1.f;
     p.c2 = c2;
     p.seed = seed;
     p.offset = offset;
-    p.wait_limit = 1u << 26;
-    p.probs_dbg = probs_dbg;
-    p.recs = at<sv::TaskRec>(workspace, w.lin.recs);
-    p.cnt = at<unsigned int>(workspace, w.lin.cnt);
-    spec_status s = launch_rows_checked(p, dtype == SPEC_F32 ? 0 : 1, B * (gamma + 1), true, st);
+    spec_status s = run_rows(p, dt, workspace, w.lin, st);
     if (s != SPEC_OK) return s;
 
     sv::MentorParams m = {};
     m.target = target;
     m.draft = draft;
-    m.draft_tokens = draft_tokens;
     m.B = B;
     m.gamma = gamma;
     m.V = V;
@@ -390,13 +385,11 @@ spec_status spec_verify_mentor(const void* target, const void* draft, spec_dtype
     m.iters = bisect_iters;
     m.seed = seed;
     m.offset = offset;
-    m.recs = at<sv::TaskRec>(workspace, w.lin.recs);
-    m.m_flags = at<int32_t>(workspace, w.mflags);
-    m.m_token = at<int32_t>(workspace, w.mtok);
-    m.cnt = at<unsigned int>(workspace, w.mcnt);
+    m.rows = at<sv::RowRec>(workspace, w.lin.rows);
     m.keys = at<uint32_t>(workspace, w.keys);
     m.idx = at<uint32_t>(workspace, w.idx);
     m.arr = at<float>(workspace, w.arr);
+    m.work = at<unsigned int>(workspace, w.lin.work) + 1;  // cleared with the row kernel's control
     m.accepted = accepted;
     m.tokens = tokens;
     m.next_token = next_token;
@@ -404,15 +397,14 @@ spec_status spec_verify_mentor(const void* target, const void* draft, spec_dtype
     m.alpha_out = alpha_out;
     m.beta_out = beta_out;
     m.probs_dbg = probs_dbg;
-    const cudaError_t e = sv::launch_mentor(m, w.slots, st);
+    const cudaError_t e = sv::launch_mentor(m, std::min(w.slots, device_sms()), st);
     return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
 }
 
 size_t spec_sample_workspace_size(int B, int P, int V, spec_dtype dtype) {
-    (void)V;
     (void)dtype;
-    if (B < 1 || P < 1) return 0;
-    return linear_ws(B, P).total;
+    if (B < 1 || P < 1 || V < 1) return 0;
+    return ws_layout(B, P, V).total;
 }
 
 spec_status spec_sample(const void* logits, spec_dtype dtype, int B, int P, int V,
@@ -423,10 +415,10 @@ spec_status spec_sample(const void* logits, spec_dtype dtype, int B, int P, int 
     if (B < 1 || B > (1 << 24) || P < 1 || P > 1024 || V < 1 || V > SPEC_MAX_V) return SPEC_EINVAL;
     if (!logits || !tokens_out || !workspace) return SPEC_EINVAL;
     if (!aligned(logits, esize(dtype)) || !aligned(workspace, kAlign)) return SPEC_EINVAL;
-    const LinearWs w = linear_ws(B, P);
+    const Ws w = ws_layout(B, P, V);
     if (ws_bytes < w.total) return SPEC_EINVAL;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (spec_status c = clear_control(workspace, w, st)) return c;
+    const int dt = dtype == SPEC_F32 ? 0 : 1;
     if (sampling.temperature == 0.f) {
         sv::ArgmaxParams p = {};
         p.logits = logits;
@@ -436,10 +428,7 @@ spec_status spec_sample(const void* logits, spec_dtype dtype, int B, int P, int 
         p.mode = sv::kArgSample;
         p.out0 = tokens_out;
         p.status = status;
-        p.rowbest = at<unsigned long long>(workspace, w.rowbest);
-        p.rowbad = at<unsigned int>(workspace, w.rowbad);
-        p.cnt = at<unsigned long long>(workspace, w.cnt64);
-        return launch_argmax_checked(p, dtype == SPEC_F32 ? 0 : 1, st);
+        return launch_argmax_checked(p, dt, workspace, w, st);
     }
     if (status) {
         const cudaError_t e = cudaMemsetAsync(status, 0, (size_t)B * sizeof(int32_t), st);
@@ -461,10 +450,9 @@ spec_status spec_sample(const void* logits, spec_dtype dtype, int B, int P, int 
     p.offset = offset;
     p.pos0 = pos0;
     p.purpose = purpose;
-    p.wait_limit = 1u << 26;
     p.status = status;
     p.sample_out = tokens_out;
-    return launch_rows_checked(p, dtype == SPEC_F32 ? 0 : 1, B * P, false, st);
+    return run_rows(p, dt, workspace, w, st);
 }
 
 spec_status spec_philox_uniform(uint64_t seed, uint64_t row0, uint32_t position, uint32_t purpose,

@@ -56,14 +56,6 @@ SV_DEV Best warp_best(Best b) {
     return b;
 }
 
-SV_DEV uint4 ld_stream(const uint4* p) {
-    uint4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
-    return r;
-}
-
 struct SharedA {
     Best red[NW];
     int bad_red[NW];
@@ -101,7 +93,7 @@ SV_DEV void segment(const ArgmaxParams& p, SharedA& s, long long r, int i0, int 
         uint4 v[U];
 #pragma unroll
         for (int u = 0; u < U; ++u)
-            if (j + u * NT < nb) v[u] = ld_stream(vp + j + u * NT);
+            if (j + u * NT < nb) v[u] = ld_stream_v4(vp + j + u * NT);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (j + u * NT < nb) {

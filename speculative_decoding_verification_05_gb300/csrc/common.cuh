@@ -19,10 +19,7 @@ constexpr int kEData = 4;
 constexpr int kETimeout = 3;
 
 // Per-task record flags.
-constexpr int kRecAccept = 1;    // the standard test u < min(1, q/p) accepted
-constexpr int kRecEData = 2;     // bad logits in this task's rows / bad token
-constexpr int kRecTimeout = 4;   // a bounded copy wait gave up
-constexpr int kRecSolved = 8;    // (mentor) the lossy test accepted
+constexpr int kRecEData = 2;     // bad logits in this row, or a draft token out of range
 
 constexpr uint32_t kPurposeAccept = 0;
 constexpr uint32_t kPurposeResample = 1;
@@ -144,6 +141,15 @@ struct VecTraits<bf16_t> {
     }
 };
 
+// Streaming 16-byte global load: read once, do not keep in L1.
+SV_DEV uint4 ld_stream_v4(const uint4* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
 // ---------------------------------------------------------------------------
 // mbarrier + bulk asynchronous copy (TMA engine, non-tensor form).
 // ---------------------------------------------------------------------------
@@ -238,13 +244,22 @@ SV_DEV float warp_seq_exclusive(float v, float* total) {
 enum RowMode : int { kModeVerify = 0, kModeMentor = 1, kModeSample = 2 };
 enum Transform : int { kXfTopK = 1, kXfTopP = 2 };
 
-// One record per (b, k) task, written by the task's cluster.
-struct TaskRec {
-    int32_t flags;  // kRec* bits
-    int32_t token;  // resampled (rejected) or bonus (k = gamma) token, -1 if none
-    float q_x, p_x; // probabilities of the draft token
-    float m_t, s_t; // target row max and sum of exp2((z - m) log2e / T)
-    float m_d, s_d; // draft row max and sum
+// One record per logit row (workspace), written by the CTA that completes the row.
+struct RowRec {
+    float m;      // row maximum
+    float S;      // sum of exp2((z - m) log2e / T) over the row
+    float thr;    // kept set: z >= thr (-inf: the whole row)
+    float Sk;     // kept mass (the normaliser of the row's probabilities)
+    float zx;     // the draft token's logit in this row (rows with a token)
+    int32_t x;    // the draft token (rows with a token), else -1
+    int32_t flags;  // kRecEData
+    int32_t pad;
+};
+
+// Partial statistics of one segment of a long row.
+struct SegRec {
+    float m, s, zx;
+    int32_t flags;
 };
 
 struct RowParams {
@@ -252,9 +267,9 @@ struct RowParams {
     const void* draft;
     const int32_t* draft_tokens;
     int B, gamma, V;
-    int C;            // CTAs per cluster (vocab split)
-    int L;            // elements per CTA slice (multiple of 16)
-    int rows_per_b;   // gamma + 1 (verify / mentor) or P (sample)
+    int rows_per_b;   // 2 gamma + 1 (verify / mentor) or P (sample)
+    int nseg;         // segments per row
+    int seg_len;      // elements per segment (multiple of 16)
     int mode;         // RowMode
     int transform;    // Transform bits
     int top_k;
@@ -262,15 +277,17 @@ struct RowParams {
     float c2;         // log2(e) / T
     uint64_t seed, offset;
     uint32_t pos0, purpose;  // sample mode
-    unsigned int wait_limit;
     int32_t* accepted;
     int32_t* tokens;
     int32_t* next_token;
     int32_t* status;
     float* probs_dbg;
     int32_t* sample_out;
-    TaskRec* recs;
-    unsigned int* cnt;
+    RowRec* rows;           // [B * rows_per_b]
+    SegRec* segs;           // [B * rows_per_b * nseg] (nseg > 1)
+    unsigned int* row_cnt;  // [B * rows_per_b] segment arrivals (nseg > 1)
+    unsigned int* seq_cnt;  // [B] row arrivals
+    unsigned int* work;     // next work unit (zero at launch)
 };
 
 enum ArgmaxMode : int { kArgVerify = 0, kArgTree = 1, kArgSample = 2 };
@@ -299,21 +316,18 @@ struct ArgmaxParams {
 struct MentorParams {
     const void* target;
     const void* draft;
-    const int32_t* draft_tokens;
     int B, gamma, V;
-    int bf16;            // logits are bf16 (else fp32)
-    float c2;            // log2(e) / T
-    float inv_t;         // 1 / T
+    int bf16;             // logits are bf16 (else fp32)
+    float c2;             // log2(e) / T
+    float inv_t;          // 1 / T
     float kl_bound;
     int iters;
     uint64_t seed, offset;
-    const TaskRec* recs;  // from the row kernel (mentor mode)
-    int32_t* m_flags;     // [B * gamma] lossy decision per task
-    int32_t* m_token;     // [B * gamma] lossy resample per task
-    unsigned int* cnt;    // [B] arrivals
+    const RowRec* rows;   // from the row kernel (mentor mode)
     uint32_t* keys;       // scratch per slot: [2][V] keys
     uint32_t* idx;        // scratch per slot: [2][V] indices
     float* arr;           // scratch per slot: [7][V] sorted arrays
+    unsigned int* work;   // next sequence (zero at launch)
     int32_t* accepted;
     int32_t* tokens;
     int32_t* next_token;
@@ -324,9 +338,8 @@ struct MentorParams {
 };
 
 // Host launchers (defined in the .cu files).
-cudaError_t launch_rows(const RowParams& p, int dtype, int num_tasks, size_t smem,
-                        cudaStream_t stream);
-size_t rows_smem_bytes(int dtype, int L, bool two_rows);
+// Persistent row kernel on up to `sms` x (resident CTAs per SM) CTAs.
+cudaError_t launch_rows(const RowParams& p, int dtype, int sms, cudaStream_t stream);
 cudaError_t launch_argmax(const ArgmaxParams& p, int dtype, int grid, cudaStream_t stream);
 cudaError_t launch_mentor(const MentorParams& p, int grid, cudaStream_t stream);
 
