@@ -2,16 +2,20 @@
 //
 // Work units are the logit rows of all sequences (2*gamma + 1 per sequence in
 // verification: target rows k = 0..gamma, draft rows k = 0..gamma-1; P rows
-// in sampling), each cut into `nseg` segments when rows are very long. CTAs
-// take units from a global counter (dynamic scheduling, so a step of any
+// in sampling), each cut into `nseg` segments when rows are long and few.
+// CTAs take units from a global counter (dynamic scheduling, so a step of any
 // shape balances over the SMs) and stream each unit once from HBM with
-// 16-byte loads, keeping an online maximum and sum of exp2((z - m) log2e / T)
-// per thread ("Accelerating Large Language Model Decoding with Speculative
-// Sampling", "与标准采样方法的兼容性": the probabilities a transform acts on).
-// The last segment of a row to finish turns the partial sums into the row's
-// record (maximum, sum, top-k / top-p threshold and kept mass); the last row of
-// a sequence to finish resolves the sequence (no thread ever waits for
-// another CTA):
+// 16-byte loads. Per row the CTA computes the maximum m and
+// S = sum_i exp2((z_i - m) log2e / T), the normaliser of the probabilities a
+// transform acts on ("Accelerating Large Language Model Decoding with
+// Speculative Sampling", "与标准采样方法的兼容性"). The exponentials are taken
+// against a fixed reference, the maximum of the first group of vectors the
+// CTA loads (one block reduction), so the loop needs no running rescale; S is
+// moved to m once at the end (a row whose sum overflows against the
+// reference is summed again against m). The last segment of a row to finish
+// writes the row's record (maximum, sum, top-k / top-p threshold and kept
+// mass); the last row of a sequence to finish resolves the sequence (no
+// thread ever waits for another CTA):
 //
 //   * acceptance left to right, u_k < min(1, q(x_k)/p(x_k)), stopping at the
 //     first rejection n ("改进的拒绝采样");
@@ -19,16 +23,20 @@
 //     token from q_gamma when all gamma were accepted. The draw re-reads that
 //     one row pair (fresh in L2) with the CTA-wide inverse CDF of draw.cuh.
 //
-// Top-p (fast path): while streaming, keys within kWin + 1 octaves of a
-// CTA-wide running maximum are kept in shared memory; under the final maximum
-// they contain every key whose mass is within 2^-kWin of the largest (an upper
-// set in key order). A radix select over those keys with fixed-point masses
-// (mass * 2^40, exact integers, so the result does not depend on summation
-// order) gives tau, the largest key whose mass from the top reaches
-// top_p * S, when the collected mass reaches that target. Top-k, rows whose
-// crossing lies deeper and segmented rows take the exact slow path: the same
-// radix select over the row read again from global memory, so both paths
-// return the same tau and kept mass.
+// Thresholds (top-k, top-p). While streaming, each thread stores in its own
+// shared-memory slots the logits above (reference - (kWin + 1) octaves); they
+// form an upper set in key order that holds every logit whose mass is within
+// 2^-kWin of the largest. tau is the largest key whose weight from the top (a
+// count for top-k, the fixed-point mass * 2^40 for top-p: exact integers, so
+// independent of summation order) reaches the target. bf16 rows count the
+// stored keys per distinct bf16 value (a histogram over the ordinals of the
+// values just below the reference) and scan it once; fp32 rows use a
+// histogram over a monotone function of the logit (1/16 octave bins near the
+// maximum) and compare the keys of the crossing bin exactly. When the stored
+// keys do not decide the threshold (a thread's slots overflowed, the crossing
+// lies deeper, or the row is split into segments) the same selection runs
+// over the row read again from global memory, so every path gives the same
+// tau and kept mass.
 
 #include <algorithm>
 
@@ -41,24 +49,41 @@ namespace {
 constexpr int NT = kDrawNT;
 constexpr int NW = NT / 32;
 constexpr int kMaxRows = 2 * 255 + 1;  // rows per sequence (verification, gamma <= 255)
-constexpr int kWin = 13;               // fast top-p: keys within 2^-kWin of the row max
-constexpr int kHeadCap = 4096;         // fast top-p: keys kept per row
+constexpr int kU = 4;                  // 16-byte vectors in flight per thread
+constexpr int kWin = 13;               // stored keys: within 2^-kWin of the row max (plus one octave)
+constexpr int kSlotBytes = 128;        // key slots per thread, in bytes
+constexpr int kSel = 256;              // keys compared exactly inside the crossing bin
+constexpr int kOrd = 2048;             // bf16 ordinal histogram: bins
+constexpr int kOrdAbove = 256;         //   of which above the reference value
 constexpr float kFx = 1099511627776.0f;  // 2^40: masses >= 2^-17 are exact integers
 
+struct GenSel {
+    unsigned hcnt[256];               // selection histogram: counts
+    unsigned long long hist[256];     //                      fixed-point masses
+    uint32_t skey[kSel];              // keys of the crossing bin
+    unsigned long long smass[kSel];
+};
+
 struct Shared {
-    int unit;
+    int next[2];                      // prefetched work units
     int last;
+    unsigned hmax;                    // key of the first group's maximum
+    int ovf;                          // a thread's key slots overflowed
+    int nsel;
     float red_m[NW], red_s[NW];
     unsigned long long ured[NW + 2];
+    unsigned long long ured2[NW];
     int bi[8];
     float bf[8];
-    // fast top-p
-    int nhead;
-    unsigned hmax;                 // key of the CTA-wide running maximum
-    uint32_t head[kHeadCap];
-    unsigned long long hist[256];  // radix select
-    // sequence resolve
-    RowRec rec[kMaxRows];
+    unsigned short hn[NT];            // stored keys per thread
+    union {
+        GenSel g;
+        unsigned ocnt[kOrd];
+    } h;
+    union {
+        unsigned char slots[kSlotBytes * NT];  // slot c of thread t at element c * NT + t
+        RowRec rec[kMaxRows];                  // sequence resolve (after the row's threshold)
+    } u;
     DrawShared draw;
 };
 
@@ -68,7 +93,16 @@ SV_DEV float max_nan(float a, float b) {
     return r;
 }
 
-// Online (max, sum of exp2((z - max) c)) of one thread.
+SV_DEV uint32_t bmax2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+SV_DEV float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+SV_DEV float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Online (max, sum of exp2((z - max) c)) of a segment.
 struct Online {
     float m;
     float s;
@@ -85,138 +119,231 @@ SV_DEV void merge(Online& a, float bm, float bs, float c2) {
     }
 }
 
-template <typename E>
-struct Streamer {
-    using T = VecTraits<E>;
-    float c2;
-    float wc;      // collection window in logits: (kWin + 1) / c2
-    bool collect;  // top-p head collection
-    Shared* s;
+// --- streaming core ------------------------------------------------------------
 
-    SV_DEV void add_vec(Online& o, const float* x, int n, float hint) const {
-        float vm = x[0];
-#pragma unroll
-        for (int e = 1; e < T::kN; ++e)
-            if (e < n) vm = max_nan(vm, x[e]);
-        if (!(vm <= o.m)) {
-            o.s = (o.m == -INFINITY) ? 0.f : o.s * ex2((o.m - vm) * c2);
-            o.m = vm;
+// Stores the raw bits of logits above `cut` in the thread's slots.
+template <typename K>
+struct Collect {
+    static constexpr int kPer = kSlotBytes / (int)sizeof(K);
+    K* base;  // slot 0 of this thread; slot c at base[c * NT]
+    float cut;
+    int hc;
+    SV_DEV void operator()(float x, uint32_t raw) {
+        if (x > cut) {
+            if (hc < kPer) base[hc * NT] = (K)raw;
+            ++hc;
         }
-        if (o.m > -INFINITY || o.m != o.m) {
-            const float mc = o.m * c2;
-            const float cut = fmaxf(o.m, hint) - wc;
-#pragma unroll
-            for (int e = 0; e < T::kN; ++e) {
-                if (e < n) {
-                    o.s += ex2(fmaf(x[e], c2, -mc));
-                    if (collect && x[e] > cut) {
-                        const int slot = atomicAdd(&s->nhead, 1);
-                        if (slot < kHeadCap) s->head[slot] = f32_key(x[e]);
-                    }
-                }
-            }
-        }
-    }
-
-    SV_DEV float shared_max() const { return key_to_f32(*reinterpret_cast<volatile unsigned*>(&s->hmax)); }
-
-    // Streams elements [i0, i1) of row; returns this thread's online state.
-    // Every thread of the CTA must call it (one barrier seeds the hint).
-    SV_DEV Online run(const E* row, int i0, int i1) const {
-        constexpr int es = sizeof(E);
-        constexpr int VE = T::kN;
-        constexpr int U = 4;
-        Online o{-INFINITY, 0.f};
-        const int tid = threadIdx.x;
-        const uintptr_t a = (uintptr_t)(row + i0);
-        const int head = min(i1 - i0, (int)(((16 - (a & 15)) & 15) / es));
-        const int base = i0 + head;
-        const int nb = (i1 - base) / VE;
-        const uint4* vp = reinterpret_cast<const uint4*>(row + base);
-        // first group of vectors; its maximum seeds the collection hint
-        uint4 v[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (tid + u * NT < nb) v[u] = ld_stream_v4(vp + tid + u * NT);
-        float hint = -INFINITY;
-        if (collect) {
-            float vm = -INFINITY;
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (tid + u * NT < nb) {
-                    float x[VE];
-                    T::unpack(v[u], x);
-#pragma unroll
-                    for (int e = 0; e < VE; ++e) vm = fmaxf(vm, x[e]);
-                }
-            }
-            for (int o2 = 16; o2; o2 >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xFFFFFFFFu, vm, o2));
-            if ((tid & 31) == 0 && vm > -INFINITY) atomicMax(&s->hmax, f32_key(vm));
-            __syncthreads();
-            hint = shared_max();
-        }
-        if (tid < head) {
-            float x[VE];
-            x[0] = T::load1(row + i0 + tid);
-            add_vec(o, x, 1, hint);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (tid + u * NT < nb) {
-                float x[VE];
-                T::unpack(v[u], x);
-                add_vec(o, x, VE, hint);
-            }
-        }
-        for (int j = tid + NT * U; j < nb; j += NT * U) {
-            if (collect) {
-                if (o.m > hint) atomicMax(&s->hmax, f32_key(o.m));
-                hint = fmaxf(hint, shared_max());
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (j + u * NT < nb) v[u] = ld_stream_v4(vp + j + u * NT);
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (j + u * NT < nb) {
-                    float x[VE];
-                    T::unpack(v[u], x);
-                    add_vec(o, x, VE, hint);
-                }
-            }
-        }
-        const int t = base + nb * VE + tid;
-        if (t < i1) {
-            float x[VE];
-            x[0] = T::load1(row + t);
-            add_vec(o, x, 1, hint);
-        }
-        return o;
     }
 };
 
-// Block-wide merge of the threads' online states; the result in every thread.
-// The tree order is fixed, so the result does not depend on timing.
-SV_DEV Online block_merge(Shared& s, Online o, float c2) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+template <typename E>
+struct Core;
+
+// bf16: running maximum on packed pairs, exponentials on f32 pairs.
+template <>
+struct Core<bf16_t> {
+    static constexpr int VE = 8;
+    using Key = uint16_t;
+    struct St {
+        uint32_t pm;
+        float2 s0, s1;
+    };
+    SV_DEV static St init() { return St{0xFF80FF80u, make_float2(0.f, 0.f), make_float2(0.f, 0.f)}; }
+    SV_DEV static float vmax(const uint4& v) {
+        const uint32_t m = bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w));
+        return fmaxf(bf_lo(m), bf_hi(m));
+    }
+    template <bool COL, typename C>
+    SV_DEV static void vec(St& st, const uint4& v, float2 c2v, float2 nr2, C& col) {
+        st.pm = bmax2(st.pm, bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w)));
+        float2 a0 = make_float2(bf_lo(v.x), bf_hi(v.x)), a1 = make_float2(bf_lo(v.y), bf_hi(v.y));
+        float2 a2 = make_float2(bf_lo(v.z), bf_hi(v.z)), a3 = make_float2(bf_lo(v.w), bf_hi(v.w));
+        if (COL) {
+            col(a0.x, v.x & 0xFFFFu);
+            col(a0.y, v.x >> 16);
+            col(a1.x, v.y & 0xFFFFu);
+            col(a1.y, v.y >> 16);
+            col(a2.x, v.z & 0xFFFFu);
+            col(a2.y, v.z >> 16);
+            col(a3.x, v.w & 0xFFFFu);
+            col(a3.y, v.w >> 16);
+        }
+        a0 = __ffma2_rn(a0, c2v, nr2);
+        a1 = __ffma2_rn(a1, c2v, nr2);
+        a2 = __ffma2_rn(a2, c2v, nr2);
+        a3 = __ffma2_rn(a3, c2v, nr2);
+        a0.x = ex2(a0.x);
+        a0.y = ex2(a0.y);
+        a1.x = ex2(a1.x);
+        a1.y = ex2(a1.y);
+        a2.x = ex2(a2.x);
+        a2.y = ex2(a2.y);
+        a3.x = ex2(a3.x);
+        a3.y = ex2(a3.y);
+        st.s0 = __fadd2_rn(st.s0, a0);
+        st.s1 = __fadd2_rn(st.s1, a1);
+        st.s0 = __fadd2_rn(st.s0, a2);
+        st.s1 = __fadd2_rn(st.s1, a3);
+    }
+    template <bool COL, typename C>
+    SV_DEV static void one(St& st, const bf16_t* p, float c2, float nref, C& col) {
+        const uint32_t raw = __ldg(reinterpret_cast<const unsigned short*>(p));
+        st.pm = bmax2(st.pm, raw | (raw << 16));
+        const float x = __uint_as_float(raw << 16);
+        if (COL) col(x, raw);
+        st.s0.x += ex2(fmaf(x, c2, nref));
+    }
+    SV_DEV static float maxof(const St& st) { return max_nan(bf_lo(st.pm), bf_hi(st.pm)); }
+    SV_DEV static float sumof(const St& st) {
+        const float2 t = __fadd2_rn(st.s0, st.s1);
+        return t.x + t.y;
+    }
+};
+
+// fp32: exponentials on pairs.
+template <>
+struct Core<float> {
+    static constexpr int VE = 4;
+    using Key = uint32_t;
+    struct St {
+        float pm;
+        float2 s0, s1;
+    };
+    SV_DEV static St init() { return St{-INFINITY, make_float2(0.f, 0.f), make_float2(0.f, 0.f)}; }
+    SV_DEV static float vmax(const uint4& v) {
+        return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+                     fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+    }
+    template <bool COL, typename C>
+    SV_DEV static void vec(St& st, const uint4& v, float2 c2v, float2 nr2, C& col) {
+        float2 a0 = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+        float2 a1 = make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+        st.pm = max_nan(st.pm, max_nan(max_nan(a0.x, a0.y), max_nan(a1.x, a1.y)));
+        if (COL) {
+            col(a0.x, v.x);
+            col(a0.y, v.y);
+            col(a1.x, v.z);
+            col(a1.y, v.w);
+        }
+        a0 = __ffma2_rn(a0, c2v, nr2);
+        a1 = __ffma2_rn(a1, c2v, nr2);
+        a0.x = ex2(a0.x);
+        a0.y = ex2(a0.y);
+        a1.x = ex2(a1.x);
+        a1.y = ex2(a1.y);
+        st.s0 = __fadd2_rn(st.s0, a0);
+        st.s1 = __fadd2_rn(st.s1, a1);
+    }
+    template <bool COL, typename C>
+    SV_DEV static void one(St& st, const float* p, float c2, float nref, C& col) {
+        const float x = __ldg(p);
+        st.pm = max_nan(st.pm, x);
+        if (COL) col(x, __float_as_uint(x));
+        st.s0.x += ex2(fmaf(x, c2, nref));
+    }
+    SV_DEV static float maxof(const St& st) { return st.pm; }
+    SV_DEV static float sumof(const St& st) {
+        const float2 t = __fadd2_rn(st.s0, st.s1);
+        return t.x + t.y;
+    }
+};
+
+struct RowStats {
+    float m;     // row (segment) maximum, NaN if any logit is NaN
+    float sref;  // sum of exp2((z - ref) c2)
+    float ref;
+};
+
+// Streams elements [i0, i1) of row: maximum and sum against a fixed
+// reference (the first group's maximum when ref_in is NaN). Every thread of
+// the CTA must call it; all return the same statistics. With COL, logits
+// above ref - wc go to the thread's key slots.
+template <typename E, bool COL>
+__device__ __noinline__ RowStats stream_row(Shared& s, const E* row, int i0, int i1, float c2, float wc,
+                                            float ref_in) {
+    using C = Core<E>;
+    constexpr int VE = C::VE;
+    constexpr int es = sizeof(E);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uintptr_t addr = (uintptr_t)(row + i0);
+    const int head = min(i1 - i0, (int)(((16 - (addr & 15)) & 15) / es));
+    const int base = i0 + head;
+    const int nb = (i1 - base) / VE;
+    const uint4* vp = reinterpret_cast<const uint4*>(row + base);
+    uint4 v[kU];
 #pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const float bm = __shfl_xor_sync(0xFFFFFFFFu, o.m, d);
-        const float bs = __shfl_xor_sync(0xFFFFFFFFu, o.s, d);
-        // the lower lane's state absorbs the higher lane's, in both lanes
-        Online lo = (lane & d) ? Online{bm, bs} : o;
-        const float hm = (lane & d) ? o.m : bm, hs = (lane & d) ? o.s : bs;
-        merge(lo, hm, hs, c2);
-        o = lo;
+    for (int u = 0; u < kU; ++u)
+        if (tid + u * NT < nb) v[u] = ld_stream_v4(vp + tid + u * NT);
+    float ref = ref_in;
+    if (ref_in != ref_in) {
+        float vm = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+            if (tid + u * NT < nb) vm = fmaxf(vm, C::vmax(v[u]));
+        for (int o = 16; o; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xFFFFFFFFu, vm, o));
+        if (lane == 0 && vm > -INFINITY) atomicMax(&s.hmax, f32_key(vm));
+        __syncthreads();
+        ref = key_to_f32(s.hmax);
+        if (!(ref > -INFINITY && ref < INFINITY)) ref = 0.f;
+    }
+    const float nref = -(ref * c2);
+    const float2 c2v = make_float2(c2, c2), nr2 = make_float2(nref, nref);
+    typename C::St st = C::init();
+    using K = typename C::Key;
+    Collect<K> col{reinterpret_cast<K*>(s.u.slots) + tid, ref - wc, 0};
+    if (tid < head) C::template one<COL>(st, row + i0 + tid, c2, nref, col);
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+        if (tid + u * NT < nb) C::template vec<COL>(st, v[u], c2v, nr2, col);
+    for (int j = tid + NT * kU; j < nb; j += NT * kU) {
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+            if (j + u * NT < nb) v[u] = ld_stream_v4(vp + j + u * NT);
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+            if (j + u * NT < nb) C::template vec<COL>(st, v[u], c2v, nr2, col);
+    }
+    const int t = base + nb * VE + tid;
+    if (t < i1) C::template one<COL>(st, row + t, c2, nref, col);
+    if (COL) {
+        s.hn[tid] = (unsigned short)min(col.hc, Collect<K>::kPer);
+        if (col.hc > Collect<K>::kPer) s.ovf = 1;
+    }
+    // block reduction: maximum (NaN-propagating), sum in a fixed order
+    float tm = C::maxof(st), ts = C::sumof(st);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        tm = max_nan(tm, __shfl_xor_sync(0xFFFFFFFFu, tm, o));
+        ts += __shfl_xor_sync(0xFFFFFFFFu, ts, o);
     }
     if (lane == 0) {
-        s.red_m[warp] = o.m;
-        s.red_s[warp] = o.s;
+        s.red_m[warp] = tm;
+        s.red_s[warp] = ts;
     }
     __syncthreads();
-    Online r{s.red_m[0], s.red_s[0]};
-    for (int w = 1; w < NW; ++w) merge(r, s.red_m[w], s.red_s[w], c2);
+    RowStats r{s.red_m[0], s.red_s[0], ref};
+    for (int w = 1; w < NW; ++w) {
+        r.m = max_nan(r.m, s.red_m[w]);
+        r.sref += s.red_s[w];
+    }
     __syncthreads();
+    return r;
+}
+
+// (m, S) of elements [i0, i1) with S against m: S = sref 2^((ref - m) c2),
+// summed again against m when the sum against the reference left the fp32
+// range. Every thread of the CTA must call it.
+template <typename E, bool COL>
+SV_DEV RowStats row_stats(Shared& s, const E* row, int i0, int i1, float c2, float wc) {
+    RowStats r = stream_row<E, COL>(s, row, i0, i1, c2, wc, NAN);
+    if (r.m > -INFINITY && r.m < INFINITY) {
+        if (r.sref > 0.f && r.sref <= 3.0e38f) {
+            r.sref *= ex2((r.ref - r.m) * c2);
+        } else {
+            const RowStats q = stream_row<E, false>(s, row, i0, i1, c2, wc, r.m);
+            r.sref = q.sref;
+        }
+    }
     return r;
 }
 
@@ -249,46 +376,96 @@ SV_DEV RowRef<E> row_ref(const RowParams& p, int b, int r) {
 
 // --- exact thresholds ------------------------------------------------------
 
-SV_DEV unsigned long long fx_mass(float z, float c2, float mc) {
-    return __float2ull_rz(ex2(fmaf(z, c2, -mc)) * kFx);
-}
+SV_DEV unsigned long long fx_of(float a) { return __float2ull_rz(ex2(a) * kFx); }
 
 // The top-p target top_p * (kept mass) in fixed point; both paths use it.
 SV_DEV unsigned long long top_p_target(float top_p, unsigned long long kept) {
-    return (unsigned long long)(top_p * (float)kept);
+    const unsigned long long t = (unsigned long long)(top_p * (float)kept);
+    return t ? t : 1ull;
 }
 
-// Radix selection (8-bit digits, exact integer histograms) over n items given
-// by src(i, key, w) -> valid: the largest key tau with W(key >= tau) >= target
-// (W the sum of the valid items' w). Returns whether the valid items' total
-// reaches the target; with *tau_out and *w_out = W(key >= tau) when it does,
-// else the smallest key present and the total. Every thread returns the same.
-// npass = 2 suffices for keys of bf16 values (their low 16 bits are fixed by
-// the sign).
-template <typename Src>
-SV_DEV bool radix_select(Shared& s, const Src& src, int n, int npass, unsigned long long target,
-                         uint32_t* tau_out, unsigned long long* w_out) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// Bin of a = (z - m) log2e / T <= 0, non-increasing in z: 1/16 octave down to
+// 12 octaves, then 1 octave down to 60, then 8 octaves down to 180, then the
+// rest (and -inf).
+SV_DEV int abin(float a) {
+    const float t = -a;
+    if (t < 12.f) return max(0, (int)(t * 16.f));
+    if (t < 60.f) return 192 + (int)(t - 12.f);
+    if (t < 180.f) return 240 + (int)((t - 60.f) * 0.125f);
+    return 255;
+}
+
+SV_DEV unsigned long long block_sum_u64(Shared& s, unsigned long long v) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    if (lane == 0) s.ured[warp] = v;
+    __syncthreads();
+    unsigned long long t = 0ull;
+    for (int w = 0; w < NW; ++w) t += s.ured[w];
+    __syncthreads();
+    return t;
+}
+
+SV_DEV uint32_t block_max_u32(Shared& s, uint32_t v) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = __reduce_max_sync(0xFFFFFFFFu, v);
+    if (lane == 0) s.ured[warp] = v;
+    __syncthreads();
+    uint32_t t = 0u;
+    for (int w = 0; w < NW; ++w) t = max(t, (uint32_t)s.ured[w]);
+    __syncthreads();
+    return t;
+}
+
+// Histogram add with the lanes of a warp that hit the same bin combined into
+// one atomic per bin. Every lane of the warp must call it (v: item valid).
+SV_DEV void hist_add(Shared& s, bool v, int bin, unsigned long long w) {
+    const unsigned act = __ballot_sync(0xFFFFFFFFu, v);
+    if (v) {
+        const unsigned peers = __match_any_sync(act, bin);
+        const unsigned lo = __reduce_add_sync(peers, (unsigned)(w & 0x1FFFFFull));
+        const unsigned hi = __reduce_add_sync(peers, (unsigned)(w >> 21));  // w < 2^41
+        if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) {
+            atomicAdd(&s.h.g.hist[bin], ((unsigned long long)hi << 21) + lo);
+            atomicAdd(&s.h.g.hcnt[bin], (unsigned)__popc(peers));
+        }
+    }
+}
+
+struct Sel {
+    uint32_t tau;                 // selected key
+    unsigned long long cnt, mass; // count and fixed-point mass of the items with key >= tau
+    bool reach;                   // the items' total reached the target
+};
+
+// Radix selection (8-bit digits, exact integer histograms) restricted to the
+// items accepted by `keep`, starting above weight A0: the largest key tau with
+// A0 + W(key >= tau) >= target. npass = 2 suffices for keys of bf16 values.
+template <typename Each, typename Keep>
+SV_DEV uint32_t radix_select(Shared& s, const Each& each, const Keep& keep, int npass, bool by_count,
+                             unsigned long long A0, unsigned long long target) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t prefix = 0;
-    unsigned long long A = 0ull, wsel = 0ull;
-    bool reach = true;
+    unsigned long long A = A0;
     for (int pass = 0; pass < npass; ++pass) {
         const int shift = 24 - 8 * pass;
-        for (int i = tid; i < 256; i += NT) s.hist[i] = 0ull;
-        __syncthreads();
-        for (int i = tid; i < n; i += NT) {
-            uint32_t key;
-            unsigned long long w;
-            if (src(i, key, w) && (pass == 0 || (key >> (shift + 8)) == (prefix >> (shift + 8))))
-                atomicAdd(&s.hist[(key >> shift) & 255u], w);
+        for (int i = threadIdx.x; i < 256; i += NT) {
+            s.h.g.hist[i] = 0ull;
+            s.h.g.hcnt[i] = 0u;
         }
         __syncthreads();
+        each([&](bool v, uint32_t key, float a) {
+            v = v && keep(key, a) && (pass == 0 || (key >> (shift + 8)) == (prefix >> (shift + 8)));
+            hist_add(s, v, v ? (int)((key >> shift) & 255u) : 0, v && !by_count ? fx_of(a) : 0ull);
+        });
+        __syncthreads();
         if (warp == 0) {
-            // lane l owns bins 255 - 8l .. 248 - 8l (descending)
+            // lane l owns digits 255 - 8l .. 248 - 8l (descending keys)
             unsigned long long h[8], L = 0ull;
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
-                h[t] = s.hist[255 - 8 * lane - t];
+                const int d = 255 - 8 * lane - t;
+                h[t] = by_count ? (unsigned long long)s.h.g.hcnt[d] : s.h.g.hist[d];
                 L += h[t];
             }
             unsigned long long P = L;
@@ -297,115 +474,335 @@ SV_DEV bool radix_select(Shared& s, const Src& src, int n, int npass, unsigned l
                 const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, P, d);
                 if (lane >= d) P += y;
             }
-            const unsigned long long total = __shfl_sync(0xFFFFFFFFu, P, 31);
-            const bool ok = A + total >= target;
             unsigned long long cum = A + (P - L), above = 0ull;
-            int dl = -1;
+            int dl = -1, lastnz = -1;
+            unsigned long long above_last = 0ull;
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
-                if (ok) {
-                    if (dl < 0 && h[t] > 0ull && cum + h[t] >= target) {
-                        dl = t;
-                        above = cum;
-                    }
-                } else if (h[t] > 0ull) {  // the lowest non-empty bin
+                if (dl < 0 && h[t] > 0ull && cum + h[t] >= target) {
                     dl = t;
                     above = cum;
                 }
+                if (h[t] > 0ull) {
+                    lastnz = t;
+                    above_last = cum;
+                }
                 cum += h[t];
             }
-            const unsigned m = __ballot_sync(0xFFFFFFFFu, dl >= 0);
-            const int src_lane = m ? (ok ? __ffs(m) - 1 : 31 - __clz(m)) : 0;
-            if (lane == src_lane) {
-                s.bi[1] = dl >= 0 ? 255 - 8 * lane - dl : 0;
-                s.ured[NW] = dl >= 0 ? above : A;
-                s.ured[NW + 1] = dl >= 0 ? above + h[dl] : A;
-                s.bi[2] = ok;
+            const unsigned mf = __ballot_sync(0xFFFFFFFFu, dl >= 0);
+            const unsigned ml = __ballot_sync(0xFFFFFFFFu, lastnz >= 0);
+            // the crossing digit, else (target not reached) the lowest non-empty digit
+            const int src = mf ? __ffs(mf) - 1 : (ml ? 31 - __clz(ml) : 0);
+            if (lane == src) {
+                const int t = mf ? dl : lastnz;
+                s.bi[1] = t >= 0 ? 255 - 8 * lane - t : 0;
+                s.ured[NW] = t >= 0 ? (mf ? above : above_last) : A;
             }
         }
         __syncthreads();
         prefix |= (uint32_t)s.bi[1] << shift;
         A = s.ured[NW];
-        wsel = s.ured[NW + 1];
-        if (pass == 0) reach = s.bi[2] != 0;
         __syncthreads();
     }
     if (npass == 2) prefix |= (prefix & 0x80000000u) ? 0u : 0xFFFFu;
-    *tau_out = prefix;
-    *w_out = wsel;
-    return reach;
+    return prefix;
 }
 
-// Fast top-p from the collected keys; false if the list overflowed or the
-// crossing lies below the collected keys. Every thread returns the same value.
-SV_DEV bool fast_top_p(Shared& s, const RowParams& p, float m, float S, int npass, float* thr, float* sk) {
-    const int nh = s.nhead;
-    if (nh > kHeadCap) return false;
-    const float mc = m * p.c2, c2 = p.c2;
-    const unsigned long long target = top_p_target(p.top_p, (unsigned long long)(S * kFx));
-    const uint32_t* head = s.head;
-    auto src = [&](int i, uint32_t& key, unsigned long long& w) {
-        key = head[i];
-        const float a = fmaf(key_to_f32(key), c2, -mc);
-        w = __float2ull_rz(ex2(a) * kFx);
-        return a > -(float)kWin;
-    };
-    uint32_t tau;
-    unsigned long long kept;
-    if (!radix_select(s, src, nh, npass, target, &tau, &kept)) return false;
-    *thr = key_to_f32(tau);
+// Exact weighted selection over the items of `each` with key >= floor_key:
+// tau = the largest key with W(key >= tau) >= target, W a count (by_count) or
+// the fixed-point mass. Every thread returns the same result. Unreached
+// targets return reach = false (tau and the sums are then unspecified).
+template <typename Each>
+SV_DEV Sel select(Shared& s, const Each& each, int npass, bool by_count, uint32_t floor_key,
+                  unsigned long long target) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < 256; i += NT) {
+        s.h.g.hist[i] = 0ull;
+        s.h.g.hcnt[i] = 0u;
+    }
+    if (tid == 0) s.nsel = 0;
+    __syncthreads();
+    each([&](bool v, uint32_t key, float a) {
+        v = v && key >= floor_key;
+        hist_add(s, v, v ? abin(a) : 0, v ? fx_of(a) : 0ull);
+    });
+    __syncthreads();
+    if (warp == 0) {
+        // lane l owns bins 8l .. 8l + 7 (descending keys)
+        unsigned long long h[8], L = 0ull;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            h[t] = by_count ? (unsigned long long)s.h.g.hcnt[8 * lane + t] : s.h.g.hist[8 * lane + t];
+            L += h[t];
+        }
+        unsigned long long P = L;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, P, d);
+            if (lane >= d) P += y;
+        }
+        const bool reach = __shfl_sync(0xFFFFFFFFu, P, 31) >= target;
+        unsigned long long cum = P - L;
+        int dl = -1;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            if (dl < 0 && h[t] > 0ull && cum + h[t] >= target) dl = t;
+            cum += h[t];
+        }
+        const unsigned mf = __ballot_sync(0xFFFFFFFFu, dl >= 0);
+        const int c = mf ? 8 * (__ffs(mf) - 1) + __shfl_sync(0xFFFFFFFFu, dl, __ffs(mf) - 1) : 0;
+        // weights of the bins above c: count, mass
+        unsigned long long ac = 0ull, am = 0ull;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            if (8 * lane + t < c) {
+                ac += s.h.g.hcnt[8 * lane + t];
+                am += s.h.g.hist[8 * lane + t];
+            }
+        }
+        for (int o = 16; o; o >>= 1) {
+            ac += __shfl_xor_sync(0xFFFFFFFFu, ac, o);
+            am += __shfl_xor_sync(0xFFFFFFFFu, am, o);
+        }
+        if (lane == 0) {
+            s.bi[0] = reach && mf;
+            s.bi[1] = c;
+            s.ured[NW] = ac;
+            s.ured[NW + 1] = am;
+        }
+    }
+    __syncthreads();
+    Sel r;
+    r.reach = s.bi[0] != 0;
+    const int c = s.bi[1];
+    const unsigned long long ac = s.ured[NW], am = s.ured[NW + 1];
+    const int nc = (int)s.h.g.hcnt[c];
+    __syncthreads();
+    if (!r.reach) return r;
+    const unsigned long long above = by_count ? ac : am;
+    if (nc <= kSel) {
+        // the crossing bin's keys, compared exactly
+        each([&](bool v, uint32_t key, float a) {
+            if (v && key >= floor_key && abin(a) == c) {
+                const int slot = atomicAdd(&s.nsel, 1);
+                s.h.g.skey[slot] = key;
+                s.h.g.smass[slot] = fx_of(a);
+            }
+        });
+        __syncthreads();
+        const int n = s.nsel;
+        uint32_t cand = 0u;
+        for (int i = tid; i < n; i += NT) {
+            const uint32_t ki = s.h.g.skey[i];
+            unsigned long long W = above;
+            for (int j = 0; j < n; ++j) W += s.h.g.skey[j] >= ki ? (by_count ? 1ull : s.h.g.smass[j]) : 0ull;
+            if (W >= target) cand = max(cand, ki);
+        }
+        r.tau = block_max_u32(s, cand);
+        unsigned long long pc = 0ull, pm = 0ull;
+        for (int i = tid; i < n; i += NT) {
+            if (s.h.g.skey[i] >= r.tau) {
+                pc += 1ull;
+                pm += s.h.g.smass[i];
+            }
+        }
+        r.cnt = ac + block_sum_u64(s, pc);
+        r.mass = am + block_sum_u64(s, pm);
+    } else {
+        auto keep = [&](uint32_t key, float a) { return key >= floor_key && abin(a) == c; };
+        r.tau = radix_select(s, each, keep, npass, by_count, above, target);
+        unsigned long long pc = 0ull, pm = 0ull;
+        each([&](bool v, uint32_t key, float a) {
+            if (v && key >= r.tau) {
+                pc += 1ull;
+                pm += fx_of(a);
+            }
+        });
+        r.cnt = block_sum_u64(s, pc);
+        r.mass = block_sum_u64(s, pm);
+    }
+    return r;
+}
+
+// Top-k then top-p over the items of `each`. Returns false (head keys only)
+// when they do not decide the threshold; the row path always decides.
+template <typename Each>
+SV_DEV bool threshold_from(Shared& s, const RowParams& p, const Each& each, int npass, bool head, float S,
+                           float* thr, float* sk) {
+    unsigned long long kept = (unsigned long long)(S * kFx);
+    float t = -INFINITY;
+    uint32_t floor_key = 0u;
+    if (p.transform & kXfTopK) {
+        const Sel r = select(s, each, npass, true, 0u, (unsigned long long)p.top_k);
+        if (!r.reach) {
+            if (head) return false;
+        } else {
+            floor_key = r.tau;
+            t = key_to_f32(r.tau);
+            kept = r.mass;
+        }
+    }
+    if (p.transform & kXfTopP) {
+        const Sel r = select(s, each, npass, false, floor_key, top_p_target(p.top_p, kept));
+        if (!r.reach) {
+            if (head) return false;
+        } else {
+            t = key_to_f32(r.tau);
+            kept = r.mass;
+        }
+    }
+    *thr = t;
     *sk = (float)kept * (1.0f / kFx);
     return true;
 }
 
-// Exact top-k / top-p over the row read from global memory (slow path).
-template <typename E>
-SV_DEV void slow_threshold(Shared& s, const RowParams& p, const E* row, float m, float S, float* thr,
-                           float* sk) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const float mc = m * p.c2, c2 = p.c2;
-    constexpr int npass = sizeof(E) == 4 ? 4 : 2;
-    uint32_t floor_key = 0u;
-    unsigned long long kept = (unsigned long long)(S * kFx);
-    float t = -INFINITY;
-    if (p.transform & kXfTopK) {
-        auto cnt = [&](int i, uint32_t& key, unsigned long long& w) {
-            key = f32_key(VecTraits<E>::load1(row + i));
-            w = 1ull;
-            return true;
-        };
-        uint32_t kk;
-        unsigned long long c;
-        radix_select(s, cnt, p.V, npass, (unsigned long long)p.top_k, &kk, &c);
-        floor_key = kk;
-        t = key_to_f32(kk);
-        unsigned long long part = 0ull;
-        for (int i = tid; i < p.V; i += NT) {
-            const float z = VecTraits<E>::load1(row + i);
-            if (f32_key(z) >= kk) part += fx_mass(z, c2, mc);
+// bf16 ordinal: order-preserving 16-bit key of a bf16 value (-0 folded onto +0).
+SV_DEV uint32_t ord16(uint32_t raw) {
+    raw = raw == 0x8000u ? 0u : raw;
+    return (raw & 0x8000u) ? (~raw & 0xFFFFu) : (raw | 0x8000u);
+}
+
+SV_DEV float ord16_value(uint32_t k) {
+    const uint32_t raw = (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
+    return __uint_as_float(raw << 16);
+}
+
+// First bin (in thread order, 8 bins per thread) whose running weight reaches
+// target among bins with count > 0 and index <= jmax; -1 if none. Every
+// thread returns the same bin and the running weights (count, mass) there.
+SV_DEV int ord_find(Shared& s, const unsigned (&cn)[8], const unsigned long long (&ms)[8], unsigned long long ec,
+                    unsigned long long em, bool by_count, unsigned long long target, int jmax,
+                    unsigned long long* cnt_at, unsigned long long* mass_at) {
+    const int tid = threadIdx.x;
+    if (tid == 0) s.bi[3] = -1;
+    __syncthreads();
+    unsigned long long c = ec, w = em;
+    for (int e = 0; e < 8; ++e) {
+        const unsigned long long pw = by_count ? c : w;
+        c += cn[e];
+        w += ms[e];
+        const unsigned long long nw = by_count ? c : w;
+        const int j = 8 * tid + e;
+        if (cn[e] && j <= jmax && pw < target && nw >= target) {
+            s.bi[3] = j;
+            s.ured[NW] = c;
+            s.ured[NW + 1] = w;
         }
-        for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, o);
-        if (lane == 0) s.ured[warp] = part;
-        __syncthreads();
-        kept = 0ull;
-        for (int w = 0; w < NW; ++w) kept += s.ured[w];
-        __syncthreads();
+    }
+    __syncthreads();
+    const int j = s.bi[3];
+    *cnt_at = s.ured[NW];
+    *mass_at = s.ured[NW + 1];
+    __syncthreads();
+    return j;
+}
+
+// Threshold of a bf16 row from its stored keys, counted per distinct value
+// (bin j holds the ordinal top - j). False when the stored keys do not decide.
+__device__ __noinline__ bool bf16_threshold(Shared& s, const RowParams& p, float ref, float m, float S, float* thr,
+                                            float* sk) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float c2 = p.c2, mc = m * c2;
+    const uint32_t top = ord16(__float_as_uint(ref) >> 16) + kOrdAbove;
+    for (int j = tid; j < kOrd; j += NT) s.h.ocnt[j] = 0u;
+    if (tid == 0) s.bi[4] = 0;
+    __syncthreads();
+    const uint16_t* slots = reinterpret_cast<const uint16_t*>(s.u.slots);
+    const int n = s.hn[tid];
+    for (int c = 0; c < n; ++c) {
+        const int j = (int)top - (int)ord16(slots[c * NT + tid]);
+        if (j < 0) s.bi[4] = 1;                       // above the histogram
+        else if (j < kOrd) atomicAdd(&s.h.ocnt[j], 1u);  // below it: not needed (upper set kept)
+    }
+    __syncthreads();
+    if (s.bi[4]) return false;
+    unsigned cn[8];
+    unsigned long long ms[8], tc = 0ull, tw = 0ull;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const int j = 8 * tid + e;
+        cn[e] = s.h.ocnt[j];
+        ms[e] = cn[e] ? (unsigned long long)cn[e] * fx_of(fmaf(ord16_value(top - j), c2, -mc)) : 0ull;
+        tc += cn[e];
+        tw += ms[e];
+    }
+    // exclusive scan of (count, mass) in thread order
+    unsigned long long ic = tc, iw = tw;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const unsigned long long yc = __shfl_up_sync(0xFFFFFFFFu, ic, d);
+        const unsigned long long yw = __shfl_up_sync(0xFFFFFFFFu, iw, d);
+        if (lane >= d) {
+            ic += yc;
+            iw += yw;
+        }
+    }
+    if (lane == 31) {
+        s.ured[warp] = ic;
+        s.ured2[warp] = iw;
+    }
+    __syncthreads();
+    unsigned long long ec = ic - tc, ew = iw - tw;
+    for (int w = 0; w < warp; ++w) {
+        ec += s.ured[w];
+        ew += s.ured2[w];
+    }
+    __syncthreads();
+    unsigned long long kept = (unsigned long long)(S * kFx), ca, ma;
+    float t = -INFINITY;
+    int jk = kOrd - 1;
+    if (p.transform & kXfTopK) {
+        jk = ord_find(s, cn, ms, ec, ew, true, (unsigned long long)p.top_k, kOrd - 1, &ca, &ma);
+        if (jk < 0) return false;
+        t = ord16_value(top - jk);
+        kept = ma;
     }
     if (p.transform & kXfTopP) {
-        auto mass = [&](int i, uint32_t& key, unsigned long long& w) {
-            const float z = VecTraits<E>::load1(row + i);
-            key = f32_key(z);
-            w = fx_mass(z, c2, mc);
-            return key >= floor_key;
-        };
-        uint32_t pk;
-        unsigned long long w;
-        radix_select(s, mass, p.V, npass, top_p_target(p.top_p, kept), &pk, &w);
-        t = key_to_f32(pk);
-        kept = w;
+        const int j = ord_find(s, cn, ms, ec, ew, false, top_p_target(p.top_p, kept), jk, &ca, &ma);
+        if (j < 0) return false;
+        t = ord16_value(top - j);
+        kept = ma;
     }
     *thr = t;
     *sk = (float)kept * (1.0f / kFx);
+    return true;
+}
+
+// Threshold and kept mass of a row: from the stored keys when they decide it,
+// else from the row in global memory.
+template <typename E>
+__device__ __noinline__ void row_threshold(Shared& s, const RowParams& p, const E* row, float ref, float m,
+                                           float S, bool use_slots, float* thr, float* sk) {
+    const int tid = threadIdx.x;
+    const float c2 = p.c2, mc = m * c2;
+    constexpr int npass = sizeof(E) == 4 ? 4 : 2;
+    if (use_slots && !s.ovf) {
+        if (sizeof(E) == 2 && bf16_threshold(s, p, ref, m, S, thr, sk)) return;
+        using K = typename Core<E>::Key;
+        const K* slots = reinterpret_cast<const K*>(s.u.slots);
+        const int n = s.hn[tid];
+        const int nmax = __reduce_max_sync(0xFFFFFFFFu, n);
+        auto each = [&](auto f) {
+            for (int c = 0; c < nmax; ++c) {
+                const bool v0 = c < n;
+                const uint32_t raw = v0 ? (uint32_t)slots[c * NT + tid] : 0u;
+                const float z = sizeof(E) == 2 ? __uint_as_float(raw << 16) : __uint_as_float(raw);
+                const float a = v0 ? fmaf(z, c2, -mc) : -INFINITY;
+                f(v0 && a > -(float)kWin, f32_key(z), a);
+            }
+        };
+        if (threshold_from(s, p, each, npass, true, S, thr, sk)) return;
+    }
+    const int V = p.V;
+    auto each = [&](auto f) {
+        for (int base = 0; base < V; base += NT) {
+            const int i = base + tid;
+            const bool v = i < V;
+            const float z = v ? VecTraits<E>::load1(row + i) : -INFINITY;
+            f(v, f32_key(z), fmaf(z, c2, -mc));
+        }
+    };
+    threshold_from(s, p, each, npass, false, S, thr, sk);
 }
 
 // --- per-row draw (sampling) and per-sequence resolve (verification) --------
@@ -414,7 +811,7 @@ SV_DEV void slow_threshold(Shared& s, const RowParams& p, const E* row, float m,
 // row's statistics (the row is still in L2).
 template <typename E>
 __device__ __noinline__ void sample_row(Shared& s, const RowParams& p, const E* row, int b, int r, int rowid) {
-    const RowRec rec = s.rec[0];
+    const RowRec rec = s.u.rec[0];
     int tok = -1;
     if (!(rec.flags & kRecEData)) {
         const float u = uniform01(p.seed, p.offset + (uint64_t)b, p.pos0 + (uint32_t)r, p.purpose);
@@ -434,15 +831,15 @@ __device__ __noinline__ void resolve_sequence(Shared& s, const RowParams& p, int
     const int tid = threadIdx.x;
     const int R = p.rows_per_b, G = p.gamma;
     __threadfence();
-    for (int i = tid; i < R; i += NT) s.rec[i] = load_rec(p.rows + (size_t)b * R + i);
+    for (int i = tid; i < R; i += NT) s.u.rec[i] = load_rec(p.rows + (size_t)b * R + i);
     __syncthreads();
     if (tid == 0) {
         int flags = 0;
-        for (int i = 0; i < R; ++i) flags |= s.rec[i].flags;
+        for (int i = 0; i < R; ++i) flags |= s.u.rec[i].flags;
         int n = G;
         for (int k = 0; k < G; ++k) {
-            const RowRec& t = s.rec[k];
-            const RowRec& d = s.rec[G + 1 + k];
+            const RowRec& t = s.u.rec[k];
+            const RowRec& d = s.u.rec[G + 1 + k];
             const float q = KeptExp{t.thr, p.c2, t.m * p.c2, 1.f}(t.zx) / t.Sk;
             const float pd = KeptExp{d.thr, p.c2, d.m * p.c2, 1.f}(d.zx) / d.Sk;
             if (p.probs_dbg) {
@@ -465,9 +862,9 @@ __device__ __noinline__ void resolve_sequence(Shared& s, const RowParams& p, int
         const RowRef<E> tr = row_ref<E>(p, b, n);
         if (n < G) {
             const RowRef<E> dr = row_ref<E>(p, b, G + 1 + n);
-            tok = draw_residual<E>(s.draw, tr.ptr, dr.ptr, p.V, s.rec[n], s.rec[G + 1 + n], p.c2, u2);
+            tok = draw_residual<E>(s.draw, tr.ptr, dr.ptr, p.V, s.u.rec[n], s.u.rec[G + 1 + n], p.c2, u2);
         } else {
-            tok = draw_q<E>(s.draw, tr.ptr, p.V, s.rec[G], p.c2, u2);
+            tok = draw_q<E>(s.draw, tr.ptr, p.V, s.u.rec[G], p.c2, u2);
         }
     }
     if (tid == 0) {
@@ -477,7 +874,7 @@ __device__ __noinline__ void resolve_sequence(Shared& s, const RowParams& p, int
     }
     for (int j = tid; j <= G; j += NT) {
         int v = -1;
-        if (!stt) v = j < n ? s.rec[j].x : (j == n ? tok : -1);
+        if (!stt) v = j < n ? s.u.rec[j].x : (j == n ? tok : -1);
         p.tokens[(size_t)b * (G + 1) + j] = v;
     }
 }
@@ -491,18 +888,19 @@ __global__ void __launch_bounds__(NT, 4) row_kernel(const __grid_constant__ RowP
     const int tid = threadIdx.x;
     const int R = p.rows_per_b;
     const int nunits = p.B * R * p.nseg;
-    const bool fast_p = XF && p.transform == kXfTopP && p.nseg == 1;
-    const Streamer<E> st{p.c2, (float)(kWin + 1) / p.c2, fast_p, &s};
-
-    for (;;) {
-        if (tid == 0) {
-            s.unit = (int)atomicAdd(p.work, 1u);
-            s.nhead = 0;
-            s.hmax = kKeyNegInf;
-        }
+    const bool col = XF && p.nseg == 1;
+    const float wc = (float)(kWin + 1) / p.c2;
+    if (tid == 0) {
+        s.next[0] = (int)atomicAdd(p.work, 1u);
+        s.hmax = kKeyNegInf;
+        s.ovf = 0;
+    }
+    for (int it = 0;; ++it) {
         __syncthreads();
-        const int unit = s.unit;
+        const int unit = s.next[it & 1];
         if (unit >= nunits) break;
+        unsigned pre = 0u;
+        if (tid == 0) pre = atomicAdd(p.work, 1u);  // the next unit, fetched while this one streams
         const int rowid = unit / p.nseg, seg = unit - rowid * p.nseg;
         const int b = rowid / R, r = rowid - b * R;
         const RowRef<E> rr = row_ref<E>(p, b, r);
@@ -515,16 +913,21 @@ __global__ void __launch_bounds__(NT, 4) row_kernel(const __grid_constant__ RowP
             if (x >= i0 && x < i1) zx = VecTraits<E>::load1(rr.ptr + x);
         }
 
-        const Online o = block_merge(s, st.run(rr.ptr, i0, i1), p.c2);
+        const RowStats st = col ? row_stats<E, true>(s, rr.ptr, i0, i1, p.c2, wc)
+                                : row_stats<E, false>(s, rr.ptr, i0, i1, p.c2, wc);
+        if (tid == 0) {
+            s.next[(it + 1) & 1] = (int)pre;
+            s.hmax = kKeyNegInf;
+        }
 
         // ---- row record (by the last segment of the row to finish) ----
         bool have_row = p.nseg == 1;
-        float m = o.m, S = o.s;
+        float m = st.m, S = st.sref;
         if (p.nseg > 1) {
             if (tid == 0) {
                 SegRec sr;
-                sr.m = o.m;
-                sr.s = o.s;
+                sr.m = m;
+                sr.s = S;
                 sr.zx = zx;
                 sr.flags = 0;
                 p.segs[unit] = sr;
@@ -553,13 +956,10 @@ __global__ void __launch_bounds__(NT, 4) row_kernel(const __grid_constant__ RowP
             }
         }
         if (have_row) {
-            const bool bad = !(S > 0.f && S <= 3.0e38f);
+            const bool bad = !(m > -INFINITY && m < INFINITY);
             float thr = -INFINITY, sk = S;
-            if (XF && !bad) {
-                bool done = false;
-                if (fast_p) done = fast_top_p(s, p, m, S, sizeof(E) == 4 ? 4 : 2, &thr, &sk);
-                if (!done) slow_threshold<E>(s, p, rr.ptr, m, S, &thr, &sk);
-            }
+            if (XF && !bad) row_threshold<E>(s, p, rr.ptr, st.ref, m, S, col, &thr, &sk);
+            __syncthreads();
             if (tid == 0) {
                 RowRec rec;
                 rec.m = m;
@@ -569,8 +969,10 @@ __global__ void __launch_bounds__(NT, 4) row_kernel(const __grid_constant__ RowP
                 rec.zx = zx;
                 rec.x = x;
                 rec.flags = (bad || (rr.has_x && (x < 0 || x >= p.V))) ? kRecEData : 0;
+                rec.pad = 0;
                 p.rows[rowid] = rec;
-                s.rec[0] = rec;
+                s.u.rec[0] = rec;
+                s.ovf = 0;
             }
             __syncthreads();
 
@@ -587,7 +989,6 @@ __global__ void __launch_bounds__(NT, 4) row_kernel(const __grid_constant__ RowP
                 if (s.last) resolve_sequence<E>(s, p, b);
             }
         }
-        __syncthreads();
     }
 }
 

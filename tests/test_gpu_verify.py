@@ -66,6 +66,45 @@ def test_transforms_ragged_vocab_across_a_cluster(dtype, T, top_p, top_k):
         max_near=0.5)
 
 
+def deep_tie_logits(B, gamma, V, T, seed, dtype):
+    """Rows with 3-8 tokens near the top and every other token exactly
+    16 octaves (16 T ln 2) below them: the ~40000 equal tokens hold more
+    than 3% of the mass, so the nucleus of top_p = 0.97 ends inside that one
+    tie group, far below the keys near the maximum."""
+    g = torch.Generator().manual_seed(seed)
+    zt = torch.zeros(B, gamma + 1, V)
+    for b in range(B):
+        for k in range(gamma + 1):
+            n = int(torch.randint(3, 9, (1,), generator=g))
+            idx = torch.randperm(V, generator=g)[:n]
+            zt[b, k, idx] = 16 * T * float(np.log(2)) + 0.05 * torch.arange(n).float()
+    zd = zt[:, :gamma].clone()
+    zd[zd > 0] += 0.5 * torch.rand(int((zd > 0).sum()), generator=g)
+    td = torch.float32 if dtype == "f32" else torch.bfloat16
+    return zt.to(td).contiguous(), zd.to(td).contiguous()
+
+
+@pytest.mark.parametrize("dtype,T,top_p,top_k", [("bf16", 1.0, 0.9, 0), ("f32", 1.0, 0.95, 100),
+                                                 ("bf16", 1.0, 0.95, 100)])
+def test_flat_rows_overflow_the_collected_keys(dtype, T, top_p, top_k):
+    """Flat rows put more keys near the maximum than each thread collects, so
+    the threshold comes from the row in global memory."""
+    zt, zd = workloads.linear_logits(12, 2, 40001, 23, dtype=dtype, sd_t=0.2, sd_d=0.3)
+    run(zt, zd, T, top_p, top_k, seed=8, label=f"flat {dtype} p={top_p} k={top_k}", max_near=0.2)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_crossing_far_below_the_collected_keys(dtype):
+    """The nucleus ends 16 octaves below the maximum (in one tie group of
+    ~40000 keys); top-k = 2000 of widely spread logits likewise lies below
+    the keys near the maximum."""
+    zt, zd = deep_tie_logits(10, 2, 40001, 0.5, 31, dtype)
+    g, r, _ = run(zt, zd, 0.5, 0.97, 0, seed=3, label=f"deep tie {dtype}", max_near=0.05)
+    assert (r["accepted"] < 2).any()
+    zt, zd = workloads.linear_logits(12, 2, 40001, 29, dtype=dtype, sd_t=6.0, sd_d=0.3)
+    run(zt, zd, 0.5, 1.0, 2000, seed=4, label=f"wide top-k {dtype}", max_near=0.05)
+
+
 @pytest.mark.parametrize("V", [1, 2, 7, 31, 999, 4097])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_small_and_ragged_vocabularies(V, dtype):
