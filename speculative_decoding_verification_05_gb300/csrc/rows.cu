@@ -55,6 +55,7 @@ constexpr int kSlotBytes = 128;        // key slots per thread, in bytes
 constexpr int kSel = 256;              // keys compared exactly inside the crossing bin
 constexpr int kOrd = 2048;             // bf16 ordinal histogram: bins
 constexpr int kOrdAbove = 256;         //   of which above the reference value
+constexpr uint32_t kPrefetchBytes = 65536;  // next units up to this size are prefetched into L2
 constexpr float kFx = 1099511627776.0f;  // 2^40: masses >= 2^-17 are exact integers
 
 struct GenSel {
@@ -65,7 +66,7 @@ struct GenSel {
 };
 
 struct Shared {
-    int next[2];                      // prefetched work units
+    int q[3];                         // work units: this one and the next two
     int last;
     unsigned hmax;                    // key of the first group's maximum
     int ovf;                          // a thread's key slots overflowed
@@ -879,6 +880,17 @@ __device__ __noinline__ void resolve_sequence(Shared& s, const RowParams& p, int
     }
 }
 
+// L2 prefetch of the 16-byte-aligned interior of elements [i0, i1) of row
+// when it is at most kPrefetchBytes (a hint: no data moves into the SM).
+// Longer units are not prefetched: across all CTAs they would exceed L2.
+template <typename E>
+SV_DEV void prefetch_l2(const E* row, int i0, int i1) {
+    const uintptr_t a = ((uintptr_t)(row + i0) + 15) & ~(uintptr_t)15;
+    const uintptr_t e = (uintptr_t)(row + i1) & ~(uintptr_t)15;
+    if (e > a && e - a <= kPrefetchBytes)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"((uint32_t)(e - a)) : "memory");
+}
+
 // --- the kernel -----------------------------------------------------------------
 
 template <typename E, bool XF>
@@ -890,21 +902,38 @@ __global__ void __launch_bounds__(NT, 4) row_kernel(const __grid_constant__ RowP
     const int nunits = p.B * R * p.nseg;
     const bool col = XF && p.nseg == 1;
     const float wc = (float)(kWin + 1) / p.c2;
+    auto locate = [&](int u, int* b, int* r, int* i0, int* i1) {
+        const int rowid = u / p.nseg, seg = u - rowid * p.nseg;
+        *b = rowid / R;
+        *r = rowid - *b * R;
+        *i0 = seg * p.seg_len;
+        *i1 = min(p.V, *i0 + p.seg_len);
+    };
     if (tid == 0) {
-        s.next[0] = (int)atomicAdd(p.work, 1u);
+        s.q[0] = (int)atomicAdd(p.work, 1u);
+        s.q[1] = (int)atomicAdd(p.work, 1u);
         s.hmax = kKeyNegInf;
         s.ovf = 0;
     }
     for (int it = 0;; ++it) {
         __syncthreads();
-        const int unit = s.next[it & 1];
+        const int unit = s.q[it % 3];
         if (unit >= nunits) break;
         unsigned pre = 0u;
-        if (tid == 0) pre = atomicAdd(p.work, 1u);  // the next unit, fetched while this one streams
-        const int rowid = unit / p.nseg, seg = unit - rowid * p.nseg;
-        const int b = rowid / R, r = rowid - b * R;
+        if (tid == 0) {
+            pre = atomicAdd(p.work, 1u);  // the unit after next, fetched while this one streams
+            // a short next unit moves from HBM into L2 while this one streams
+            const int nxt = s.q[(it + 1) % 3];
+            if (nxt < nunits) {
+                int b2, r2, j0, j1;
+                locate(nxt, &b2, &r2, &j0, &j1);
+                prefetch_l2(row_ref<E>(p, b2, r2).ptr, j0, j1);
+            }
+        }
+        const int rowid = unit / p.nseg;
+        int b, r, i0, i1;
+        locate(unit, &b, &r, &i0, &i1);
         const RowRef<E> rr = row_ref<E>(p, b, r);
-        const int i0 = seg * p.seg_len, i1 = min(p.V, i0 + p.seg_len);
         // the draft token and its logit in this row (loaded early, used at the end)
         int x = -1;
         float zx = 0.f;
@@ -916,7 +945,7 @@ __global__ void __launch_bounds__(NT, 4) row_kernel(const __grid_constant__ RowP
         const RowStats st = col ? row_stats<E, true>(s, rr.ptr, i0, i1, p.c2, wc)
                                 : row_stats<E, false>(s, rr.ptr, i0, i1, p.c2, wc);
         if (tid == 0) {
-            s.next[(it + 1) & 1] = (int)pre;
+            s.q[(it + 2) % 3] = (int)pre;
             s.hmax = kKeyNegInf;
         }
 
