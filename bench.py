@@ -7,7 +7,10 @@ for the default workload ("nucleus": B=8, gamma=4, V=32000, bf16, T=0.8,
 top_p=0.95, 1000 steps) the 1000 verification steps are issued as one call
 over 8000 sequences (offset = step * B, so every Philox counter is the one a
 step-by-step loop would use). Inputs (4.6 GB) are resident in HBM and larger
-than L2, so no flush is needed between timed steps.
+than L2, so no flush is needed between timed steps; workloads smaller than
+twice L2 (tiny) overwrite a 256 MB buffer before each timed step, outside
+the timed events. ``--stack S`` overrides the number of stacked steps (a
+smaller case of the same workload, used for ncu captures).
 
 Prints one JSON line: verified positions/s (whole job), the roofline of the
 dominant kernel (algorithmic bytes / CUDA-event time against the measured HBM
@@ -95,7 +98,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except OSError:
@@ -239,12 +242,13 @@ def reference_arm(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="nucleus", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--stack", type=int, default=0, help="stacked steps per call (default: the workload's)")
     args = ap.parse_args()
     if args.impl == "reference":
         return reference_arm(args)
@@ -261,6 +265,8 @@ def main():
 
     sv.load_library()
     cfg, stacked, temp = WORKLOADS[args.workload]
+    if args.stack > 0:
+        stacked = args.stack
     inp = make_inputs(cfg, stacked, temp, device, seed=2024 + rank)
     nbytes, npos = algorithmic(inp)
     stream = torch.cuda.current_stream(device)
@@ -271,24 +277,31 @@ def main():
             dist.barrier()
         torch.cuda.synchronize(device)
 
-    for _ in range(args.warmup):
-        run_step(inp)
-    barrier()
+    l2_bytes = 129 * 2**20
+    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=device) if nbytes < 2 * l2_bytes else None
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    # clocks are sampled from the warm-up through the timed steps; a short
+    # timed region is followed by untimed steps until 0.3 s of load is sampled
     with ClockSampler(local) as clk:
+        t_load0 = time.perf_counter()
+        for _ in range(args.warmup):
+            if flush is not None:
+                flush.fill_(1)
+            run_step(inp)
         barrier()
-        t_all0 = torch.cuda.Event(enable_timing=True)
-        t_all1 = torch.cuda.Event(enable_timing=True)
-        t_all0.record(stream)
         for i in range(args.steps):
+            if flush is not None:
+                flush.fill_(i & 255)  # evicts the previous step's inputs from L2 (untimed)
             starts[i].record(stream)
             run_step(inp)
             ends[i].record(stream)
-        t_all1.record(stream)
         barrier()
-    total_ms = t_all0.elapsed_time(t_all1)
+        while time.perf_counter() - t_load0 < 0.3:
+            run_step(inp)
+            torch.cuda.synchronize(device)
     per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(per_launch_ms)
     if ws > 1:
         import torch.distributed as dist
         t = torch.tensor([total_ms], device=device)
@@ -341,11 +354,11 @@ def main():
         "config": {"workload": f"{args.workload}: {cfg} x {stacked} steps in one call "
                                f"(B={inp['B']}, V={inp['V']})", "global_batch": inp["B"] * ws,
                    "bytes_per_step": nbytes, "positions_per_step": npos,
-                   "l2": "inputs larger than L2 (no flush)" if nbytes > 4 * 129e6 else "L2 flushed",
+                   "l2": "L2 flushed between steps" if flush is not None else "inputs larger than 2x L2 (no flush)",
                    "parallelism": f"replicas x{ws}"},
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step(inp) * args.steps,
-        "clocks": clk.summary(),
+        "clocks": dict(clk.summary(), window="warm-up + timed steps (+ untimed steps up to 0.3 s)"),
         "hbm_gbs": achieved, "mean_accepted": acc_mean,
     }
     print(json.dumps(line))
