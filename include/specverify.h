@@ -37,8 +37,10 @@
  *    `status[b]` (when `status` is not NULL): SPEC_EDATA for a logit row that
  *    holds NaN or +inf or only -inf, a draft token outside [0, V), or a
  *    malformed tree; that sequence's outputs are then all -1. -inf alone is
- *    an ordinary zero-probability logit. SPEC_ETIMEOUT marks a sequence whose
- *    bounded wait for its own asynchronous copies gave up.
+ *    an ordinary zero-probability logit. SPEC_ETIMEOUT is reserved for a
+ *    device wait that gives up; the current kernels never wait on one
+ *    another (every hand-off is a last-arriver counter), so it is not
+ *    reported.
  *  - Workspace: a device buffer of at least the size the matching
  *    *_workspace_size() function returns, 256-byte aligned, owned by the
  *    caller. Its content on entry does not matter: each call clears the small
