@@ -854,6 +854,12 @@ __device__ __noinline__ void resolve_sequence(Shared& s, const RowParams& p, int
         }
         s.bi[2] = n;
         s.bi[3] = (flags & kRecEData) ? kEData : kOk;
+        if (!(flags & kRecEData)) {
+            // the one row pair (or bonus row) the draw reads: into L2 now
+            const size_t bytes = (size_t)p.V * sizeof(E);
+            prefetch_span_l2(row_ref<E>(p, b, n).ptr, bytes);
+            if (n < G) prefetch_span_l2(row_ref<E>(p, b, G + 1 + n).ptr, bytes);
+        }
     }
     __syncthreads();
     const int n = s.bi[2], stt = s.bi[3];
