@@ -51,10 +51,9 @@ constexpr int NW = NT / 32;
 constexpr int kMaxRows = 2 * 255 + 1;  // rows per sequence (verification, gamma <= 255)
 constexpr int kU = 4;                  // 16-byte vectors in flight per thread
 constexpr int kWin = 13;               // stored keys: within 2^-kWin of the row max (plus one octave)
-constexpr int kSlotBytes = 128;        // key slots per thread, in bytes
+constexpr int kSlotBytes = 96;         // key slots per thread, in bytes
 constexpr int kSel = 256;              // keys compared exactly inside the crossing bin
 constexpr int kOrd = 2048;             // bf16 ordinal histogram: bins
-constexpr int kOrdAbove = 256;         //   of which above the reference value
 constexpr uint32_t kPrefetchBytes = 65536;  // next units up to this size are prefetched into L2
 constexpr float kFx = 1099511627776.0f;  // 2^40: masses >= 2^-17 are exact integers
 
@@ -78,9 +77,11 @@ struct Shared {
     float bf[8];
     unsigned short hn[NT];            // stored keys per thread
     union {
-        GenSel g;
-        unsigned ocnt[kOrd];
+        GenSel g;                     // binned selection (fp32 rows, global fallback)
+        unsigned ocnt[kOrd];          // bf16 rows: stored keys per distinct value
     } h;
+    int jmax;                         // deepest ordinal bin in use
+    int odirty;                       // h.g was used since h.ocnt was last cleared
     union {
         unsigned char slots[kSlotBytes * NT];  // slot c of thread t at element c * NT + t
         RowRec rec[kMaxRows];                  // sequence resolve (after the row's threshold)
@@ -450,6 +451,7 @@ SV_DEV uint32_t radix_select(Shared& s, const Each& each, const Keep& keep, int 
     unsigned long long A = A0;
     for (int pass = 0; pass < npass; ++pass) {
         const int shift = 24 - 8 * pass;
+        if (threadIdx.x == 0) s.odirty = 1;
         for (int i = threadIdx.x; i < 256; i += NT) {
             s.h.g.hist[i] = 0ull;
             s.h.g.hcnt[i] = 0u;
@@ -521,7 +523,10 @@ SV_DEV Sel select(Shared& s, const Each& each, int npass, bool by_count, uint32_
         s.h.g.hist[i] = 0ull;
         s.h.g.hcnt[i] = 0u;
     }
-    if (tid == 0) s.nsel = 0;
+    if (tid == 0) {
+        s.nsel = 0;
+        s.odirty = 1;
+    }
     __syncthreads();
     each([&](bool v, uint32_t key, float a) {
         v = v && key >= floor_key;
@@ -668,105 +673,116 @@ SV_DEV float ord16_value(uint32_t k) {
     return __uint_as_float(raw << 16);
 }
 
-// First bin (in thread order, 8 bins per thread) whose running weight reaches
-// target among bins with count > 0 and index <= jmax; -1 if none. Every
-// thread returns the same bin and the running weights (count, mass) there.
-SV_DEV int ord_find(Shared& s, const unsigned (&cn)[8], const unsigned long long (&ms)[8], unsigned long long ec,
-                    unsigned long long em, bool by_count, unsigned long long target, int jmax,
-                    unsigned long long* cnt_at, unsigned long long* mass_at) {
-    const int tid = threadIdx.x;
-    if (tid == 0) s.bi[3] = -1;
-    __syncthreads();
-    unsigned long long c = ec, w = em;
-    for (int e = 0; e < 8; ++e) {
-        const unsigned long long pw = by_count ? c : w;
-        c += cn[e];
-        w += ms[e];
-        const unsigned long long nw = by_count ? c : w;
-        const int j = 8 * tid + e;
-        if (cn[e] && j <= jmax && pw < target && nw >= target) {
-            s.bi[3] = j;
-            s.ured[NW] = c;
-            s.ured[NW + 1] = w;
-        }
-    }
-    __syncthreads();
-    const int j = s.bi[3];
-    *cnt_at = s.ured[NW];
-    *mass_at = s.ured[NW + 1];
-    __syncthreads();
-    return j;
-}
-
-// Threshold of a bf16 row from its stored keys, counted per distinct value
-// (bin j holds the ordinal top - j). False when the stored keys do not decide.
-__device__ __noinline__ bool bf16_threshold(Shared& s, const RowParams& p, float ref, float m, float S, float* thr,
+// Threshold of a bf16 row from its stored keys counted per distinct value
+// (bin j holds the values of ordinal ord16(m) - j, largest first; the cut was
+// fixed for the row, so the stored values form an upper set). Warp 0 scans
+// the bins in use; the bins are cleared again before returning. False when
+// the stored keys do not decide the threshold. Every thread must call it.
+__device__ __noinline__ bool bf16_threshold(Shared& s, const RowParams& p, float m, float S, float* thr,
                                             float* sk) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float c2 = p.c2, mc = m * c2;
-    const uint32_t top = ord16(__float_as_uint(ref) >> 16) + kOrdAbove;
-    for (int j = tid; j < kOrd; j += NT) s.h.ocnt[j] = 0u;
-    if (tid == 0) s.bi[4] = 0;
-    __syncthreads();
+    const int top = (int)ord16(__float_as_uint(m) >> 16);  // every stored key is <= m
+    if (s.odirty) {  // the binned selection has used this storage: clear every bin once
+        for (int j = tid; j < kOrd; j += NT) s.h.ocnt[j] = 0u;
+        __syncthreads();
+        if (tid == 0) s.odirty = 0;
+    }
     const uint16_t* slots = reinterpret_cast<const uint16_t*>(s.u.slots);
     const int n = s.hn[tid];
+    int jm = -1;
     for (int c = 0; c < n; ++c) {
-        const int j = (int)top - (int)ord16(slots[c * NT + tid]);
-        if (j < 0) s.bi[4] = 1;                       // above the histogram
-        else if (j < kOrd) atomicAdd(&s.h.ocnt[j], 1u);  // below it: not needed (upper set kept)
+        const int j = top - (int)ord16(slots[c * NT + tid]);
+        if (j < kOrd) {
+            atomicAdd(&s.h.ocnt[j], 1u);
+            jm = max(jm, j);
+        }  // below it: not needed, the counted values stay an upper set
     }
+    jm = __reduce_max_sync(0xFFFFFFFFu, jm);
+    if (lane == 0 && jm >= 0) atomicMax(&s.jmax, jm);
     __syncthreads();
-    if (s.bi[4]) return false;
-    unsigned cn[8];
-    unsigned long long ms[8], tc = 0ull, tw = 0ull;
+    const int jz = s.jmax;
+    if (warp == 0) {
+        bool ok = true;
+        const int nbins = jz + 1;
+        const int per = (nbins + 31) / 32;
+        const int j0 = min(nbins, lane * per), j1 = min(nbins, j0 + per);
+        auto mass_of = [&](int j, unsigned c) {
+            return (unsigned long long)c * fx_of(fmaf(ord16_value((uint32_t)(top - j)), c2, -mc));
+        };
+        unsigned long long tc = 0ull, tw = 0ull;
+        for (int j = j0; j < j1; ++j) {
+            const unsigned c = s.h.ocnt[j];
+            if (c) {
+                tc += c;
+                tw += mass_of(j, c);
+            }
+        }
+        unsigned long long ic = tc, iw = tw;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const int j = 8 * tid + e;
-        cn[e] = s.h.ocnt[j];
-        ms[e] = cn[e] ? (unsigned long long)cn[e] * fx_of(fmaf(ord16_value(top - j), c2, -mc)) : 0ull;
-        tc += cn[e];
-        tw += ms[e];
-    }
-    // exclusive scan of (count, mass) in thread order
-    unsigned long long ic = tc, iw = tw;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const unsigned long long yc = __shfl_up_sync(0xFFFFFFFFu, ic, d);
-        const unsigned long long yw = __shfl_up_sync(0xFFFFFFFFu, iw, d);
-        if (lane >= d) {
-            ic += yc;
-            iw += yw;
+        for (int d = 1; d < 32; d <<= 1) {
+            const unsigned long long yc = __shfl_up_sync(0xFFFFFFFFu, ic, d);
+            const unsigned long long yw = __shfl_up_sync(0xFFFFFFFFu, iw, d);
+            if (lane >= d) {
+                ic += yc;
+                iw += yw;
+            }
+        }
+        const unsigned long long ec = ic - tc, ew = iw - tw;
+        // the first non-empty bin j <= jlim whose running weight reaches target
+        auto find = [&](bool by_count, unsigned long long target, int jlim, int* jo, unsigned long long* wo) {
+            unsigned long long c = ec, w = ew, hw = 0ull;
+            int hit = -1;
+            for (int j = j0; j < j1 && hit < 0; ++j) {
+                const unsigned k = s.h.ocnt[j];
+                if (!k) continue;
+                c += k;
+                w += mass_of(j, k);
+                if (j <= jlim && (by_count ? c : w) >= target) {
+                    hit = j;
+                    hw = w;
+                }
+            }
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, hit >= 0);
+            if (!bal) return false;
+            const int src = __ffs(bal) - 1;
+            *jo = __shfl_sync(0xFFFFFFFFu, hit, src);
+            *wo = __shfl_sync(0xFFFFFFFFu, hw, src);
+            return true;
+        };
+        unsigned long long kept = (unsigned long long)(S * kFx);
+        float t = -INFINITY;
+        int jk = nbins - 1;
+        if (ok && (p.transform & kXfTopK)) {
+            unsigned long long w;
+            ok = find(true, (unsigned long long)p.top_k, nbins - 1, &jk, &w);
+            if (ok) {
+                t = ord16_value((uint32_t)(top - jk));
+                kept = w;
+            }
+        }
+        if (ok && (p.transform & kXfTopP)) {
+            int j;
+            unsigned long long w;
+            ok = find(false, top_p_target(p.top_p, kept), jk, &j, &w);
+            if (ok) {
+                t = ord16_value((uint32_t)(top - j));
+                kept = w;
+            }
+        }
+        if (lane == 0) {
+            s.bi[5] = ok;
+            s.bf[5] = t;
+            s.ured[NW] = kept;
         }
     }
-    if (lane == 31) {
-        s.ured[warp] = ic;
-        s.ured2[warp] = iw;
-    }
     __syncthreads();
-    unsigned long long ec = ic - tc, ew = iw - tw;
-    for (int w = 0; w < warp; ++w) {
-        ec += s.ured[w];
-        ew += s.ured2[w];
-    }
-    __syncthreads();
-    unsigned long long kept = (unsigned long long)(S * kFx), ca, ma;
-    float t = -INFINITY;
-    int jk = kOrd - 1;
-    if (p.transform & kXfTopK) {
-        jk = ord_find(s, cn, ms, ec, ew, true, (unsigned long long)p.top_k, kOrd - 1, &ca, &ma);
-        if (jk < 0) return false;
-        t = ord16_value(top - jk);
-        kept = ma;
-    }
-    if (p.transform & kXfTopP) {
-        const int j = ord_find(s, cn, ms, ec, ew, false, top_p_target(p.top_p, kept), jk, &ca, &ma);
-        if (j < 0) return false;
-        t = ord16_value(top - j);
-        kept = ma;
-    }
-    *thr = t;
-    *sk = (float)kept * (1.0f / kFx);
-    return true;
+    const bool ok = s.bi[5] != 0;
+    *thr = s.bf[5];
+    *sk = (float)s.ured[NW] * (1.0f / kFx);
+    for (int j = tid; j <= jz; j += NT) s.h.ocnt[j] = 0u;  // clean for the next row
+    if (tid == 0) s.jmax = -1;
+    return ok;
 }
 
 // Threshold and kept mass of a row: from the stored keys when they decide it,
@@ -778,7 +794,7 @@ __device__ __noinline__ void row_threshold(Shared& s, const RowParams& p, const 
     const float c2 = p.c2, mc = m * c2;
     constexpr int npass = sizeof(E) == 4 ? 4 : 2;
     if (use_slots && !s.ovf) {
-        if (sizeof(E) == 2 && bf16_threshold(s, p, ref, m, S, thr, sk)) return;
+        if (sizeof(E) == 2 && bf16_threshold(s, p, m, S, thr, sk)) return;
         using K = typename Core<E>::Key;
         const K* slots = reinterpret_cast<const K*>(s.u.slots);
         const int n = s.hn[tid];
@@ -916,6 +932,8 @@ __global__ void __launch_bounds__(NT, 4) row_kernel(const __grid_constant__ RowP
         *i1 = min(p.V, *i0 + p.seg_len);
     };
     if (tid == 0) {
+        s.odirty = 1;
+        s.jmax = -1;
         s.q[0] = (int)atomicAdd(p.work, 1u);
         s.q[1] = (int)atomicAdd(p.work, 1u);
         s.hmax = kKeyNegInf;
