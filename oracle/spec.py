@@ -187,7 +187,7 @@ def _uniform_fn(seed, uniform_fn):
 
 
 def verify(target, draft, draft_tokens, temperature=1.0, top_p=1.0, top_k=0,
-           seed=0, offset=0, uniform_fn=None):
+           seed=0, offset=0, uniform_fn=None, lenience=1.0):
     """Batched speculative verification (modified rejection sampling).
 
     target [B, gamma+1, V], draft [B, gamma, V] (unused when temperature is
@@ -206,6 +206,17 @@ def verify(target, draft, draft_tokens, temperature=1.0, top_p=1.0, top_k=0,
 
     Uniforms: u_k = U(seed, offset+b, k, ACCEPT), u'_n = U(seed, offset+b,
     n, RESAMPLE); ``uniform_fn(rows, pos, purpose)`` may replace them.
+
+    ``lenience`` l in ]0, 1] is the lenient variant of [SD] "方法细节"
+    (extension in its appendix F): the draft probability is scaled by l
+    before the comparison, so x_k is accepted with probability
+    min(1, q(x)/(l p(x))), and a rejection resamples from
+    norm(max(0, q - l p)). No token is then emitted with probability above
+    q(x)/l (the guarantee that section states); l = 1 is the exact method.
+    The pages state only the scaled comparison and the bound; the residual
+    max(0, q - l p) is the reading that keeps the bound and reduces to
+    (q - p)+ at l = 1. Temperature 0 is unaffected (one-hot rows give the
+    same decisions for every l).
 
     Returns a dict: accepted [B], tokens [B, gamma+1] (-1 padded),
     next_token [B], status [B], near_tie [B] (a decision within the near-tie
@@ -253,12 +264,12 @@ def verify(target, draft, draft_tokens, temperature=1.0, top_p=1.0, top_k=0,
             q_x[:, k] = q[brange, xs[:, k]]
             p_x[:, k] = p[brange, xs[:, k]]
             prob_near[:, k] = nq | npd
-            acc, _, near_acc = accept_test(U(rows, k, PURPOSE_ACCEPT), q_x[:, k], p_x[:, k])
+            acc, _, near_acc = accept_test(U(rows, k, PURPOSE_ACCEPT), q_x[:, k], lenience * p_x[:, k])
             live = n == gamma
             near |= live & (near_acc | nq | npd)
             rej = live & ~acc
             if rej.any():
-                w = np.maximum(0.0, q[rej] - p[rej])
+                w = np.maximum(0.0, q[rej] - lenience * p[rej])
                 zero = w.sum(axis=1) == 0
                 w[zero] = q[rej][zero]
                 tok, _, a = inverse_cdf(U(rows[rej], k, PURPOSE_RESAMPLE), w, with_alt=True)
