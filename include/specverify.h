@@ -137,6 +137,23 @@ spec_status spec_verify(const void* target, const void* draft, spec_dtype dtype,
                         void* workspace, size_t ws_bytes, spec_stream stream);
 
 /* ------------------------------------------------------------------------
+ * spec_verify_lenient - lenient verification ([SD] "方法细节", the lenience
+ * extension of its appendix F): the draft probability is scaled by
+ * `lenience` = l in ]0, 1] before the comparison, so x_k is accepted with
+ * probability min(1, q(x)/(l p(x))), and a rejection resamples from
+ * norm(max(0, q - l p)) (from q if that vanishes). No token is emitted with
+ * probability above q(x)/l; l = 1 is spec_verify exactly. Arguments,
+ * outputs, workspace and errors as spec_verify (l outside ]0, 1] or not
+ * finite: SPEC_EINVAL). Temperature 0 ignores l (same decisions).
+ * ---------------------------------------------------------------------- */
+spec_status spec_verify_lenient(const void* target, const void* draft, spec_dtype dtype,
+                                const int32_t* draft_tokens, int B, int gamma, int V,
+                                spec_sampling sampling, float lenience, uint64_t seed, uint64_t offset,
+                                int32_t* accepted, int32_t* tokens, int32_t* next_token,
+                                int32_t* status, float* probs_dbg,
+                                void* workspace, size_t ws_bytes, spec_stream stream);
+
+/* ------------------------------------------------------------------------
  * spec_verify_tree - greedy exact-match verification of a REST draft tree
  * ([REST] "REST: 基于检索的投机解码").
  *

@@ -30,7 +30,7 @@ SPEC_F32, SPEC_BF16 = 0, 1
 PURPOSE_ACCEPT, PURPOSE_RESAMPLE, PURPOSE_DRAFT = 0, 1, 2
 
 EXPORTED = [
-    "spec_verify_workspace_size", "spec_verify",
+    "spec_verify_workspace_size", "spec_verify", "spec_verify_lenient",
     "spec_verify_tree_workspace_size", "spec_verify_tree",
     "spec_verify_mentor_workspace_size", "spec_verify_mentor",
     "spec_sample_workspace_size", "spec_sample",
@@ -69,6 +69,9 @@ def load_library(path=LIB_PATH):
         lib.spec_verify.argtypes = [_P, _P, _I, _P, _I, _I, _I, SpecSampling, _U64, _U64,
                                     _P, _P, _P, _P, _P, _P, _SZ, _P]
         lib.spec_verify.restype = _I
+        lib.spec_verify_lenient.argtypes = [_P, _P, _I, _P, _I, _I, _I, SpecSampling, ctypes.c_float, _U64, _U64,
+                                            _P, _P, _P, _P, _P, _P, _SZ, _P]
+        lib.spec_verify_lenient.restype = _I
         lib.spec_verify_tree_workspace_size.argtypes = [_I, _I, _I, _I]
         lib.spec_verify_tree_workspace_size.restype = _SZ
         lib.spec_verify_tree.argtypes = [_P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P,
@@ -175,12 +178,14 @@ class _Staging:
 
 
 def verify(target, draft, draft_tokens, temperature=1.0, top_p=1.0, top_k=0, seed=0, offset=0,
-           debug=False, out=None):
+           debug=False, out=None, lenience=1.0):
     """Modified rejection sampling over target [B, gamma+1, V] and draft [B, gamma, V].
 
     Returns a dict of tensors: accepted [B], tokens [B, gamma+1], next_token [B],
     status [B] and, with debug=True, probs [B, gamma, 2] = (q(x_k), p(x_k)).
     ``out`` may pass preallocated output tensors under the same keys.
+    ``lenience`` l < 1 selects spec_verify_lenient (acceptance min(1, q/(l p)),
+    residual max(0, q - l p)); l = 1 is spec_verify.
     """
     lib = load_library()
     sg = _Staging(target)
@@ -204,11 +209,15 @@ def verify(target, draft, draft_tokens, temperature=1.0, top_p=1.0, top_k=0, see
     stream = torch.cuda.current_stream(sg.device)
     nbytes = lib.spec_verify_workspace_size(B, gamma, V, dt)
     ws = workspace(nbytes, sg.device, stream)
-    rc = lib.spec_verify(_ptr(target), _ptr(draft), dt, _ptr(toks), B, gamma, V,
-                         SpecSampling(float(temperature), float(top_p), int(top_k)),
-                         int(seed), int(offset), _ptr(o["accepted"]), _ptr(o["tokens"]),
-                         _ptr(o["next_token"]), _ptr(o["status"]), _ptr(o.get("probs")),
-                         _ptr(ws), ws.numel(), ctypes.c_void_p(stream.cuda_stream))
+    smp = SpecSampling(float(temperature), float(top_p), int(top_k))
+    outs = (_ptr(o["accepted"]), _ptr(o["tokens"]), _ptr(o["next_token"]), _ptr(o["status"]),
+            _ptr(o.get("probs")), _ptr(ws), ws.numel(), ctypes.c_void_p(stream.cuda_stream))
+    if lenience == 1.0:
+        rc = lib.spec_verify(_ptr(target), _ptr(draft), dt, _ptr(toks), B, gamma, V, smp, int(seed), int(offset),
+                             *outs)
+    else:
+        rc = lib.spec_verify_lenient(_ptr(target), _ptr(draft), dt, _ptr(toks), B, gamma, V, smp,
+                                     float(lenience), int(seed), int(offset), *outs)
     _check(rc)
     return sg.back(o)
 

@@ -197,41 +197,14 @@ __global__ void philox_uniform_kernel(uint64_t seed, uint64_t row0, uint32_t pos
     if (i < n) out[i] = sv::uniform01(seed, row0 + (uint64_t)i, pos, purpose);
 }
 
-}  // namespace
-
-// Records a CUDA error for spec_last_cuda_error (used by other translation units).
-spec_status sv::note_cuda_error(cudaError_t e) { return cuda_fail(e); }
-
-extern "C" {
-
-int spec_version(void) { return 100; }
-
-const char* spec_status_string(spec_status s) {
-    switch (s) {
-        case SPEC_OK: return "SPEC_OK";
-        case SPEC_EINVAL: return "SPEC_EINVAL";
-        case SPEC_ECUDA: return "SPEC_ECUDA";
-        case SPEC_ETIMEOUT: return "SPEC_ETIMEOUT";
-        case SPEC_EDATA: return "SPEC_EDATA";
-    }
-    return "SPEC_UNKNOWN";
-}
-
-const char* spec_last_cuda_error(void) { return g_cuda_err; }
-
-size_t spec_verify_workspace_size(int B, int gamma, int V, spec_dtype dtype) {
-    (void)dtype;
-    if (B < 1 || gamma < 1 || V < 1) return 0;
-    return ws_layout(B, 2 * gamma + 1, V).total;
-}
-
-spec_status spec_verify(const void* target, const void* draft, spec_dtype dtype,
+spec_status verify_impl(const void* target, const void* draft, spec_dtype dtype,
                         const int32_t* draft_tokens, int B, int gamma, int V,
                         spec_sampling sampling, uint64_t seed, uint64_t offset,
                         int32_t* accepted, int32_t* tokens, int32_t* next_token,
                         int32_t* status, float* probs_dbg,
-                        void* workspace, size_t ws_bytes, spec_stream stream) {
+                        void* workspace, size_t ws_bytes, spec_stream stream, float lenience) {
     if (!dtype_ok(dtype) || !sampling_ok(sampling)) return SPEC_EINVAL;
+    if (!finite(lenience) || !(lenience > 0.f) || lenience > 1.f) return SPEC_EINVAL;
     if (B < 1 || B > (1 << 24) || gamma < 1 || gamma > SPEC_MAX_GAMMA || V < 1 || V > SPEC_MAX_V)
         return SPEC_EINVAL;
     const bool greedy = sampling.temperature == 0.f;
@@ -273,6 +246,7 @@ spec_status spec_verify(const void* target, const void* draft, spec_dtype dtype,
     p.top_k = sampling.top_k;
     p.top_p = sampling.top_p;
     p.c2 = kLog2e / sampling.temperature;
+    p.lenience = lenience;
     p.seed = seed;
     p.offset = offset;
     p.accepted = accepted;
@@ -282,6 +256,54 @@ spec_status spec_verify(const void* target, const void* draft, spec_dtype dtype,
     p.probs_dbg = probs_dbg;
     if (!std::isfinite(p.c2)) return SPEC_EINVAL;
     return run_rows(p, dt, workspace, w, st);
+}
+
+}  // namespace
+
+// Records a CUDA error for spec_last_cuda_error (used by other translation units).
+spec_status sv::note_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
+extern "C" {
+
+int spec_version(void) { return 100; }
+
+const char* spec_status_string(spec_status s) {
+    switch (s) {
+        case SPEC_OK: return "SPEC_OK";
+        case SPEC_EINVAL: return "SPEC_EINVAL";
+        case SPEC_ECUDA: return "SPEC_ECUDA";
+        case SPEC_ETIMEOUT: return "SPEC_ETIMEOUT";
+        case SPEC_EDATA: return "SPEC_EDATA";
+    }
+    return "SPEC_UNKNOWN";
+}
+
+const char* spec_last_cuda_error(void) { return g_cuda_err; }
+
+size_t spec_verify_workspace_size(int B, int gamma, int V, spec_dtype dtype) {
+    (void)dtype;
+    if (B < 1 || gamma < 1 || V < 1) return 0;
+    return ws_layout(B, 2 * gamma + 1, V).total;
+}
+
+spec_status spec_verify(const void* target, const void* draft, spec_dtype dtype,
+                        const int32_t* draft_tokens, int B, int gamma, int V,
+                        spec_sampling sampling, uint64_t seed, uint64_t offset,
+                        int32_t* accepted, int32_t* tokens, int32_t* next_token,
+                        int32_t* status, float* probs_dbg,
+                        void* workspace, size_t ws_bytes, spec_stream stream) {
+    return verify_impl(target, draft, dtype, draft_tokens, B, gamma, V, sampling, seed, offset, accepted,
+                       tokens, next_token, status, probs_dbg, workspace, ws_bytes, stream, 1.f);
+}
+
+spec_status spec_verify_lenient(const void* target, const void* draft, spec_dtype dtype,
+                                const int32_t* draft_tokens, int B, int gamma, int V,
+                                spec_sampling sampling, float lenience, uint64_t seed, uint64_t offset,
+                                int32_t* accepted, int32_t* tokens, int32_t* next_token,
+                                int32_t* status, float* probs_dbg,
+                                void* workspace, size_t ws_bytes, spec_stream stream) {
+    return verify_impl(target, draft, dtype, draft_tokens, B, gamma, V, sampling, seed, offset, accepted,
+                       tokens, next_token, status, probs_dbg, workspace, ws_bytes, stream, lenience);
 }
 
 size_t spec_verify_tree_workspace_size(int B, int N, int V, spec_dtype dtype) {
@@ -364,6 +386,7 @@ spec_status spec_verify_mentor(const void* target, const void* draft, spec_dtype
     p.V = V;
     p.rows_per_b = 2 * gamma + 1;
     p.mode = sv::kModeMentor;
+    p.lenience = 1.f;
     p.transform = 0;
     p.top_p = 1.f;
     p.c2 = c2;
@@ -441,6 +464,7 @@ spec_status spec_sample(const void* logits, spec_dtype dtype, int B, int P, int 
     p.V = V;
     p.rows_per_b = P;
     p.mode = sv::kModeSample;
+    p.lenience = 1.f;
     p.transform = transform_bits(sampling, V);
     p.top_k = sampling.top_k;
     p.top_p = sampling.top_p;

@@ -275,6 +275,7 @@ struct RowParams {
     int top_k;
     float top_p;
     float c2;         // log2(e) / T
+    float lenience;   // l in ]0, 1]: the draft probability is scaled by l (1: exact)
     uint64_t seed, offset;
     uint32_t pos0, purpose;  // sample mode
     int32_t* accepted;

@@ -183,8 +183,9 @@ struct ResidualW {
     SV_DEV float operator()(float zt, float zd) const { return fmaxf(0.f, q(zt) - p(zd)); }
 };
 
-SV_DEV ResidualW residual_weight(const RowRec& t, const RowRec& d, float c2) {
-    return ResidualW{KeptExp{t.thr, c2, t.m * c2, 1.f / t.Sk}, KeptExp{d.thr, c2, d.m * c2, 1.f / d.Sk}};
+// max(0, q - l p) with l the lenience (1: the exact residual (q - p)+).
+SV_DEV ResidualW residual_weight(const RowRec& t, const RowRec& d, float c2, float l = 1.f) {
+    return ResidualW{KeptExp{t.thr, c2, t.m * c2, 1.f / t.Sk}, KeptExp{d.thr, c2, d.m * c2, l * (1.f / d.Sk)}};
 }
 
 // Accept with probability min(1, q/p): u < q/p; p = 0 accepts iff q > 0.
@@ -202,12 +203,12 @@ SV_DEV int draw_q(DrawShared& ds, const E* row, int V, const RowRec& r, float c2
     return block_draw<E>(ds, row, (const E*)nullptr, V, u, [&](float zt, float) { return q(zt); }, &W);
 }
 
-// Residual draw x ~ max(0, q - p) over a target/draft row pair; from q when
-// the residual vanishes (q = p to rounding).
+// Residual draw x ~ max(0, q - l p) over a target/draft row pair (l = 1: the
+// exact residual); from q when the residual vanishes (q = l p to rounding).
 template <typename E>
 SV_DEV int draw_residual(DrawShared& ds, const E* rt, const E* rd, int V, const RowRec& t, const RowRec& d,
-                         float c2, float u) {
-    const ResidualW w = residual_weight(t, d, c2);
+                         float c2, float u, float l = 1.f) {
+    const ResidualW w = residual_weight(t, d, c2, l);
     float W;
     const int tok = block_draw<E>(ds, rt, rd, V, u, w, &W);
     if (W > 0.f) return tok;

@@ -842,7 +842,10 @@ __device__ __noinline__ void sample_row(Shared& s, const RowParams& p, const E* 
 
 // Sequence b, once all its rows have records: acceptance left to right up to
 // the first rejection n, then exactly one draw (the residual of position n,
-// or the bonus token from q_gamma), then the outputs.
+// or the bonus token from q_gamma), then the outputs. With lenience l the
+// test is u < q/(l p) and the residual max(0, q - l p) (the lenient variant
+// of "Fast Inference from Transformers via Speculative Decoding", method
+// details, extension of its appendix F); l = 1 is the exact method.
 template <typename E>
 __device__ __noinline__ void resolve_sequence(Shared& s, const RowParams& p, int b) {
     const int tid = threadIdx.x;
@@ -865,7 +868,7 @@ __device__ __noinline__ void resolve_sequence(Shared& s, const RowParams& p, int
             }
             if (n == G) {
                 const float u = uniform01(p.seed, p.offset + (uint64_t)b, (uint32_t)k, kPurposeAccept);
-                if (!accept_test(u, q, pd)) n = k;
+                if (!accept_test(u, q, p.lenience * pd)) n = k;
             }
         }
         s.bi[2] = n;
@@ -885,7 +888,8 @@ __device__ __noinline__ void resolve_sequence(Shared& s, const RowParams& p, int
         const RowRef<E> tr = row_ref<E>(p, b, n);
         if (n < G) {
             const RowRef<E> dr = row_ref<E>(p, b, G + 1 + n);
-            tok = draw_residual<E>(s.draw, tr.ptr, dr.ptr, p.V, s.u.rec[n], s.u.rec[G + 1 + n], p.c2, u2);
+            tok = draw_residual<E>(s.draw, tr.ptr, dr.ptr, p.V, s.u.rec[n], s.u.rec[G + 1 + n], p.c2, u2,
+                                   p.lenience);
         } else {
             tok = draw_q<E>(s.draw, tr.ptr, p.V, s.u.rec[G], p.c2, u2);
         }

@@ -93,3 +93,10 @@ def test_tree_mentor_sample_reject_bad_arguments(lib):
     S = lambda **k: lib.spec_sample(FAKE, 0, k.get("B", 2), k.get("P", 1), 100, k.get("s", SpecSampling(1, 1, 0)),
                                     0, 0, 0, 2, FAKE, None, FAKE, 1 << 30, None)
     assert S(B=0) == EINVAL and S(P=0) == EINVAL and S(s=SpecSampling(1, 2, 0)) == EINVAL
+
+
+@pytest.mark.parametrize("l", [0.0, -0.5, 1.5, float("nan"), float("inf")])
+def test_lenient_verify_rejects_bad_lenience(lib, l):
+    rc = lib.spec_verify_lenient(FAKE, FAKE, 0, FAKE, 2, 3, 100, SpecSampling(1.0, 1.0, 0), l, 0, 0,
+                                 FAKE, FAKE, FAKE, None, None, FAKE, 1 << 30, None)
+    assert rc == EINVAL
