@@ -78,7 +78,7 @@ void seg_plan(long long rows, int V, bool xf, int* nseg, int* seg_len) {
 struct Ws {
     size_t work, seq_cnt, row_cnt, row_zero_end;  // row kernel control
     size_t cnt64, rowbest, rowbad, arg_end;         // argmax control
-    size_t rows, segs, total;
+    size_t rows, segs, seqn, total;
     int nseg_max;
 };
 
@@ -106,6 +106,8 @@ Ws ws_layout(int B, int R, int V) {
     o = al(o + rows * sizeof(sv::RowRec));
     w.segs = o;
     if (w.nseg_max > 1) o = al(o + rows * w.nseg_max * sizeof(sv::SegRec));
+    w.seqn = o;
+    o = al(o + (size_t)B * sizeof(int32_t));
     w.total = o;
     return w;
 }
@@ -155,8 +157,10 @@ spec_status run_rows(sv::RowParams& p, int dtype, void* ws, const Ws& w, cudaStr
     p.row_cnt = at<unsigned int>(ws, w.row_cnt);
     p.seq_cnt = at<unsigned int>(ws, w.seq_cnt);
     p.work = at<unsigned int>(ws, w.work);
+    p.seq_n = at<int32_t>(ws, w.seqn);
     if (spec_status c = clear(ws, 0, w.row_zero_end, st)) return c;
-    const cudaError_t e = sv::launch_rows(p, dtype, device_sms(), st);
+    cudaError_t e = sv::launch_rows(p, dtype, device_sms(), st);
+    if (e == cudaSuccess && p.mode == sv::kModeVerify) e = sv::launch_draws(p, dtype, device_sms(), st);
     return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
 }
 

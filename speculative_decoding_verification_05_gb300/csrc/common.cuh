@@ -288,7 +288,8 @@ struct RowParams {
     SegRec* segs;           // [B * rows_per_b * nseg] (nseg > 1)
     unsigned int* row_cnt;  // [B * rows_per_b] segment arrivals (nseg > 1)
     unsigned int* seq_cnt;  // [B] row arrivals
-    unsigned int* work;     // next work unit (zero at launch)
+    unsigned int* work;     // [2] next work unit, next sequence to draw (zero at launch)
+    int32_t* seq_n;         // [B] accepted length of each resolved sequence (-1: bad data)
 };
 
 enum ArgmaxMode : int { kArgVerify = 0, kArgTree = 1, kArgSample = 2 };
@@ -341,6 +342,8 @@ struct MentorParams {
 // Host launchers (defined in the .cu files).
 // Persistent row kernel on up to `sms` x (resident CTAs per SM) CTAs.
 cudaError_t launch_rows(const RowParams& p, int dtype, int sms, cudaStream_t stream);
+// The one draw of every sequence the row kernel resolved (verification).
+cudaError_t launch_draws(const RowParams& p, int dtype, int sms, cudaStream_t stream);
 cudaError_t launch_argmax(const ArgmaxParams& p, int dtype, int grid, cudaStream_t stream);
 cudaError_t launch_mentor(const MentorParams& p, int grid, cudaStream_t stream);
 

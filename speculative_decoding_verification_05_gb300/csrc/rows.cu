@@ -841,9 +841,10 @@ __device__ __noinline__ void sample_row(Shared& s, const RowParams& p, const E* 
 }
 
 // Sequence b, once all its rows have records: acceptance left to right up to
-// the first rejection n, then exactly one draw (the residual of position n,
-// or the bonus token from q_gamma), then the outputs. With lenience l the
-// test is u < q/(l p) and the residual max(0, q - l p) (the lenient variant
+// the first rejection n, then the outputs except the one drawn token (the
+// residual of position n, or the bonus token from q_gamma), which the draw
+// kernel below writes; n (or -1 for a sequence with bad data) is left in
+// p.seq_n[b]. With lenience l the test is u < q/(l p) (the lenient variant
 // of "Fast Inference from Transformers via Speculative Decoding", method
 // details, extension of its appendix F); l = 1 is the exact method.
 template <typename E>
@@ -871,38 +872,56 @@ __device__ __noinline__ void resolve_sequence(Shared& s, const RowParams& p, int
                 if (!accept_test(u, q, p.lenience * pd)) n = k;
             }
         }
+        const int stt = (flags & kRecEData) ? kEData : kOk;
+        p.accepted[b] = stt ? -1 : n;
+        p.seq_n[b] = stt ? -1 : n;
+        if (stt) p.next_token[b] = -1;
+        if (p.status) p.status[b] = stt;
         s.bi[2] = n;
-        s.bi[3] = (flags & kRecEData) ? kEData : kOk;
-        if (!(flags & kRecEData)) {
-            // the one row pair (or bonus row) the draw reads: into L2 now
-            const size_t bytes = (size_t)p.V * sizeof(E);
-            prefetch_span_l2(row_ref<E>(p, b, n).ptr, bytes);
-            if (n < G) prefetch_span_l2(row_ref<E>(p, b, G + 1 + n).ptr, bytes);
-        }
+        s.bi[3] = stt;
     }
     __syncthreads();
     const int n = s.bi[2], stt = s.bi[3];
-    int tok = -1;
-    if (!stt) {
-        const float u2 = uniform01(p.seed, p.offset + (uint64_t)b, (uint32_t)n, kPurposeResample);
-        const RowRef<E> tr = row_ref<E>(p, b, n);
-        if (n < G) {
-            const RowRef<E> dr = row_ref<E>(p, b, G + 1 + n);
-            tok = draw_residual<E>(s.draw, tr.ptr, dr.ptr, p.V, s.u.rec[n], s.u.rec[G + 1 + n], p.c2, u2,
-                                   p.lenience);
-        } else {
-            tok = draw_q<E>(s.draw, tr.ptr, p.V, s.u.rec[G], p.c2, u2);
+    for (int j = tid; j <= G; j += NT)
+        if (stt || j != n) p.tokens[(size_t)b * (G + 1) + j] = (!stt && j < n) ? s.u.rec[j].x : -1;
+}
+
+// One draw per resolved sequence: the residual max(0, q_n - l p_n) after a
+// rejection at n, or the bonus token from q_gamma (with the same inverse CDF
+// as every other draw). Persistent CTAs take sequences from a counter; many
+// sequences are drawn at once, so the rounds' memory latency overlaps.
+template <typename E>
+__global__ void __launch_bounds__(NT, 4) draw_kernel(const __grid_constant__ RowParams p) {
+    __shared__ DrawShared ds;
+    __shared__ RowRec rec[2];
+    __shared__ int job;
+    const int tid = threadIdx.x;
+    const int R = p.rows_per_b, G = p.gamma;
+    unsigned* counter = p.work + 1;
+    for (;;) {
+        if (tid == 0) job = (int)atomicAdd(counter, 1u);
+        __syncthreads();
+        const int b = job;
+        if (b >= p.B) break;
+        const int n = p.seq_n[b];
+        if (n >= 0) {
+            if (tid == 0) rec[0] = load_rec(p.rows + (size_t)b * R + n);
+            if (tid == 1 && n < G) rec[1] = load_rec(p.rows + (size_t)b * R + G + 1 + n);
+            __syncthreads();
+            const float u2 = uniform01(p.seed, p.offset + (uint64_t)b, (uint32_t)n, kPurposeResample);
+            const E* rt = row_ref<E>(p, b, n).ptr;
+            int tok;
+            if (n < G)
+                tok = draw_residual<E>(ds, rt, row_ref<E>(p, b, G + 1 + n).ptr, p.V, rec[0], rec[1], p.c2, u2,
+                                       p.lenience);
+            else
+                tok = draw_q<E>(ds, rt, p.V, rec[0], p.c2, u2);
+            if (tid == 0) {
+                p.next_token[b] = tok;
+                p.tokens[(size_t)b * (G + 1) + n] = tok;
+            }
         }
-    }
-    if (tid == 0) {
-        p.accepted[b] = stt ? -1 : n;
-        p.next_token[b] = stt ? -1 : tok;
-        if (p.status) p.status[b] = stt;
-    }
-    for (int j = tid; j <= G; j += NT) {
-        int v = -1;
-        if (!stt) v = j < n ? s.u.rec[j].x : (j == n ? tok : -1);
-        p.tokens[(size_t)b * (G + 1) + j] = v;
+        __syncthreads();
     }
 }
 
@@ -1068,12 +1087,28 @@ cudaError_t launch_t(const RowParams& p, int sms, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+template <typename E>
+cudaError_t launch_draws_t(const RowParams& p, int sms, cudaStream_t stream) {
+    static const int per_sm = [] {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, draw_kernel<E>, NT, 0) != cudaSuccess || n < 1) n = 1;
+        return n;
+    }();
+    const int grid = (int)std::min<long long>(p.B, (long long)sms * per_sm);
+    draw_kernel<E><<<grid, NT, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_rows(const RowParams& p, int dtype, int sms, cudaStream_t stream) {
     const bool xf = p.transform != 0;
     if (dtype == 0) return xf ? launch_t<float, true>(p, sms, stream) : launch_t<float, false>(p, sms, stream);
     return xf ? launch_t<bf16_t, true>(p, sms, stream) : launch_t<bf16_t, false>(p, sms, stream);
+}
+
+cudaError_t launch_draws(const RowParams& p, int dtype, int sms, cudaStream_t stream) {
+    return dtype == 0 ? launch_draws_t<float>(p, sms, stream) : launch_draws_t<bf16_t>(p, sms, stream);
 }
 
 }  // namespace sv
