@@ -11,10 +11,10 @@
 //
 // The row is cut into rounds of NT * PER consecutive elements; inside a round
 // thread t owns PER consecutive elements. Pass 1 sums every round with a fixed
-// order (thread: left to right; warp: lanes left to right; round: warps left
-// to right) and keeps the per-warp totals; the crossing round is found from
-// the sequential round totals; pass 2 re-reads only that round and walks the
-// same hierarchy down to the element.
+// order (thread: left to right; warp: a butterfly over the lanes) and keeps
+// the per-warp totals; warp 0 adds the rounds in a fixed order (lane l owns
+// consecutive rounds) and finds the crossing round; pass 2 re-reads only that
+// round and walks warps, lanes and elements down to the token.
 #pragma once
 
 #include "common.cuh"
@@ -86,21 +86,30 @@ SV_DEV int block_draw(DrawShared& ds, const E* rt, const E* rd, int V, float u, 
     // pass 1: per-round, per-warp totals
     for (int r = 0; act && r < rounds; ++r) {
         float w[PER];
-        const float tsum = thread_sum(r, w);
-        float wsum;
-        warp_seq_exclusive(tsum, &wsum);
+        float wsum = thread_sum(r, w);
+        // butterfly: every lane ends with the same warp total, in a fixed order
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) wsum += __shfl_xor_sync(0xFFFFFFFFu, wsum, o);
         if (lane == 0) ds.wt[r][warp] = wsum;
     }
     __syncthreads();
-    if (tid == 0) {
-        float W = 0.f;
-        for (int r = 0; r < rounds; ++r)
-            for (int w = 0; w < kDrawNW; ++w) W += ds.wt[r][w];
+    if (warp == 0) {
+        // round totals in a fixed order; lane l owns rounds [l * per, (l + 1) * per)
+        const int per = (rounds + 31) / 32;
+        const int q0 = min(rounds, lane * per), q1 = min(rounds, q0 + per);
+        float lsum = 0.f;
+        for (int r = q0; r < q1; ++r) {
+            float R = 0.f;
+            for (int w = 0; w < kDrawNW; ++w) R += ds.wt[r][w];
+            lsum += R;
+        }
+        float W;
+        const float lpre = warp_seq_exclusive(lsum, &W);
         const float t = u * W;
         // the round holding the crossing: the last round whose start <= t with positive weight
-        float carry = 0.f, rem = 0.f;
+        float carry = lpre, rem = 0.f;
         int rr = -1;
-        for (int r = 0; r < rounds; ++r) {
+        for (int r = q0; r < q1; ++r) {
             float R = 0.f;
             for (int w = 0; w < kDrawNW; ++w) R += ds.wt[r][w];
             if (carry <= t && R > 0.f) {
@@ -109,10 +118,13 @@ SV_DEV int block_draw(DrawShared& ds, const E* rt, const E* rd, int V, float u, 
             }
             carry += R;
         }
-        ds.W = W;
-        ds.round = rr;
-        ds.rem = rem;
-        ds.token = -1;
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, rr >= 0);
+        if (lane == (m ? 31 - __clz(m) : 0)) {
+            ds.W = W;
+            ds.round = rr;
+            ds.rem = rem;
+            ds.token = -1;
+        }
     }
     __syncthreads();
     const int rr = ds.round;

@@ -891,7 +891,7 @@ __device__ __noinline__ void resolve_sequence(Shared& s, const RowParams& p, int
 // as every other draw). Persistent CTAs take sequences from a counter; many
 // sequences are drawn at once, so the rounds' memory latency overlaps.
 template <typename E>
-__global__ void __launch_bounds__(NT, 4) draw_kernel(const __grid_constant__ RowParams p) {
+__global__ void __launch_bounds__(NT, 6) draw_kernel(const __grid_constant__ RowParams p) {
     __shared__ DrawShared ds;
     __shared__ RowRec rec[2];
     __shared__ int job;
