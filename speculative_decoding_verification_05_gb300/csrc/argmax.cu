@@ -69,6 +69,25 @@ struct SharedA {
     int bi[8];
 };
 
+// NaN-propagating maximum of the logits of one 16-byte vector.
+SV_DEV float vec_max(const uint4& v, float) {
+    float a, b, r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(a) : "f"(__uint_as_float(v.x)), "f"(__uint_as_float(v.y)));
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(b) : "f"(__uint_as_float(v.z)), "f"(__uint_as_float(v.w)));
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+SV_DEV float vec_max(const uint4& v, bf16_t) {
+    uint32_t a, b, m;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(a) : "r"(v.x), "r"(v.y));
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(b) : "r"(v.z), "r"(v.w));
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(a), "r"(b));
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(__uint_as_float(m << 16)), "f"(__uint_as_float(m & 0xFFFF0000u)));
+    return r;
+}
+
 template <typename E>
 SV_DEV void segment(const ArgmaxParams& p, SharedA& s, long long r, int i0, int i1) {
     using T = VecTraits<E>;
@@ -97,13 +116,20 @@ SV_DEV void segment(const ArgmaxParams& p, SharedA& s, long long r, int i0, int 
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (j + u * NT < nb) {
-                float x[VE];
-                T::unpack(v[u], x);
-                const int i = base + (j + u * NT) * VE;
+                // the vector's maximum decides; the index is looked up only when it
+                // beats this thread's best (vectors come in increasing index order,
+                // so equal values keep the lower index)
+                const float vm = vec_max(v[u], E{});
+                bad |= !(vm < INFINITY);
+                if (vm > best.v || best.i < 0) {
+                    float x[VE];
+                    T::unpack(v[u], x);
+                    int e0 = VE - 1;
 #pragma unroll
-                for (int e = 0; e < VE; ++e) {
-                    bad |= !(x[e] < INFINITY);
-                    take(best, x[e], i + e);
+                    for (int e = VE - 1; e >= 0; --e)
+                        if (x[e] == vm) e0 = e;
+                    best.v = vm;
+                    best.i = base + (j + u * NT) * VE + e0;
                 }
             }
         }
