@@ -136,6 +136,12 @@ struct Collect {
             ++hc;
         }
     }
+    // Branch-free form for when at least one slot is free: the key is always
+    // written to the next slot and kept only if it passes the cut.
+    SV_DEV void put(float x, uint32_t raw) {
+        base[hc * NT] = (K)raw;
+        hc += x > cut;
+    }
 };
 
 template <typename E>
@@ -146,6 +152,7 @@ template <>
 struct Core<bf16_t> {
     static constexpr int VE = 8;
     using Key = uint16_t;
+    static constexpr int kPer = kSlotBytes / (int)sizeof(Key);
     struct St {
         uint32_t pm;
         float2 s0, s1;
@@ -161,14 +168,25 @@ struct Core<bf16_t> {
         float2 a0 = make_float2(bf_lo(v.x), bf_hi(v.x)), a1 = make_float2(bf_lo(v.y), bf_hi(v.y));
         float2 a2 = make_float2(bf_lo(v.z), bf_hi(v.z)), a3 = make_float2(bf_lo(v.w), bf_hi(v.w));
         if (COL) {
-            col(a0.x, v.x & 0xFFFFu);
-            col(a0.y, v.x >> 16);
-            col(a1.x, v.y & 0xFFFFu);
-            col(a1.y, v.y >> 16);
-            col(a2.x, v.z & 0xFFFFu);
-            col(a2.y, v.z >> 16);
-            col(a3.x, v.w & 0xFFFFu);
-            col(a3.y, v.w >> 16);
+            if (col.hc <= C::kPer - 8) {  // room for the whole vector
+                col.put(a0.x, v.x);
+                col.put(a0.y, v.x >> 16);
+                col.put(a1.x, v.y);
+                col.put(a1.y, v.y >> 16);
+                col.put(a2.x, v.z);
+                col.put(a2.y, v.z >> 16);
+                col.put(a3.x, v.w);
+                col.put(a3.y, v.w >> 16);
+            } else {
+                col(a0.x, v.x & 0xFFFFu);
+                col(a0.y, v.x >> 16);
+                col(a1.x, v.y & 0xFFFFu);
+                col(a1.y, v.y >> 16);
+                col(a2.x, v.z & 0xFFFFu);
+                col(a2.y, v.z >> 16);
+                col(a3.x, v.w & 0xFFFFu);
+                col(a3.y, v.w >> 16);
+            }
         }
         a0 = __ffma2_rn(a0, c2v, nr2);
         a1 = __ffma2_rn(a1, c2v, nr2);
