@@ -720,84 +720,91 @@ __device__ __noinline__ bool bf16_threshold(Shared& s, const RowParams& p, float
     if (lane == 0 && jm >= 0) atomicMax(&s.jmax, jm);
     __syncthreads();
     const int jz = s.jmax;
-    if (warp == 0) {
-        bool ok = true;
-        const int nbins = jz + 1;
-        const int per = (nbins + 31) / 32;
-        const int j0 = min(nbins, lane * per), j1 = min(nbins, j0 + per);
-        auto mass_of = [&](int j, unsigned c) {
-            return (unsigned long long)c * fx_of(fmaf(ord16_value((uint32_t)(top - j)), c2, -mc));
-        };
-        unsigned long long tc = 0ull, tw = 0ull;
-        for (int j = j0; j < j1; ++j) {
-            const unsigned c = s.h.ocnt[j];
-            if (c) {
-                tc += c;
-                tw += mass_of(j, c);
-            }
+    // every thread owns a few consecutive bins; an exclusive scan of (count,
+    // mass) in thread order gives each thread its running weights
+    const int nbins = jz + 1;
+    const int per = (nbins + NT - 1) / NT;
+    const int j0 = min(nbins, tid * per), j1 = min(nbins, j0 + per);
+    auto mass_of = [&](int j, unsigned c) {
+        return (unsigned long long)c * fx_of(fmaf(ord16_value((uint32_t)(top - j)), c2, -mc));
+    };
+    unsigned long long tc = 0ull, tw = 0ull;
+    for (int j = j0; j < j1; ++j) {
+        const unsigned c = s.h.ocnt[j];
+        if (c) {
+            tc += c;
+            tw += mass_of(j, c);
         }
-        unsigned long long ic = tc, iw = tw;
+    }
+    unsigned long long ic = tc, iw = tw;
 #pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const unsigned long long yc = __shfl_up_sync(0xFFFFFFFFu, ic, d);
-            const unsigned long long yw = __shfl_up_sync(0xFFFFFFFFu, iw, d);
-            if (lane >= d) {
-                ic += yc;
-                iw += yw;
-            }
+    for (int d = 1; d < 32; d <<= 1) {
+        const unsigned long long yc = __shfl_up_sync(0xFFFFFFFFu, ic, d);
+        const unsigned long long yw = __shfl_up_sync(0xFFFFFFFFu, iw, d);
+        if (lane >= d) {
+            ic += yc;
+            iw += yw;
         }
-        const unsigned long long ec = ic - tc, ew = iw - tw;
-        // the first non-empty bin j <= jlim whose running weight reaches target
-        auto find = [&](bool by_count, unsigned long long target, int jlim, int* jo, unsigned long long* wo) {
-            unsigned long long c = ec, w = ew, hw = 0ull;
-            int hit = -1;
-            for (int j = j0; j < j1 && hit < 0; ++j) {
+    }
+    if (lane == 31) {
+        s.ured[warp] = ic;
+        s.ured2[warp] = iw;
+    }
+    if (tid == 0) s.bi[5] = -1;
+    __syncthreads();
+    unsigned long long ec = ic - tc, ew = iw - tw;
+    for (int w = 0; w < warp; ++w) {
+        ec += s.ured[w];
+        ew += s.ured2[w];
+    }
+    // the first non-empty bin j <= jlim whose running weight reaches target:
+    // found by the one thread whose bins hold it
+    auto find = [&](bool by_count, unsigned long long target, int jlim, int* jo, unsigned long long* wo) {
+        if ((by_count ? ec : ew) < target) {
+            unsigned long long c = ec, w = ew;
+            for (int j = j0; j < j1 && j <= jlim; ++j) {
                 const unsigned k = s.h.ocnt[j];
                 if (!k) continue;
                 c += k;
                 w += mass_of(j, k);
-                if (j <= jlim && (by_count ? c : w) >= target) {
-                    hit = j;
-                    hw = w;
+                if ((by_count ? c : w) >= target) {
+                    s.bi[5] = j;
+                    s.ured[NW] = w;
+                    break;
                 }
             }
-            const unsigned bal = __ballot_sync(0xFFFFFFFFu, hit >= 0);
-            if (!bal) return false;
-            const int src = __ffs(bal) - 1;
-            *jo = __shfl_sync(0xFFFFFFFFu, hit, src);
-            *wo = __shfl_sync(0xFFFFFFFFu, hw, src);
-            return true;
-        };
-        unsigned long long kept = (unsigned long long)(S * kFx);
-        float t = -INFINITY;
-        int jk = nbins - 1;
-        if (ok && (p.transform & kXfTopK)) {
-            unsigned long long w;
-            ok = find(true, (unsigned long long)p.top_k, nbins - 1, &jk, &w);
-            if (ok) {
-                t = ord16_value((uint32_t)(top - jk));
-                kept = w;
-            }
         }
-        if (ok && (p.transform & kXfTopP)) {
-            int j;
-            unsigned long long w;
-            ok = find(false, top_p_target(p.top_p, kept), jk, &j, &w);
-            if (ok) {
-                t = ord16_value((uint32_t)(top - j));
-                kept = w;
-            }
-        }
-        if (lane == 0) {
-            s.bi[5] = ok;
-            s.bf[5] = t;
-            s.ured[NW] = kept;
+        __syncthreads();
+        *jo = s.bi[5];
+        *wo = s.ured[NW];
+        __syncthreads();
+        if (tid == 0) s.bi[5] = -1;
+        return *jo >= 0;
+    };
+    unsigned long long kept = (unsigned long long)(S * kFx);
+    float t = -INFINITY;
+    int jk = nbins - 1;
+    bool ok = true;
+    if (p.transform & kXfTopK) {
+        unsigned long long w;
+        ok = find(true, (unsigned long long)p.top_k, nbins - 1, &jk, &w);
+        if (ok) {
+            t = ord16_value((uint32_t)(top - jk));
+            kept = w;
         }
     }
-    __syncthreads();
-    const bool ok = s.bi[5] != 0;
-    *thr = s.bf[5];
-    *sk = (float)s.ured[NW] * (1.0f / kFx);
+    if (ok && (p.transform & kXfTopP)) {
+        int j;
+        unsigned long long w;
+        if (p.transform & kXfTopK) __syncthreads();  // s.bi[5] reset before the second search
+        ok = find(false, top_p_target(p.top_p, kept), jk, &j, &w);
+        if (ok) {
+            t = ord16_value((uint32_t)(top - j));
+            kept = w;
+        }
+    }
+    *thr = t;
+    *sk = (float)kept * (1.0f / kFx);
     for (int j = tid; j <= jz; j += NT) s.h.ocnt[j] = 0u;  // clean for the next row
     if (tid == 0) s.jmax = -1;
     return ok;
