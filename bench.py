@@ -52,10 +52,13 @@ WORKLOADS = {
 }
 LENIENCE = {"nucleus_lenient": 0.5}   # lenient verification (l < 1); others are exact
 
-KERNEL_OF = {"nucleus": "row_kernel<bf16,transform>", "tiny": "row_kernel<f32>",
-             "large_vocab": "row_kernel<f32>", "large_vocab_t0": "argmax_kernel<f32>",
-             "tree": "argmax_kernel<f32>", "mentor": "row_kernel<f32> + mentor_kernel",
-             "nucleus_lenient": "row_kernel<bf16,transform>"}
+# The timed unit is one library call; where a call launches several kernels the
+# label names them all (the row or argmax kernel reads every logit byte).
+KERNEL_OF = {"nucleus": "row_kernel<bf16,transform> + draw_kernel", "tiny": "row_kernel<f32> + draw_kernel",
+             "large_vocab": "row_kernel<f32> + draw_kernel", "large_vocab_t0": "argmax_kernel<f32>",
+             "tree": "argmax_kernel<f32>",
+             "mentor": "row_kernel<f32> + mentor_kernel + mentor_resolve_kernel",
+             "nucleus_lenient": "row_kernel<bf16,transform> + draw_kernel"}
 
 
 def dist_env():
@@ -186,7 +189,13 @@ def algorithmic(inp):
 
 
 def launches_per_step(inp):
-    return 2 if inp["kind"] == "mentor" else 1
+    """Kernels one library call launches: rows, position solve and resolve
+    (mentor); the argmax kernel (tree, T = 0); rows and draws otherwise."""
+    if inp["kind"] == "mentor":
+        return 3
+    if inp["kind"] == "tree" or inp["T"] == 0:
+        return 1
+    return 2
 
 
 def cpu_baseline(name, temperature, budget_s=12.0, lenience=1.0):

@@ -121,7 +121,7 @@ constexpr int kMentorSlots = 152;
 
 struct MentorWs {
     Ws lin;
-    size_t keys, idx, arr, total;
+    size_t keys, idx, arr, pos_state, pos_beta, total;
     int slots;
 };
 
@@ -129,13 +129,17 @@ MentorWs mentor_ws(int B, int gamma, int V) {
     MentorWs w;
     w.lin = ws_layout(B, 2 * gamma + 1, V);
     size_t o = w.lin.total;
-    w.slots = std::min(B, kMentorSlots);
+    w.slots = (int)std::min<long long>((long long)B * gamma, kMentorSlots);
     w.keys = o;
     o = al(o + (size_t)w.slots * 2 * V * 4);
     w.idx = o;
     o = al(o + (size_t)w.slots * 2 * V * 4);
     w.arr = o;
     o = al(o + (size_t)w.slots * 7 * V * 4);
+    w.pos_state = o;
+    o = al(o + (size_t)B * gamma * 4);
+    w.pos_beta = o;
+    o = al(o + (size_t)B * gamma * 4);
     w.total = o;
     return w;
 }
@@ -416,7 +420,11 @@ spec_status spec_verify_mentor(const void* target, const void* draft, spec_dtype
     m.keys = at<uint32_t>(workspace, w.keys);
     m.idx = at<uint32_t>(workspace, w.idx);
     m.arr = at<float>(workspace, w.arr);
-    m.work = at<unsigned int>(workspace, w.lin.work) + 1;  // cleared with the row kernel's control
+    // both cleared with the row kernel's control; mentor mode uses neither
+    m.work = at<unsigned int>(workspace, w.lin.work) + 1;
+    m.rejmark = at<unsigned int>(workspace, w.lin.seq_cnt);
+    m.pos_state = at<int32_t>(workspace, w.pos_state);
+    m.pos_beta = at<float>(workspace, w.pos_beta);
     m.accepted = accepted;
     m.tokens = tokens;
     m.next_token = next_token;
@@ -424,7 +432,7 @@ spec_status spec_verify_mentor(const void* target, const void* draft, spec_dtype
     m.alpha_out = alpha_out;
     m.beta_out = beta_out;
     m.probs_dbg = probs_dbg;
-    const cudaError_t e = sv::launch_mentor(m, std::min(w.slots, device_sms()), st);
+    const cudaError_t e = sv::launch_mentor(m, std::min(w.slots, device_sms()), device_sms() * 8, st);
     return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
 }
 

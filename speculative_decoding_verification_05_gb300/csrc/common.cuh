@@ -329,7 +329,10 @@ struct MentorParams {
     uint32_t* keys;       // scratch per slot: [2][V] keys
     uint32_t* idx;        // scratch per slot: [2][V] indices
     float* arr;           // scratch per slot: [7][V] sorted arrays
-    unsigned int* work;   // next sequence (zero at launch)
+    unsigned int* work;   // next (sequence, position) job (zero at launch)
+    unsigned int* rejmark;  // [B]: max over rejected positions k of gamma - k (zero at launch)
+    int32_t* pos_state;   // [B, gamma]: outcome of each solved position
+    float* pos_beta;      // [B, gamma]: beta of each solved position
     int32_t* accepted;
     int32_t* tokens;
     int32_t* next_token;
@@ -345,6 +348,7 @@ cudaError_t launch_rows(const RowParams& p, int dtype, int sms, cudaStream_t str
 // The one draw of every sequence the row kernel resolved (verification).
 cudaError_t launch_draws(const RowParams& p, int dtype, int sms, cudaStream_t stream);
 cudaError_t launch_argmax(const ArgmaxParams& p, int dtype, int grid, cudaStream_t stream);
-cudaError_t launch_mentor(const MentorParams& p, int grid, cudaStream_t stream);
+// Position kernel on `grid` persistent CTAs, then the per-sequence resolve.
+cudaError_t launch_mentor(const MentorParams& p, int grid, int resolve_grid, cudaStream_t stream);
 
 }  // namespace sv

@@ -14,14 +14,16 @@
 //   KL(alpha) = ln(alpha) cq_{k-1} + (cl_{m-1} - cl_{k-1}) + ln(beta) sq_m.
 //
 // The row kernel has already written every row's record (maximum, sum, the
-// draft token's logit). Here one CTA (1024 threads, persistent) takes one
-// sequence at a time and walks its positions left to right, solving only the
-// positions that reach the solver, up to the first rejection. The sort is a
-// stable LSD radix sort (four 8-bit digit passes) of the fp32 keys of ln(rho)
-// in global scratch. The bisection's result (the smallest dyadic
-// alpha = j 2^-iters with KL(alpha) <= D) is found by a multiway search: each
-// round evaluates KL at up to 1023 interior grid points of the current
-// interval in parallel, ten bisection steps at a time. Rejections with
+// draft token's logit). Each position's outcome depends only on its own rows
+// and its own uniforms, so the position kernel (1024 threads, one persistent
+// CTA per SM) solves (sequence, position) jobs independently, skipping a job
+// once an earlier position of its sequence is known to be rejected; the
+// resolve kernel then finds each sequence's first rejection and makes its one
+// draw. The sort is a stable LSD radix sort (four 8-bit digit passes) of the
+// fp32 keys of ln(rho) in global scratch. The bisection's result (the smallest
+// dyadic alpha = j 2^-iters with KL(alpha) <= D) is found by a multiway
+// search: each round evaluates KL at up to 1023 interior grid points of the
+// current interval in parallel, ten bisection steps at a time. Rejections with
 // alpha = 1 (beta = 1) and the bonus token use the verification path's own
 // draw, so D = 0 reproduces spec_verify bit for bit.
 
@@ -42,8 +44,8 @@ struct SharedM {
     uint32_t base[256];
     double dred[NW];
     float fred[NW];
-    float warp_tot[NW];
-    float warp_pre[NW + 1];
+    float wsum[5][NW];           // solve: per-warp chunk totals
+    float woff[5][NW];           //        and chunk offsets
     int ibuf[NW];
     int bi[8];
     float bf[8];
@@ -61,30 +63,6 @@ SV_DEV double block_sum_d(SharedM& s, double v) {
     for (int w = 0; w < NW; ++w) t += s.dred[w];
     __syncthreads();
     return t;
-}
-
-// Inclusive scan over the flattened order (thread chunks in thread order),
-// sequential inside each thread and warp, so every running sum is an ordinary
-// left-to-right sum of the previous partial sums. Returns the thread's
-// exclusive prefix.
-SV_DEV float block_excl(SharedM& s, float thr_sum) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    float wt;
-    const float lp = warp_seq_exclusive(thr_sum, &wt);
-    if (lane == 0) s.warp_tot[warp] = wt;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float acc = 0.f;
-        for (int w = 0; w < NW; ++w) {
-            s.warp_pre[w] = acc;
-            acc += s.warp_tot[w];
-        }
-        s.warp_pre[NW] = acc;
-    }
-    __syncthreads();
-    const float r = s.warp_pre[warp] + lp;
-    __syncthreads();
-    return r;
 }
 
 template <typename E>
@@ -119,7 +97,14 @@ SV_DEV void radix_sort(SharedM& s, uint32_t* k0, uint32_t* i0, uint32_t* k1, uin
         // digit histogram -> exclusive bucket starts
         for (int d = tid; d < 256; d += NT) s.base[d] = 0;
         __syncthreads();
-        for (int i = tid; i < n; i += NT) atomicAdd(&s.base[(__ldcg(sk + i) >> shift) & 255u], 1u);
+        for (int ib = tid; ib < n; ib += NT * 8) {  // eight loads in flight per thread
+            uint32_t kk[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) kk[u] = ib + u * NT < n ? __ldcg(sk + ib + u * NT) : 0u;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (ib + u * NT < n) atomicAdd(&s.base[(kk[u] >> shift) & 255u], 1u);
+        }
         __syncthreads();
         if (warp == 0) {
             uint32_t c[8], seg = 0;
@@ -256,7 +241,8 @@ SV_DEV int first_g_le(const Arrays& a, double R) {
 }
 
 SV_DEV double kl_at(const Arrays& a, double alpha, double* beta_out) {
-    const int k = count_less(a, log(alpha));
+    const double lna = (double)logf((float)alpha);  // fp32 log: ~1e-7, far inside the KL tolerance
+    const int k = count_less(a, lna);
     const double qlow = k ? (double)__ldcg(a.CQ + k - 1) : 0.0;
     const double plow = k ? (double)__ldcg(a.CP + k - 1) : 0.0;
     const double llow = k ? (double)__ldcg(a.CL + k - 1) : 0.0;
@@ -267,7 +253,7 @@ SV_DEV double kl_at(const Arrays& a, double alpha, double* beta_out) {
     const double beta = sqm / (R + spm);
     const double lmid = (m ? (double)__ldcg(a.CL + m - 1) : 0.0) - llow;
     if (beta_out) *beta_out = beta;
-    return log(alpha) * qlow + lmid + log(beta) * sqm;
+    return lna * qlow + lmid + (double)logf((float)beta) * sqm;
 }
 
 // Solves one row pair: alpha (the bisection result) and beta. kl0 > D > 0.
@@ -286,49 +272,124 @@ SV_DEV void solve(SharedM& s, float* coarse, const MentorParams& p, const Row<E>
     float* SQ = A + 4 * (size_t)V;
     float* SP = A + 5 * (size_t)V;
     float* Gg = A + 6 * (size_t)V;
-    const int per = (V + NT - 1) / NT;
-    const int j0 = tid * per, j1 = min(V, j0 + per);
-    float tq = 0.f, tp = 0.f, tl = 0.f;
-    for (int j = j0; j < j1; ++j) {
-        float q, pp, l;
-        qpl(r, (int)__ldcg(i0 + j), q, pp, l);
-        L[j] = l;
-        tq += q;
-        tp += pp;
-        tl += q * l;
+    // q, p and ln rho per index were left in CQ, CP, CL by the KL pass. Warp w
+    // owns the contiguous chunk [w cw, (w + 1) cw) of sorted positions and
+    // walks it 32 positions at a time, so every pass below is coalesced.
+    const int lane = tid & 31, warp = tid >> 5;
+    const int cw = ((V + NW - 1) / NW + 31) & ~31;
+    const int w0 = min(V, warp * cw), w1 = min(V, w0 + cw);
+    // gather into sorted order: L, and q, p in the SQ, SP slots
+    for (int jb = w0; jb < w1; jb += 4 * 32) {
+        int idx[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int j = jb + u * 32 + lane;
+            idx[u] = j < w1 ? (int)__ldcg(i0 + j) : -1;
+        }
+        float lv[4], qv[4], pv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (idx[u] >= 0) {
+                lv[u] = __ldcg(CL + idx[u]);
+                qv[u] = __ldcg(CQ + idx[u]);
+                pv[u] = __ldcg(CP + idx[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (idx[u] >= 0) {
+                const int j = jb + u * 32 + lane;
+                L[j] = lv[u];
+                SQ[j] = qv[u];
+                SP[j] = pv[u];
+            }
+        }
     }
-    float eq = block_excl(s, tq), ep = block_excl(s, tp), el = block_excl(s, tl);
-    for (int j = j0; j < j1; ++j) {
-        float q, pp, l;
-        qpl(r, (int)__ldcg(i0 + j), q, pp, l);
-        eq += q;
-        ep += pp;
-        el += q * l;
-        CQ[j] = eq;
-        CP[j] = ep;
-        CL[j] = el;
+    __syncthreads();
+    // chunk-local prefix sums (q, p, q ln rho) and suffix sums (q, p): a warp
+    // scan per 32 positions plus a running carry
+    {
+        float cq = 0.f, cp = 0.f, cl = 0.f;
+        for (int jb = w0; jb < w1; jb += 32) {
+            const int j = jb + lane;
+            const bool ok = j < w1;
+            float q = ok ? __ldcg(SQ + j) : 0.f, pp = ok ? __ldcg(SP + j) : 0.f;
+            float ql = ok ? q * __ldcg(L + j) : 0.f;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float a1 = __shfl_up_sync(0xFFFFFFFFu, q, o), a2 = __shfl_up_sync(0xFFFFFFFFu, pp, o),
+                            a3 = __shfl_up_sync(0xFFFFFFFFu, ql, o);
+                if (lane >= o) {
+                    q += a1;
+                    pp += a2;
+                    ql += a3;
+                }
+            }
+            if (ok) {
+                CQ[j] = cq + q;
+                CP[j] = cp + pp;
+                CL[j] = cl + ql;
+            }
+            cq += __shfl_sync(0xFFFFFFFFu, q, 31);
+            cp += __shfl_sync(0xFFFFFFFFu, pp, 31);
+            cl += __shfl_sync(0xFFFFFFFFu, ql, 31);
+        }
+        float sq = 0.f, sp = 0.f;
+        for (int jb = w0 + ((w1 - w0 - 1) & ~31); w1 > w0 && jb >= w0; jb -= 32) {
+            const int j = jb + lane;
+            const bool ok = j < w1;
+            float q = ok ? __ldcg(SQ + j) : 0.f, pp = ok ? __ldcg(SP + j) : 0.f;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float a1 = __shfl_down_sync(0xFFFFFFFFu, q, o), a2 = __shfl_down_sync(0xFFFFFFFFu, pp, o);
+                if (lane + o < 32) {
+                    q += a1;
+                    pp += a2;
+                }
+            }
+            if (ok) {
+                SQ[j] = sq + q;
+                SP[j] = sp + pp;
+            }
+            sq += __shfl_sync(0xFFFFFFFFu, q, 0);
+            sp += __shfl_sync(0xFFFFFFFFu, pp, 0);
+        }
+        if (lane == 0) {
+            s.wsum[0][warp] = cq;
+            s.wsum[1][warp] = cp;
+            s.wsum[2][warp] = cl;
+            s.wsum[3][warp] = sq;
+            s.wsum[4][warp] = sp;
+        }
+    }
+    __syncthreads();
+    // chunk offsets in a fixed order: prefixes left to right, suffixes right to left
+    if (tid < 5) {
+        float acc = 0.f;
+        if (tid < 3) {
+            for (int w = 0; w < NW; ++w) {
+                s.woff[tid][w] = acc;
+                acc += s.wsum[tid][w];
+            }
+        } else {
+            for (int w = NW - 1; w >= 0; --w) {
+                s.woff[tid][w] = acc;
+                acc += s.wsum[tid][w];
+            }
+        }
     }
     __syncthreads();
     {
-        // reverse order: thread NT-1-tid, chunk walked backwards
-        const int rt = NT - 1 - tid;
-        const int rj0 = rt * per, rj1 = min(V, rj0 + per);
-        float sq = 0.f, sp = 0.f;
-        for (int j = rj1 - 1; j >= rj0; --j) {
-            float q, pp, l;
-            qpl(r, (int)__ldcg(i0 + j), q, pp, l);
-            sq += q;
-            sp += pp;
-        }
-        float xq = block_excl(s, sq), xp = block_excl(s, sp);
-        for (int j = rj1 - 1; j >= rj0; --j) {
-            float q, pp, l;
-            qpl(r, (int)__ldcg(i0 + j), q, pp, l);
-            xq += q;
-            xp += pp;
-            SQ[j] = xq;
-            SP[j] = xp;
-            Gg[j] = xq * ex2(-l * 1.4426950408889634f) - xp;
+        const float oq = s.woff[0][warp], op = s.woff[1][warp], ol = s.woff[2][warp];
+        const float xq = s.woff[3][warp], xp = s.woff[4][warp];
+        for (int j = w0 + lane; j < w1; j += 32) {
+            CQ[j] = oq + __ldcg(CQ + j);
+            CP[j] = op + __ldcg(CP + j);
+            CL[j] = ol + __ldcg(CL + j);
+            const float sqj = xq + __ldcg(SQ + j), spj = xp + __ldcg(SP + j);
+            SQ[j] = sqj;
+            SP[j] = spj;
+            Gg[j] = sqj * ex2(-__ldcg(L + j) * 1.4426950408889634f) - spj;
         }
     }
     __threadfence_block();
@@ -386,6 +447,17 @@ SV_DEV void solve(SharedM& s, float* coarse, const MentorParams& p, const Row<E>
     }
 }
 
+// Position states left for the resolve kernel.
+constexpr int kPosAccepted = 1;
+constexpr int kPosRejected = 0;        // rejected by the standard test (alpha = 1, beta = 1)
+constexpr int kPosRejectedScaled = 2;  // rejected with alpha < 1: resample from max(0, q/beta - p)
+
+// One job per (sequence, position), position-major, so every sequence's first
+// position is taken before any second one. Each position's outcome depends
+// only on its own rows and its own uniforms, so positions are solved
+// independently; a job whose sequence already has an earlier rejection on
+// record is skipped (its outcome cannot matter). Positions up to the first
+// rejection are never skipped.
 template <typename E>
 __global__ void __launch_bounds__(NT, 1) mentor_kernel(const __grid_constant__ MentorParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -402,112 +474,154 @@ __global__ void __launch_bounds__(NT, 1) mentor_kernel(const __grid_constant__ M
     float* A = p.arr + slot * 7 * (size_t)V;
     const E* tgt = reinterpret_cast<const E*>(p.target);
     const E* dft = reinterpret_cast<const E*>(p.draft);
+    const long long jobs = (long long)p.B * G;
 
     for (;;) {
         if (tid == 0) s.bi[4] = (int)atomicAdd(p.work, 1u);
         __syncthreads();
-        const int b = s.bi[4];
-        if (b >= p.B) break;
+        const long long job = s.bi[4];
+        if (job >= jobs) break;
+        const int k = (int)(job / p.B), b = (int)(job % p.B);
+        const size_t pos = (size_t)b * G + k;
         const RowRec* rb = p.rows + (size_t)b * R;
-        int flags = 0;
-        for (int i = 0; i < R; ++i) flags |= __ldcg(&rb[i].flags);
-        const bool bad = (flags & kRecEData) != 0;
-        if (p.probs_dbg) {
-            for (int k = tid; k < G; k += NT) {
-                const RowRec t = load_rec(rb + k), d = load_rec(rb + G1 + k);
-                p.probs_dbg[((size_t)b * G + k) * 2 + 0] = KeptExp{t.thr, c2, t.m * c2, 1.f}(t.zx) / t.Sk;
-                p.probs_dbg[((size_t)b * G + k) * 2 + 1] = KeptExp{d.thr, c2, d.m * c2, 1.f}(d.zx) / d.Sk;
-            }
+        const RowRec t = load_rec(rb + k), d = load_rec(rb + G1 + k);
+        const float q = KeptExp{t.thr, c2, t.m * c2, 1.f}(t.zx) / t.Sk;
+        const float pd = KeptExp{d.thr, c2, d.m * c2, 1.f}(d.zx) / d.Sk;
+        if (p.probs_dbg && tid == 0) {
+            p.probs_dbg[pos * 2 + 0] = q;
+            p.probs_dbg[pos * 2 + 1] = pd;
         }
-        int n = G, tok = -1;
-        if (!bad) {
-            for (int k = 0; k < G && n == G; ++k) {
-                const RowRec t = load_rec(rb + k), d = load_rec(rb + G1 + k);
-                const E* rt = tgt + ((size_t)b * G1 + k) * V;
-                const E* rd = dft + ((size_t)b * G + k) * V;
-                // the verification path's probabilities and standard test
-                const float q = KeptExp{t.thr, c2, t.m * c2, 1.f}(t.zx) / t.Sk;
-                const float pd = KeptExp{d.thr, c2, d.m * c2, 1.f}(d.zx) / d.Sk;
-                const float u = uniform01(p.seed, p.offset + (uint64_t)b, (uint32_t)k, kPurposeAccept);
-                float alpha = -1.f, beta = 0.f;
-                bool acc = accept_test(u, q, pd);
-                if (!acc) {
-                    Row<E> r;
-                    r.rt = rt;
-                    r.rd = rd;
-                    r.c2 = c2;
-                    r.inv_t = p.inv_t;
-                    r.mtc = t.m * c2;
-                    r.mdc = d.m * c2;
-                    r.iSt = 1.f / t.S;
-                    r.iSd = 1.f / d.S;
-                    r.lnr0 = -(t.m - d.m) * p.inv_t - logf(t.S) + logf(d.S);
-                    // KL(q || p) and the sort keys
-                    float acc_kl = 0.f;
-                    for (int i = tid; i < V; i += NT) {
-                        float qq, pp, l;
-                        qpl(r, i, qq, pp, l);
-                        acc_kl += qq * l;
-                        k0[i] = f32_key(l);
-                        i0[i] = (uint32_t)i;
-                    }
-                    const double kl0 = block_sum_d(s, (double)acc_kl);
-                    const float u2 = uniform01(p.seed, p.offset + (uint64_t)b, (uint32_t)k, kPurposeResample);
-                    if (kl0 <= (double)p.kl_bound) {
-                        acc = true;
-                        alpha = 0.f;
-                    } else {
-                        double a = 1.0;
-                        beta = 1.f;
-                        if (p.kl_bound > 0.f) {
-                            __threadfence_block();
-                            __syncthreads();
-                            solve<E>(s, coarse, p, r, k0, i0, k1, i1, A, &a, &beta);
-                        }
-                        alpha = (float)a;
-                        // alpha = 1 is the standard test, which failed
-                        if (a < 1.0) {
-                            const double rho = pd > 0.f ? (double)q / (double)pd : (q > 0.f ? HUGE_VAL : 0.0);
-                            acc = (double)u < fmin(1.0, rho / a);
-                        }
-                        if (!acc) {
-                            if (a == 1.0) {
-                                tok = draw_residual<E>(s.draw, rt, rd, V, t, d, c2, u2);
-                            } else {
-                                const ResidualW w{KeptExp{t.thr, c2, t.m * c2, r.iSt * (1.f / beta)},
-                                                  KeptExp{d.thr, c2, d.m * c2, r.iSd}};
-                                float W;
-                                tok = block_draw<E>(s.draw, rt, rd, V, u2, w, &W);
-                                if (!(W > 0.f)) tok = draw_q<E>(s.draw, rt, V, t, c2, u2);
-                            }
-                        }
-                    }
-                }
-                if (tid == 0) {
-                    if (p.alpha_out) p.alpha_out[(size_t)b * G + k] = alpha;
-                    if (p.beta_out) p.beta_out[(size_t)b * G + k] = beta;
-                }
-                if (!acc) n = k;
-                __syncthreads();
+        int fl = 0;
+        for (int i = tid; i < R; i += NT) fl |= __ldcg(&rb[i].flags);
+        const bool bad = __syncthreads_or(fl & kRecEData) != 0;
+        if (tid == 0) s.bi[5] = G - (int)__ldcg(p.rejmark + b) < k;
+        __syncthreads();
+        const bool skip = s.bi[5] != 0;
+        __syncthreads();
+        if (bad || skip) continue;
+
+        // the verification path's probabilities and standard test
+        const float u = uniform01(p.seed, p.offset + (uint64_t)b, (uint32_t)k, kPurposeAccept);
+        float alpha = -1.f, beta = 0.f;
+        int state = accept_test(u, q, pd) ? kPosAccepted : kPosRejected;
+        if (state != kPosAccepted) {
+            Row<E> r;
+            r.rt = tgt + ((size_t)b * G1 + k) * V;
+            r.rd = dft + ((size_t)b * G + k) * V;
+            r.c2 = c2;
+            r.inv_t = p.inv_t;
+            r.mtc = t.m * c2;
+            r.mdc = d.m * c2;
+            r.iSt = 1.f / t.S;
+            r.iSd = 1.f / d.S;
+            r.lnr0 = -(t.m - d.m) * p.inv_t - logf(t.S) + logf(d.S);
+            // KL(q || p), the sort keys, and q, p, ln rho per index for the solve
+            float acc_kl = 0.f;
+            for (int i = tid; i < V; i += NT) {
+                float qq, pp, l;
+                qpl(r, i, qq, pp, l);
+                acc_kl += qq * l;
+                k0[i] = f32_key(l);
+                i0[i] = (uint32_t)i;
+                A[V + i] = qq;
+                A[2 * (size_t)V + i] = pp;
+                A[3 * (size_t)V + i] = l;
             }
-            if (n == G) {
-                const RowRec t = load_rec(rb + G);
-                const float u2 = uniform01(p.seed, p.offset + (uint64_t)b, (uint32_t)G, kPurposeResample);
-                tok = draw_q<E>(s.draw, tgt + ((size_t)b * G1 + G) * V, V, t, c2, u2);
+            const double kl0 = block_sum_d(s, (double)acc_kl);
+            if (kl0 <= (double)p.kl_bound) {
+                state = kPosAccepted;
+                alpha = 0.f;
+            } else {
+                double a = 1.0;
+                beta = 1.f;
+                if (p.kl_bound > 0.f) {
+                    __threadfence_block();
+                    __syncthreads();
+                    solve<E>(s, coarse, p, r, k0, i0, k1, i1, A, &a, &beta);
+                }
+                alpha = (float)a;
+                // alpha = 1 is the standard test, which failed
+                if (a < 1.0) {
+                    const double rho = pd > 0.f ? (double)q / (double)pd : (q > 0.f ? HUGE_VAL : 0.0);
+                    state = (double)u < fmin(1.0, rho / a) ? kPosAccepted : kPosRejectedScaled;
+                }
             }
         }
         if (tid == 0) {
-            const int st = bad ? kEData : kOk;
+            if (p.alpha_out) p.alpha_out[pos] = alpha;
+            if (p.beta_out) p.beta_out[pos] = beta;
+            p.pos_beta[pos] = beta;
+            p.pos_state[pos] = state;
+            if (state != kPosAccepted) atomicMax(p.rejmark + b, (unsigned)(G - k));
+        }
+        __syncthreads();
+    }
+}
+
+// One sequence per CTA pass: n = the first rejected position (gamma if none),
+// the one draw at n (resample or bonus), and the outputs. Every position up
+// to n was solved by the position kernel.
+template <typename E>
+__global__ void __launch_bounds__(kDrawNT) mentor_resolve_kernel(const __grid_constant__ MentorParams p) {
+    __shared__ DrawShared ds;
+    __shared__ int sh[2];
+    const int tid = threadIdx.x;
+    const int V = p.V, G = p.gamma, G1 = G + 1, R = 2 * G + 1;
+    const float c2 = p.c2;
+    const E* tgt = reinterpret_cast<const E*>(p.target);
+    const E* dft = reinterpret_cast<const E*>(p.draft);
+    for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+        const RowRec* rb = p.rows + (size_t)b * R;
+        int fl = 0;
+        for (int i = tid; i < R; i += kDrawNT) fl |= __ldcg(&rb[i].flags);
+        const bool bad = __syncthreads_or(fl & kRecEData) != 0;
+        if (tid == 0) {
+            int n = G, st = kPosAccepted;
+            for (int k = 0; k < G && !bad; ++k) {
+                st = __ldcg(p.pos_state + (size_t)b * G + k);
+                if (st != kPosAccepted) {
+                    n = k;
+                    break;
+                }
+            }
+            sh[0] = n;
+            sh[1] = st;
+        }
+        __syncthreads();
+        const int n = sh[0], st = sh[1];
+        int tok = -1;
+        if (!bad) {
+            const float u2 = uniform01(p.seed, p.offset + (uint64_t)b, (uint32_t)n, kPurposeResample);
+            const RowRec t = load_rec(rb + n);
+            const E* rt = tgt + ((size_t)b * G1 + n) * V;
+            if (n == G) {
+                tok = draw_q<E>(ds, rt, V, t, c2, u2);
+            } else {
+                const RowRec d = load_rec(rb + G1 + n);
+                const E* rd = dft + ((size_t)b * G + n) * V;
+                if (st == kPosRejected) {
+                    tok = draw_residual<E>(ds, rt, rd, V, t, d, c2, u2);
+                } else {
+                    const float beta = __ldcg(p.pos_beta + (size_t)b * G + n);
+                    const ResidualW w{KeptExp{t.thr, c2, t.m * c2, (1.f / t.S) * (1.f / beta)},
+                                      KeptExp{d.thr, c2, d.m * c2, 1.f / d.S}};
+                    float W;
+                    tok = block_draw<E>(ds, rt, rd, V, u2, w, &W);
+                    if (!(W > 0.f)) tok = draw_q<E>(ds, rt, V, t, c2, u2);
+                }
+            }
+        }
+        if (tid == 0) {
             p.accepted[b] = bad ? -1 : n;
             p.next_token[b] = bad ? -1 : tok;
-            if (p.status) p.status[b] = st;
+            if (p.status) p.status[b] = bad ? kEData : kOk;
         }
-        for (int j = tid; j <= G; j += NT) {
+        for (int j = tid; j <= G; j += kDrawNT) {
             int v = -1;
             if (!bad) v = j < n ? __ldcg(&rb[j].x) : (j == n ? tok : -1);
             p.tokens[(size_t)b * G1 + j] = v;
         }
-        for (int k = tid; k < G; k += NT) {
+        for (int k = tid; k < G; k += kDrawNT) {
             if (bad || k > n) {
                 if (p.alpha_out) p.alpha_out[(size_t)b * G + k] = NAN;
                 if (p.beta_out) p.beta_out[(size_t)b * G + k] = NAN;
@@ -524,12 +638,16 @@ size_t mentor_smem_bytes(int V) {
     return ((sizeof(SharedM) + 15) & ~size_t(15)) + 2 * (size_t)nc * sizeof(float);
 }
 
-cudaError_t launch_mentor(const MentorParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_mentor(const MentorParams& p, int grid, int resolve_grid, cudaStream_t stream) {
     const size_t smem = mentor_smem_bytes(p.V);
     auto kern = p.bf16 ? mentor_kernel<bf16_t> : mentor_kernel<float>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, NT, smem, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int rgrid = p.B < resolve_grid ? p.B : resolve_grid;
+    (p.bf16 ? mentor_resolve_kernel<bf16_t> : mentor_resolve_kernel<float>)<<<rgrid, kDrawNT, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
