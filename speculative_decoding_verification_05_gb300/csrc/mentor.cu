@@ -41,7 +41,13 @@ constexpr int kCoarse = 32;      // coarse index stride
 
 struct SharedM {
     uint32_t wcnt[NW][256];      // per-warp digit counts, then offsets
-    uint32_t base[256];
+    uint32_t stk[kTile];         // one tile in digit order (keys, indices)
+    uint32_t sti[kTile];
+    uint32_t hist[4][256];       // all four digit histograms
+    uint32_t base[256];          // next free global position per bucket
+    uint32_t dtot[256];          // tile: per-digit count, start, global offset
+    uint32_t dstart[256];
+    uint32_t gofs[256];
     double dred[NW];
     float fred[NW];
     float wsum[5][NW];           // solve: per-warp chunk totals
@@ -84,33 +90,41 @@ SV_DEV void qpl(const Row<E>& r, int i, float& q, float& p, float& l) {
 }
 
 // Stable LSD radix sort of (key, idx) pairs, ascending, four 8-bit digits.
-// k0/i0 hold the input; the sorted result ends in k0/i0 again.
+// k0/i0 hold the input; the sorted result ends in k0/i0 again. A key's digits
+// do not change from pass to pass, so one read of the keys builds all four
+// digit histograms. Each tile of kTile items is ranked per warp (stable),
+// laid out in digit order in shared memory, and written out from there so
+// that consecutive threads write consecutive positions of a bucket.
 SV_DEV void radix_sort(SharedM& s, uint32_t* k0, uint32_t* i0, uint32_t* k1, uint32_t* i1, int n) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned lt = (1u << lane) - 1u;
+    for (int e = tid; e < 4 * 256; e += NT) (&s.hist[0][0])[e] = 0u;
+    __syncthreads();
+    for (int ib = tid; ib < n; ib += NT * 8) {  // eight loads in flight per thread
+        uint32_t kk[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) kk[u] = ib + u * NT < n ? __ldcg(k0 + ib + u * NT) : 0u;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (ib + u * NT < n) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) atomicAdd(&s.hist[g][(kk[u] >> (8 * g)) & 255u], 1u);
+            }
+        }
+    }
+    __syncthreads();
     for (int pass = 0; pass < 4; ++pass) {
         const int shift = 8 * pass;
         uint32_t* sk = pass & 1 ? k1 : k0;
         uint32_t* si = pass & 1 ? i1 : i0;
         uint32_t* dk = pass & 1 ? k0 : k1;
         uint32_t* di = pass & 1 ? i0 : i1;
-        // digit histogram -> exclusive bucket starts
-        for (int d = tid; d < 256; d += NT) s.base[d] = 0;
-        __syncthreads();
-        for (int ib = tid; ib < n; ib += NT * 8) {  // eight loads in flight per thread
-            uint32_t kk[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) kk[u] = ib + u * NT < n ? __ldcg(sk + ib + u * NT) : 0u;
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (ib + u * NT < n) atomicAdd(&s.base[(kk[u] >> shift) & 255u], 1u);
-        }
-        __syncthreads();
+        // exclusive bucket starts of this digit
         if (warp == 0) {
             uint32_t c[8], seg = 0;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                c[j] = s.base[lane * 8 + j];
+                c[j] = s.hist[pass][lane * 8 + j];
                 seg += c[j];
             }
             uint32_t incl = seg;
@@ -127,10 +141,9 @@ SV_DEV void radix_sort(SharedM& s, uint32_t* k0, uint32_t* i0, uint32_t* k1, uin
             }
         }
         __syncthreads();
-        // stable scatter, tile by tile; warp w owns items [w*256, w*256+256) of a tile
         for (int t0 = 0; t0 < n; t0 += kTile) {
             for (int e = tid; e < NW * 256; e += NT) (&s.wcnt[0][0])[e] = 0u;
-            __syncthreads();
+            // warp w owns items [w*256, w*256+256) of the tile
             uint32_t key[kIPT], idv[kIPT], rank[kIPT];
             int dig[kIPT];
 #pragma unroll
@@ -140,6 +153,11 @@ SV_DEV void radix_sort(SharedM& s, uint32_t* k0, uint32_t* i0, uint32_t* k1, uin
                 key[r] = ok ? __ldcg(sk + i) : 0u;
                 idv[r] = ok ? __ldcg(si + i) : 0u;
                 dig[r] = ok ? (int)((key[r] >> shift) & 255u) : -1;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int r = 0; r < kIPT; ++r) {
+                const bool ok = dig[r] >= 0;
                 const unsigned act = __ballot_sync(0xFFFFFFFFu, ok);
                 unsigned peers = __match_any_sync(0xFFFFFFFFu, dig[r]);
                 peers &= act;
@@ -154,39 +172,69 @@ SV_DEV void radix_sort(SharedM& s, uint32_t* k0, uint32_t* i0, uint32_t* k1, uin
                 __syncwarp();
             }
             __syncthreads();
-            // offsets: digit-major over warps, starting at the bucket's running base
-            {
-                const int d = tid >> 2, q = tid & 3;
-                uint32_t c[8], sum = 0;
+            // tile-local starts: digit-major, warps in order inside a digit
+            const int d = tid >> 2, q = tid & 3;
+            uint32_t c[8], sum = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                c[j] = s.wcnt[q * 8 + j][d];
+                sum += c[j];
+            }
+            uint32_t incl = sum;
+            const uint32_t v1 = __shfl_up_sync(0xFFFFFFFFu, incl, 1, 4);
+            if (q >= 1) incl += v1;
+            const uint32_t v2 = __shfl_up_sync(0xFFFFFFFFu, incl, 2, 4);
+            if (q >= 2) incl += v2;
+            if (q == 3) s.dtot[d] = incl;
+            __syncthreads();
+            if (warp == 0) {
+                uint32_t cc[8], seg = 0;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    c[j] = s.wcnt[q * 8 + j][d];
-                    sum += c[j];
+                    cc[j] = s.dtot[lane * 8 + j];
+                    seg += cc[j];
                 }
-                uint32_t incl = sum;
-                const uint32_t v1 = __shfl_up_sync(0xFFFFFFFFu, incl, 1, 4);
-                if (q >= 1) incl += v1;
-                const uint32_t v2 = __shfl_up_sync(0xFFFFFFFFu, incl, 2, 4);
-                if (q >= 2) incl += v2;
-                const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 3, 4);
-                const uint32_t b0 = s.base[d];
-                uint32_t run = b0 + incl - sum;
-                __syncthreads();
+                uint32_t in2 = seg;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, in2, o);
+                    if (lane >= o) in2 += v;
+                }
+                uint32_t run = in2 - seg;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int dd = lane * 8 + j;
+                    s.dstart[dd] = run;
+                    s.gofs[dd] = s.base[dd] - run;  // global position = gofs + tile-local position
+                    s.base[dd] += cc[j];
+                    run += cc[j];
+                }
+            }
+            __syncthreads();
+            {
+                uint32_t run = s.dstart[d] + incl - sum;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     s.wcnt[q * 8 + j][d] = run;
                     run += c[j];
                 }
-                if (q == 3) s.base[d] = b0 + total;
             }
             __syncthreads();
 #pragma unroll
             for (int r = 0; r < kIPT; ++r) {
                 if (dig[r] >= 0) {
-                    const uint32_t pos = s.wcnt[warp][dig[r]] + rank[r];
-                    dk[pos] = key[r];
-                    di[pos] = idv[r];
+                    const uint32_t lp = s.wcnt[warp][dig[r]] + rank[r];
+                    s.stk[lp] = key[r];
+                    s.sti[lp] = idv[r];
                 }
+            }
+            __syncthreads();
+            const int cnt = min(kTile, n - t0);
+            for (int lp = tid; lp < cnt; lp += NT) {
+                const uint32_t kv = s.stk[lp];
+                const uint32_t pos = s.gofs[(kv >> shift) & 255u] + (uint32_t)lp;
+                dk[pos] = kv;
+                di[pos] = s.sti[lp];
             }
             __syncthreads();
         }
