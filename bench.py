@@ -357,7 +357,8 @@ def main():
     avg_launch_ms = statistics.mean(per_launch_ms)
     achieved = nbytes / (avg_launch_ms / 1e3) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-            "frac": achieved / peak, "traffic": recorded_traffic(args.workload),
+            "frac": achieved / peak,
+            "traffic": recorded_traffic(args.workload) if args.stack in (0, WORKLOADS[args.workload][1]) else None,
             "kernel": KERNEL_OF[args.workload], "algorithmic_bytes_per_launch": nbytes,
             "peak_source": f"{peak_kind} hbm_gbs (copy)", "frac_of_nominal_8TBps": achieved / 8000.0}
     cpu = None if args.no_cpu else cpu_baseline(cfg, temp, lenience=LENIENCE.get(args.workload, 1.0))
