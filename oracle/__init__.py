@@ -21,7 +21,8 @@ Sources (cited by page title and section throughout):
            operation factors), appendix E worked example.
 * [REST]   "简单好用！北大、普林斯顿联合提出即插即用的大语言模型加速方法"
            (REST, retrieval-based speculative decoding): section
-           "REST: 基于检索的投机解码" (trie, BFS pseudo-sequence, exact-match
+           "REST: 基于检索的投机解码" (trie with prefix counts, the heaviest
+           subtree, BFS pseudo-sequence and tree attention mask, exact-match
            acceptance).
 * [Mentor] "推测解码的一种最优有损变体" (an optimal lossy variant of
            speculative decoding): sections "导师解码" and "解决优化问题".
@@ -54,3 +55,4 @@ from .spec import (
     walltime_factor,
     ops_factor,
 )
+from .rest import MAX_COUNT as REST_MAX_COUNT, rest_tree, rest_tree_batch
