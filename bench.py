@@ -48,6 +48,7 @@ WORKLOADS = {
     "large_vocab_t0": ("large_vocab", 1, 0.0),
     "tree": ("tree", 4, None),
     "mentor": ("mentor", 12, None),
+    "rest": ("rest", 4, None),
     "nucleus_lenient": ("nucleus", 1000, None),
 }
 LENIENCE = {"nucleus_lenient": 0.5}   # lenient verification (l < 1); others are exact
@@ -58,7 +59,8 @@ KERNEL_OF = {"nucleus": "row_kernel<bf16,transform> + draw_kernel", "tiny": "row
              "large_vocab": "row_kernel<f32> + draw_kernel", "large_vocab_t0": "argmax_kernel<f32>",
              "tree": "argmax_kernel<f32>",
              "mentor": "row_kernel<f32> + mentor_kernel + mentor_resolve_kernel",
-             "nucleus_lenient": "row_kernel<bf16,transform> + draw_kernel"}
+             "nucleus_lenient": "row_kernel<bf16,transform> + draw_kernel",
+             "rest": "tree_build_kernel + argmax_kernel<f32>"}
 
 
 def dist_env():
@@ -140,6 +142,17 @@ def make_inputs(name, steps_stacked, temperature, device, seed=2024, lenience=1.
     import speculative_decoding_verification_05_gb300 as sv
 
     c = dict(workloads.CONFIGS[name])
+    if c["kind"] == "rest":
+        B = c["B"] * steps_stacked
+        cand = torch.from_numpy(workloads.rest_candidates(B, c["C"], c["L"], c["V"], seed, bases=c["bases"],
+                                                          diverge=c["diverge"])).to(device)
+        root = torch.from_numpy(np.random.default_rng(seed).integers(0, c["V"], B).astype(np.int32)).to(device)
+        t = sv.tree_build(cand, root, c["V"], c["N"], with_mask=False)   # the tree, to force its logits
+        z = workloads.forced_tree_logits(t["node_tokens"].cpu().numpy(), t["parent"].cpu().numpy(),
+                                         t["n_nodes"].cpu().numpy(), c["V"], seed, sd=c["sd"],
+                                         force_p=c["force_p"], device=device)
+        return dict(kind="rest", cand=cand, root=root, z=z, B=B, N=c["N"], V=c["V"], C=c["C"], L=c["L"],
+                    max_depth=c["L"], esize=4)
     if c["kind"] == "tree":
         B = c["B"] * steps_stacked
         z, tok, par, dep = workloads.tree_inputs(B, c["N"], c["V"], seed, device="cpu")
@@ -159,6 +172,9 @@ def make_inputs(name, steps_stacked, temperature, device, seed=2024, lenience=1.
 def run_step(inp):
     import speculative_decoding_verification_05_gb300 as sv
 
+    if inp["kind"] == "rest":
+        t = sv.tree_build(inp["cand"], inp["root"], inp["V"], inp["N"])
+        return sv.verify_tree(inp["z"], t["node_tokens"], t["parent"], t["depth"], inp["max_depth"])
     if inp["kind"] == "tree":
         return sv.verify_tree(inp["z"], inp["tok"], inp["par"], inp["dep"], inp["max_depth"])
     if inp["kind"] == "mentor":
@@ -170,6 +186,11 @@ def run_step_host(inp, host):
     """End-to-end through the public API: pinned host inputs in, host outputs back."""
     import speculative_decoding_verification_05_gb300 as sv
 
+    if inp["kind"] == "rest":
+        # two public calls on host buffers: the tree (and its mask) comes back in between
+        t = sv.tree_build(host["cand"], host["root"], inp["V"], inp["N"])
+        r = sv.verify_tree(host["z"], t["node_tokens"], t["parent"], t["depth"], inp["max_depth"])
+        return {**{"tree_" + k: v for k, v in t.items()}, **r}
     if inp["kind"] == "tree":
         return sv.verify_tree(host["z"], host["tok"], host["par"], host["dep"], inp["max_depth"])
     if inp["kind"] == "mentor":
@@ -180,6 +201,12 @@ def run_step_host(inp, host):
 
 def algorithmic(inp):
     """(bytes, verified positions) one step must read / decides."""
+    if inp["kind"] == "rest":
+        # logits once, the candidates once, the tree arrays and mask written once
+        B, N = inp["B"], inp["N"]
+        extra = B * inp["C"] * inp["L"] * 4 + B * N * (3 * 4 + N) + B * 2 * 4
+        return (workloads.algorithmic_bytes("rest", B, inp["V"], 4, N=N) + extra,
+                workloads.verified_positions("rest", B, N=N))
     if inp["kind"] == "tree":
         return (workloads.algorithmic_bytes("tree", inp["B"], inp["V"], inp["esize"], N=inp["N"]),
                 workloads.verified_positions("tree", inp["B"], N=inp["N"]))
@@ -193,6 +220,8 @@ def launches_per_step(inp):
     (mentor); the argmax kernel (tree, T = 0); rows and draws otherwise."""
     if inp["kind"] == "mentor":
         return 3
+    if inp["kind"] == "rest":
+        return 2
     if inp["kind"] == "tree" or inp["T"] == 0:
         return 1
     return 2
@@ -203,7 +232,24 @@ def cpu_baseline(name, temperature, budget_s=12.0, lenience=1.0):
     import oracle
 
     c = dict(workloads.CONFIGS[name])
-    T = c["temperature"] if temperature is None else temperature
+    if c["kind"] == "rest":
+        B = c["B"]
+        cand = workloads.rest_candidates(B, c["C"], c["L"], c["V"], 99, bases=c["bases"], diverge=c["diverge"])
+        root = np.arange(B, dtype=np.int32)
+        tr = oracle.rest_tree_batch(cand, None, root, c["N"], c["V"])
+        z = workloads.forced_tree_logits(tr["tokens"], tr["parent"], tr["n_nodes"], c["V"], 99, sd=c["sd"],
+                                         force_p=c["force_p"])
+        t0 = time.perf_counter()
+        n = 0
+        while time.perf_counter() - t0 < budget_s:
+            t = oracle.rest_tree_batch(cand, None, root, c["N"], c["V"])
+            oracle.verify_tree(z, t["tokens"], t["parent"], t["depth"], c["L"])
+            n += 1
+        dt = time.perf_counter() - t0
+        return {"value": n * B * (c["N"] - 1) / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": f"{n} REST steps of {B} sequences (C={c['C']}, L={c['L']}, N={c['N']}, "
+                          f"V={c['V']}) in {dt:.1f} s"}
+    T = c.get("temperature", 0.0) if temperature is None else temperature
     if c["kind"] == "tree":
         B = c["B"]
         z, tok, par, dep = workloads.tree_inputs(B, c["N"], c["V"], 99)

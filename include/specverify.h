@@ -100,7 +100,11 @@ enum {
     SPEC_MAX_V = 262144,      /* vocabulary size */
     SPEC_MAX_GAMMA = 255,     /* draft length */
     SPEC_MAX_TREE_N = 1024,   /* tree nodes, root included */
-    SPEC_MAX_BISECT = 64      /* mentor bisection iterations */
+    SPEC_MAX_BISECT = 64,     /* mentor bisection iterations */
+    SPEC_MAX_TREE_C = 1024,   /* tree construction: candidates per sequence */
+    SPEC_MAX_TREE_L = 32,     /*                    tokens per candidate */
+    SPEC_MAX_TREE_CL = 4096,  /*                    candidates x tokens */
+    SPEC_TREE_MAX_COUNT = 1 << 20  /* multiplicities are below this */
 };
 
 /* ------------------------------------------------------------------------
@@ -182,6 +186,47 @@ spec_status spec_verify_tree(const void* target, spec_dtype dtype,
                              int32_t* accept_len, int32_t* path_nodes, int32_t* tokens,
                              int32_t* bonus, int32_t* status,
                              void* workspace, size_t ws_bytes, spec_stream stream);
+
+/* ------------------------------------------------------------------------
+ * spec_tree_build - the REST draft tree of each sequence from its retrieved
+ * continuations ([REST] "REST: 基于检索的投机解码"): every prefix of a
+ * candidate is a trie node whose weight is how often the prefix occurs (the
+ * sum of the multiplicities of the candidates that start with it); the N - 1
+ * nodes ranked first by (weight descending, length ascending, token path
+ * lexicographically ascending) form the draft tree, which is closed under
+ * taking parents; its breadth-first order (a node's children by ascending
+ * token) is the pseudo-sequence spec_verify_tree takes, and `mask` is its
+ * tree attention mask.
+ *
+ *   candidates    [B, C, L] int32; a candidate ends at its first -1; every
+ *                 entry must be -1 or a token in [0, V)
+ *   counts        [B, C] int32 multiplicities in [0, SPEC_TREE_MAX_COUNT);
+ *                 NULL: every candidate counts once
+ *   root_token    [B] int32 in [0, V): the last context token (node 0)
+ *   B, C, L, V, N 1 <= B <= 2^24, 1 <= C <= SPEC_MAX_TREE_C,
+ *                 1 <= L <= SPEC_MAX_TREE_L, C * L <= SPEC_MAX_TREE_CL,
+ *                 1 <= V, 2 <= N <= SPEC_MAX_TREE_N
+ * Outputs (device, written for every b; all pointers 4-byte aligned except
+ * mask):
+ *   node_tokens   [B, N] int32 token of each node, root first
+ *   parent        [B, N] int32, parent[0] = -1, 0 <= parent[i] < i
+ *   depth         [B, N] int32, depth[0] = 0
+ *                 (positions n_nodes[b] .. N-1 hold -1 in all three)
+ *   mask          [B, N, N] uint8, mask[b][i][j] = 1 iff node j is node i or
+ *                 one of its ancestors (rows from n_nodes[b] on are zero);
+ *                 NULL allowed
+ *   n_nodes       [B] int32: 1 + the number of chosen nodes, at most N (fewer
+ *                 when the candidates have fewer distinct prefixes)
+ *   status        [B] SPEC_OK, or SPEC_EDATA for an entry, multiplicity or
+ *                 root token out of range (that sequence's outputs are -1 and
+ *                 its mask rows zero); NULL allowed
+ * No workspace: each sequence is built in one CTA's shared memory. Invalid
+ * sizes or NULL required pointers: SPEC_EINVAL, nothing enqueued.
+ * ---------------------------------------------------------------------- */
+spec_status spec_tree_build(const int32_t* candidates, const int32_t* counts, const int32_t* root_token,
+                            int B, int C, int L, int V, int N,
+                            int32_t* node_tokens, int32_t* parent, int32_t* depth, uint8_t* mask,
+                            int32_t* n_nodes, int32_t* status, spec_stream stream);
 
 /* ------------------------------------------------------------------------
  * spec_verify_mentor - lossy "mentor" verification ([Mentor] "导师解码",

@@ -31,7 +31,7 @@ PURPOSE_ACCEPT, PURPOSE_RESAMPLE, PURPOSE_DRAFT = 0, 1, 2
 
 EXPORTED = [
     "spec_verify_workspace_size", "spec_verify", "spec_verify_lenient",
-    "spec_verify_tree_workspace_size", "spec_verify_tree",
+    "spec_verify_tree_workspace_size", "spec_verify_tree", "spec_tree_build",
     "spec_verify_mentor_workspace_size", "spec_verify_mentor",
     "spec_sample_workspace_size", "spec_sample",
     "spec_philox_uniform", "spec_verify_noalloc", "spec_status_string", "spec_last_cuda_error",
@@ -77,6 +77,8 @@ def load_library(path=LIB_PATH):
         lib.spec_verify_tree.argtypes = [_P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P,
                                          _P, _SZ, _P]
         lib.spec_verify_tree.restype = _I
+        lib.spec_tree_build.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]
+        lib.spec_tree_build.restype = _I
         lib.spec_verify_mentor_workspace_size.argtypes = [_I, _I, _I, _I]
         lib.spec_verify_mentor_workspace_size.restype = _SZ
         lib.spec_verify_mentor.argtypes = [_P, _P, _I, _P, _I, _I, _I, ctypes.c_float, ctypes.c_float,
@@ -247,6 +249,30 @@ def verify_tree(target, node_tokens, parent, depth, max_depth):
     return sg.back(o)
 
 
+def tree_build(candidates, root_token, V, N, counts=None, with_mask=True):
+    """REST draft trees from retrieved continuations candidates [B, C, L] (-1 ends one).
+
+    Returns node_tokens, parent, depth [B, N] (the layout ``verify_tree`` takes),
+    mask [B, N, N] uint8 (when ``with_mask``), n_nodes [B] and status [B].
+    """
+    lib = load_library()
+    sg = _Staging(candidates)
+    cand = sg.dev(candidates, torch.int32)
+    root = sg.dev(root_token, torch.int32)
+    cnt = sg.dev(counts, torch.int32)
+    B, C, L = cand.shape
+    o = {"node_tokens": sg.out((B, N)), "parent": sg.out((B, N)), "depth": sg.out((B, N)),
+         "n_nodes": sg.out((B,)), "status": sg.out((B,))}
+    if with_mask:
+        o["mask"] = sg.out((B, N, N), torch.uint8)
+    stream = torch.cuda.current_stream(sg.device)
+    rc = lib.spec_tree_build(_ptr(cand), _ptr(cnt), _ptr(root), B, C, L, int(V), int(N),
+                             _ptr(o["node_tokens"]), _ptr(o["parent"]), _ptr(o["depth"]), _ptr(o.get("mask")),
+                             _ptr(o["n_nodes"]), _ptr(o["status"]), ctypes.c_void_p(stream.cuda_stream))
+    _check(rc)
+    return sg.back(o)
+
+
 def verify_mentor(target, draft, draft_tokens, temperature=1.0, kl_bound=0.0, bisect_iters=30,
                   seed=0, offset=0, debug=False):
     """Lossy mentor verification; returns the ``verify`` outputs plus alpha and beta [B, gamma]."""
@@ -305,5 +331,5 @@ def philox_uniform(seed, row0, position, purpose, n, device=None):
     return out
 
 
-__all__ = ["philox_uniform", "verify", "verify_tree", "verify_mentor", "sample", "load_library", "workspace",
+__all__ = ["philox_uniform", "verify", "verify_tree", "tree_build", "verify_mentor", "sample", "load_library", "workspace",
            "SpecError", "SpecSampling", "EXPORTED", "LIB_PATH"]

@@ -16,7 +16,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspecverify.so")
-SOURCES = ["csrc/api.cu", "csrc/rows.cu", "csrc/argmax.cu", "csrc/mentor.cu", "csrc/noalloc.cu"]
+SOURCES = ["csrc/api.cu", "csrc/rows.cu", "csrc/argmax.cu", "csrc/mentor.cu", "csrc/noalloc.cu",
+           "csrc/tree_build.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
           "-Xptxas", "-v", "-I", os.path.join(ROOT, "include"), "-I", os.path.join(HERE, "csrc")]

@@ -354,6 +354,23 @@ spec_status spec_verify_tree(const void* target, spec_dtype dtype, const int32_t
                                  reinterpret_cast<cudaStream_t>(stream));
 }
 
+spec_status spec_tree_build(const int32_t* candidates, const int32_t* counts, const int32_t* root_token,
+                            int B, int C, int L, int V, int N, int32_t* node_tokens, int32_t* parent,
+                            int32_t* depth, uint8_t* mask, int32_t* n_nodes, int32_t* status,
+                            spec_stream stream) {
+    if (B < 1 || B > (1 << 24) || C < 1 || C > SPEC_MAX_TREE_C || L < 1 || L > SPEC_MAX_TREE_L ||
+        C * L > SPEC_MAX_TREE_CL || V < 1 || N < 2 || N > SPEC_MAX_TREE_N)
+        return SPEC_EINVAL;
+    if (!candidates || !root_token || !node_tokens || !parent || !depth || !n_nodes) return SPEC_EINVAL;
+    if (!aligned(candidates, 4) || !aligned(counts, 4) || !aligned(root_token, 4) || !aligned(node_tokens, 4) ||
+        !aligned(parent, 4) || !aligned(depth, 4) || !aligned(n_nodes, 4) || !aligned(status, 4))
+        return SPEC_EINVAL;
+    const cudaError_t e = sv::launch_tree_build(candidates, counts, root_token, B, C, L, V, N, node_tokens, parent,
+                                                depth, mask, n_nodes, status,
+                                                reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
+}
+
 size_t spec_verify_mentor_workspace_size(int B, int gamma, int V, spec_dtype dtype) {
     (void)dtype;
     if (B < 1 || gamma < 1 || V < 1) return 0;

@@ -350,5 +350,10 @@ cudaError_t launch_draws(const RowParams& p, int dtype, int sms, cudaStream_t st
 cudaError_t launch_argmax(const ArgmaxParams& p, int dtype, int grid, cudaStream_t stream);
 // Position kernel on `grid` persistent CTAs, then the per-sequence resolve.
 cudaError_t launch_mentor(const MentorParams& p, int grid, int resolve_grid, cudaStream_t stream);
+// REST draft-tree construction: one CTA per sequence.
+size_t tree_build_smem_bytes();
+cudaError_t launch_tree_build(const int32_t* cand, const int32_t* counts, const int32_t* root, int B, int C,
+                              int L, int V, int N, int32_t* tokens, int32_t* parent, int32_t* depth,
+                              uint8_t* mask, int32_t* n_nodes, int32_t* status, cudaStream_t stream);
 
 }  // namespace sv

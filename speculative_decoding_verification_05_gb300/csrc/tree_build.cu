@@ -1,0 +1,378 @@
+// REST draft-tree construction.
+//
+// "简单好用！北大、普林斯顿联合提出即插即用的大语言模型加速方法" (REST), section
+// "REST: 基于检索的投机解码": every prefix of a retrieved continuation is a
+// node of a trie weighted by how often it occurs; the heaviest nodes form the
+// draft tree; its breadth-first order is the pseudo-sequence the target model
+// scores, with an attention mask that restores each token's ancestry.
+//
+// One CTA builds one sequence's tree in shared memory, without building a
+// trie. Sorted lexicographically, the candidates that share a prefix of
+// length l form one run; a node is (l, k) with k the first sorted candidate
+// of its run (where the common prefix with the previous candidate is shorter
+// than l), its weight the multiplicities summed over the run, its children
+// the nodes of depth l + 1 that start inside the run. So:
+//   1. candidates into shared memory, each ended at its first -1;
+//   2. bitonic sort of the candidate indices (lexicographic, index on ties);
+//   3. common-prefix length with the previous sorted candidate, prefix sums
+//      of the multiplicities, a sparse table of range minima of the common
+//      prefixes, and every node (l, k) with its run's end e (the first later
+//      candidate whose common prefix is shorter than l, found by descending
+//      the table) and its weight;
+//   4. bitonic sort of the 64-bit node keys (weight descending, length, k,
+//      then e, which (l, k) determines): the first N - 1 are the chosen nodes
+//      (k order is path order);
+//   5. bitonic sort of their (l, k, e) words: breadth-first positions; a
+//      node's parent is the last chosen node of depth l - 1 starting at or
+//      before k;
+//   6. the mask: node j is node i or its ancestor iff j is no deeper than i
+//      and i's first candidate lies in j's run.
+// Candidate rows are stored with an odd stride, so the threads of a warp that
+// read one column of different candidates hit different banks. The work is a
+// few thousand integers per sequence: latency-bound, no HBM stream worth
+// staging.
+
+#include "common.cuh"
+#include "specverify.h"
+
+namespace sv {
+namespace {
+
+constexpr int TB = 512;
+constexpr int TW = TB / 32;
+constexpr int kMaxC = SPEC_MAX_TREE_C;
+constexpr int kMaxCL = SPEC_MAX_TREE_CL;
+constexpr int kMaxN = SPEC_MAX_TREE_N;
+constexpr int kLog = 10;  // 2^kLog = kMaxC
+
+// Node key: (2^30 - 1 - weight) | l | k | e, so ascending keys rank by weight
+// descending, then length, then path; breadth-first words: l | k | e.
+constexpr int kKeyE = 0, kKeyK = 11, kKeyL = 22, kKeyW = 28;
+SV_DEV uint32_t word_of(int l, int k, int e) {
+    return ((uint32_t)l << kKeyL) | ((uint32_t)k << kKeyK) | ((uint32_t)e << kKeyE);
+}
+
+struct TreeParams {
+    const int32_t* cand;
+    const int32_t* counts;
+    const int32_t* root;
+    int B, C, L, V, N;
+    int32_t* tokens;
+    int32_t* parent;
+    int32_t* depth;
+    uint8_t* mask;
+    int32_t* n_nodes;
+    int32_t* status;
+};
+
+struct TreeSmem {
+    int32_t tok[kMaxCL + kMaxC];  // candidate c, position l at c * LS + l (LS odd); -1 after its end
+    int32_t len[kMaxC];
+    int32_t cnt[kMaxC];
+    int32_t ord[kMaxC];          // sorted position -> candidate
+    int32_t lcp[kMaxC];          // common prefix with the previous sorted candidate
+    int32_t pm[kMaxC + 1];       // exclusive prefix sums of the sorted multiplicities
+    int32_t noff[kMaxC + 1];     // first node of each sorted candidate
+    uint8_t mn[kLog + 1][kMaxC]; // mn[j][i] = min(lcp[i .. i + 2^j))
+    uint32_t bfs[kMaxN];         // chosen words (l, k, e), breadth-first order
+    union {
+        unsigned long long key[kMaxCL];  // node keys (steps 3-4)
+        struct {
+            int32_t l[kMaxN], k[kMaxN], e[kMaxN];  // position -> depth, run start, run end
+        } pos;
+    } u;
+    int32_t scan[TW + 1];
+    int32_t flag;
+};
+
+// Lexicographic order of candidates a, b on their first `l` tokens (-1 after
+// a candidate's end sorts first): <0, 0, >0. LS is the row stride.
+SV_DEV int cmp_prefix(const TreeSmem& s, int LS, int a, int b, int l) {
+    for (int i = 0; i < l; ++i) {
+        const int x = s.tok[a * LS + i], y = s.tok[b * LS + i];
+        if (x != y) return x < y ? -1 : 1;
+    }
+    return 0;
+}
+
+// Candidate order: tokens, then index (a strict total order). Indices >= C pad.
+SV_DEV bool cand_less(const TreeSmem& s, int C, int L, int LS, int a, int b) {
+    if (a >= C || b >= C) return a < b;
+    const int c = cmp_prefix(s, LS, a, b, L);
+    return c != 0 ? c < 0 : a < b;
+}
+
+// Ascending bitonic sort of n (a power of two) elements; every thread calls.
+template <typename T, typename Less>
+SV_DEV void bitonic(T* a, int n, Less less) {
+    for (int k = 2; k <= n; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < n; i += TB) {
+                const int p = i ^ j;
+                if (p > i) {
+                    const T x = a[i], y = a[p];
+                    const bool up = (i & k) == 0;
+                    if (up ? less(y, x) : less(x, y)) {
+                        a[i] = y;
+                        a[p] = x;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// Exclusive scan of a[0, n) in place, n <= 2 * TB; returns the total.
+SV_DEV int block_scan(TreeSmem& s, int32_t* a, int n) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int i0 = 2 * tid;
+    const int x0 = i0 < n ? a[i0] : 0, x1 = i0 + 1 < n ? a[i0 + 1] : 0;
+    const int t = x0 + x1;
+    int incl = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) s.scan[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int w = lane < TW ? s.scan[lane] : 0;
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+            if (lane >= o) wi += y;
+        }
+        if (lane < TW) s.scan[lane] = wi - w;
+        if (lane == 31) s.scan[TW] = wi;
+    }
+    __syncthreads();
+    const int base = s.scan[warp] + incl - t;
+    if (i0 < n) a[i0] = base;
+    if (i0 + 1 < n) a[i0 + 1] = base + x0;
+    const int total = s.scan[TW];
+    __syncthreads();
+    return total;
+}
+
+// End of the run of sorted candidates sharing the first l tokens of sorted
+// candidate k: the first k2 > k with lcp[k2] < l (C if none), by jumping over
+// blocks whose minimum is at least l.
+SV_DEV int run_end(const TreeSmem& s, int C, int k, int l) {
+    int pos = k + 1;
+    for (int j = kLog; j >= 0; --j)
+        if (pos + (1 << j) <= C && (int)s.mn[j][pos] >= l) pos += 1 << j;
+    return pos;
+}
+
+SV_DEV int pow2_at_least(int n) {
+    int p = 1;
+    while (p < n) p <<= 1;
+    return p;
+}
+
+__global__ void __launch_bounds__(TB) tree_build_kernel(const __grid_constant__ TreeParams p) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    TreeSmem& s = *reinterpret_cast<TreeSmem*>(smem_raw);
+    const int tid = threadIdx.x;
+    const int C = p.C, L = p.L, N = p.N, LS = L | 1;
+    const int b = blockIdx.x;
+    const int32_t* cb = p.cand + (size_t)b * C * L;
+    const int root = p.root[b];
+
+    // 1. candidates, multiplicities, validation
+    int bad = root < 0 || root >= p.V;
+    for (int e = tid; e < C * L; e += TB) {
+        const int t = cb[e];
+        bad |= t < -1 || t >= p.V;
+        const int c = e / L;
+        s.tok[c * LS + (e - c * L)] = t;
+    }
+    for (int c = tid; c < C; c += TB) {
+        const int m = p.counts ? p.counts[(size_t)b * C + c] : 1;
+        bad |= m < 0 || m >= SPEC_TREE_MAX_COUNT;
+        s.cnt[c] = m;
+    }
+    bad = __syncthreads_or(bad);
+    if (!bad) {
+        for (int c = tid; c < C; c += TB) {
+            int n = L;
+            for (int l = 0; l < L; ++l) {
+                if (s.tok[c * LS + l] == -1) {
+                    n = l;
+                    break;
+                }
+            }
+            s.len[c] = n;
+            for (int l = n; l < L; ++l) s.tok[c * LS + l] = -1;
+        }
+        const int CP = pow2_at_least(C);
+        for (int i = tid; i < CP; i += TB) s.ord[i] = i;  // CP <= kMaxC (a power of two)
+        __syncthreads();
+
+        // 2. candidates in lexicographic order
+        bitonic(s.ord, CP, [&](int a, int c) { return cand_less(s, C, L, LS, a, c); });
+
+        // 3. common prefixes, multiplicity sums, nodes
+        for (int k = tid; k < C; k += TB) {
+            const int a = s.ord[k];
+            int lc = 0;
+            if (k > 0) {
+                const int pr = s.ord[k - 1];
+                while (lc < L && s.tok[pr * LS + lc] == s.tok[a * LS + lc] && s.tok[a * LS + lc] != -1) ++lc;
+            }
+            s.lcp[k] = lc;
+            s.mn[0][k] = (uint8_t)lc;
+            s.pm[k] = s.cnt[a];
+            s.noff[k] = max(0, s.len[a] - lc);
+        }
+        __syncthreads();
+        const int wsum = block_scan(s, s.pm, C);
+        const int M = block_scan(s, s.noff, C);
+        if (tid == 0) {
+            s.pm[C] = wsum;
+            s.noff[C] = M;
+        }
+        for (int j = 1; (1 << j) <= C; ++j) {
+            __syncthreads();
+            const int h = 1 << (j - 1);
+            for (int i = tid; i + (1 << j) <= C; i += TB) s.mn[j][i] = min(s.mn[j - 1][i], s.mn[j - 1][i + h]);
+        }
+        __syncthreads();
+        for (int k = tid; k < C; k += TB) {
+            const int a = s.ord[k];
+            int o = s.noff[k];
+            for (int l = s.lcp[k] + 1; l <= s.len[a]; ++l, ++o) {
+                const int e = run_end(s, C, k, l);
+                const uint32_t w = (uint32_t)(s.pm[e] - s.pm[k]);  // < 2^30
+                s.u.key[o] = ((unsigned long long)((1u << 30) - 1u - w) << kKeyW) | word_of(l, k, e);
+            }
+        }
+        const int MP = pow2_at_least(max(M, 1));
+        for (int i = M + tid; i < MP; i += TB) s.u.key[i] = ~0ull;
+        __syncthreads();
+
+        // 4. the heaviest N - 1 nodes
+        bitonic(s.u.key, MP, [](unsigned long long x, unsigned long long y) { return x < y; });
+        const int S = min(N - 1, M);
+        const int SP = pow2_at_least(max(S, 1));
+        for (int i = tid; i < SP; i += TB)
+            s.bfs[i] = i < S ? (uint32_t)(s.u.key[i] & ((1ull << kKeyW) - 1)) : 0xFFFFFFFFu;
+        __syncthreads();
+
+        // 5. breadth-first positions, parents
+        bitonic(s.bfs, SP, [](uint32_t x, uint32_t y) { return x < y; });
+        for (int q = tid; q < N; q += TB) {
+            int32_t tk = -1, pa = -1, de = -1;
+            if (q == 0) {
+                tk = root;
+                de = 0;
+                s.u.pos.l[0] = 0;
+                s.u.pos.k[0] = 0;
+                s.u.pos.e[0] = C;
+            } else if (q <= S) {
+                const uint32_t w = s.bfs[q - 1];
+                const int l = (int)(w >> kKeyL), k = (int)((w >> kKeyK) & 0x7FFu), e = (int)(w & 0x7FFu);
+                tk = s.tok[s.ord[k] * LS + l - 1];
+                de = l;
+                pa = 0;
+                if (l > 1) {
+                    // the last chosen word <= (l - 1, k, any e)
+                    const uint32_t want = word_of(l - 1, k, 0x7FF);
+                    int lo = 0, hi = q - 1;  // bfs[q - 1] > want
+                    while (lo < hi) {
+                        const int mid = (lo + hi) >> 1;
+                        if (s.bfs[mid] <= want)
+                            lo = mid + 1;
+                        else
+                            hi = mid;
+                    }
+                    pa = lo;  // position of bfs[lo - 1] is lo
+                }
+                s.u.pos.l[q] = l;
+                s.u.pos.k[q] = k;
+                s.u.pos.e[q] = e;
+            }
+            const size_t o = (size_t)b * N + q;
+            p.tokens[o] = tk;
+            p.parent[o] = pa;
+            p.depth[o] = de;
+        }
+        if (tid == 0) {
+            p.n_nodes[b] = S + 1;
+            if (p.status) p.status[b] = kOk;
+            s.flag = S;
+        }
+        __syncthreads();
+    } else {
+        for (int q = tid; q < N; q += TB) {
+            const size_t o = (size_t)b * N + q;
+            p.tokens[o] = -1;
+            p.parent[o] = -1;
+            p.depth[o] = -1;
+        }
+        if (tid == 0) {
+            p.n_nodes[b] = -1;
+            if (p.status) p.status[b] = kEData;
+            s.flag = -1;
+        }
+        __syncthreads();
+    }
+
+    // 6. the tree attention mask
+    if (!p.mask) return;
+    const int S = s.flag;
+    uint8_t* mb = p.mask + (size_t)b * N * N;
+    auto bit = [&](int i, int j) -> uint32_t {
+        if (i > S || j > S) return 0u;
+        if (j == 0) return 1u;
+        const int ki = s.u.pos.k[i];
+        return (uint32_t)(s.u.pos.l[j] <= s.u.pos.l[i] && s.u.pos.k[j] <= ki && ki < s.u.pos.e[j]);
+    };
+    if ((N & 3) == 0 && ((uintptr_t)mb & 3) == 0) {
+        uint32_t* mw = reinterpret_cast<uint32_t*>(mb);
+        const int words = N * N / 4;
+        for (int w = tid; w < words; w += TB) {
+            const int e = 4 * w, i = e / N, j = e - i * N;
+            mw[w] = bit(i, j) | (bit(i, j + 1) << 8) | (bit(i, j + 2) << 16) | (bit(i, j + 3) << 24);
+        }
+    } else {
+        for (int e = tid; e < N * N; e += TB) {
+            const int i = e / N;
+            mb[e] = (uint8_t)bit(i, e - i * N);
+        }
+    }
+}
+
+}  // namespace
+
+size_t tree_build_smem_bytes() { return sizeof(TreeSmem); }
+
+cudaError_t launch_tree_build(const int32_t* cand, const int32_t* counts, const int32_t* root, int B, int C,
+                              int L, int V, int N, int32_t* tokens, int32_t* parent, int32_t* depth,
+                              uint8_t* mask, int32_t* n_nodes, int32_t* status, cudaStream_t stream) {
+    TreeParams p;
+    p.cand = cand;
+    p.counts = counts;
+    p.root = root;
+    p.B = B;
+    p.C = C;
+    p.L = L;
+    p.V = V;
+    p.N = N;
+    p.tokens = tokens;
+    p.parent = parent;
+    p.depth = depth;
+    p.mask = mask;
+    p.n_nodes = n_nodes;
+    p.status = status;
+    const int smem = (int)sizeof(TreeSmem);
+    cudaError_t e = cudaFuncSetAttribute(tree_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    tree_build_kernel<<<B, TB, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace sv

@@ -100,3 +100,15 @@ def test_lenient_verify_rejects_bad_lenience(lib, l):
     rc = lib.spec_verify_lenient(FAKE, FAKE, 0, FAKE, 2, 3, 100, SpecSampling(1.0, 1.0, 0), l, 0, 0,
                                  FAKE, FAKE, FAKE, None, None, FAKE, 1 << 30, None)
     assert rc == EINVAL
+
+
+def test_tree_build_rejects_bad_arguments(lib):
+    def T(**k):
+        a = dict(cand=FAKE, B=2, C=8, L=4, V=100, N=16, tok=FAKE, nn=FAKE)
+        a.update(k)
+        return lib.spec_tree_build(a["cand"], None, FAKE, a["B"], a["C"], a["L"], a["V"], a["N"],
+                                   a["tok"], FAKE, FAKE, None, a["nn"], None, None)
+    for kw in (dict(B=0), dict(C=0), dict(C=1025), dict(L=0), dict(L=33), dict(C=512, L=16),
+               dict(V=0), dict(N=1), dict(N=1025), dict(cand=None), dict(tok=None), dict(nn=None),
+               dict(cand=ctypes.c_void_p((1 << 20) + 2))):
+        assert T(**kw) == EINVAL, kw

@@ -28,6 +28,16 @@ pages' datasets and models are not available, these stand in for them):
                0.7 one uniformly chosen child's token gets the row max + 1.
 * mentor       B=32, gamma=5, V=32128, f32, T=1, D in {0.01, 0.1}.
                z_t ~ N(0, 2^2); z_d = z_t + N(0, 1.2^2).
+* rest         the REST step: B=16 sequences, C=256 retrieved continuations
+               of up to L=16 tokens each (a stand-in for datastore retrieval:
+               12 base continuations per sequence, chosen with Zipf(1)
+               popularity; each candidate copies its base up to a divergence
+               point ~ Geometric(0.15) and continues with uniform tokens;
+               lengths uniform in [L/2, L]); the draft tree of N=64 nodes is
+               built from them and verified against [B, N, V=32016] f32
+               logits z ~ N(0, 2^2), where, for each node with children,
+               with probability 0.7 one uniformly chosen child's token gets
+               the row max + 1.
 
 Draft tokens for the parity tests are drawn by the oracle's sampler from the
 transformed draft distribution. ``gumbel_drafts`` below is a stand-in draft
@@ -51,6 +61,8 @@ CONFIGS = {
                  force_p=0.7),
     "mentor": dict(kind="mentor", B=32, gamma=5, V=32128, dtype="f32", temperature=1.0,
                    steps=500, sd_t=2.0, sd_d=1.2, kl_bound=0.1, iters=30),
+    "rest": dict(kind="rest", B=16, N=64, V=32016, dtype="f32", C=256, L=16, bases=12,
+                 diverge=0.15, sd=2.0, force_p=0.7),
 }
 
 TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
@@ -186,12 +198,56 @@ def tree_inputs(B, N, V, seed, max_depth=6, sd=2.0, force_p=0.7, device="cpu"):
     return z.contiguous(), as_t(toks), as_t(par), as_t(dep)
 
 
+def rest_candidates(B, C, L, V, seed, bases=12, diverge=0.15):
+    """Retrieved continuations [B, C, L] int32 (-1 after each one's end)."""
+    rng = np.random.default_rng(seed)
+    out = np.full((B, C, L), -1, np.int32)
+    pop = 1.0 / np.arange(1, bases + 1)
+    pop /= pop.sum()
+    for b in range(B):
+        base = rng.integers(0, V, (bases, L))
+        pick = rng.choice(bases, size=C, p=pop)
+        cut = np.minimum(rng.geometric(diverge, size=C), L)
+        lens = rng.integers(L // 2, L + 1, size=C)
+        fresh = rng.integers(0, V, (C, L))
+        for c in range(C):
+            row = np.where(np.arange(L) < cut[c], base[pick[c]], fresh[c])
+            out[b, c, :lens[c]] = row[:lens[c]]
+    return out
+
+
+def forced_tree_logits(node_tokens, parent, n_nodes, V, seed, sd=2.0, force_p=0.7, device="cpu"):
+    """Logits [B, N, V] f32 ~ N(0, sd^2) for a built tree; for each node with
+    children, with probability force_p one uniformly chosen child's token gets
+    the row max + 1 (so the greedy walk descends)."""
+    tok = np.asarray(node_tokens)
+    par = np.asarray(parent)
+    B, N = tok.shape
+    rng = np.random.default_rng(seed)
+    forced = []
+    for b in range(B):
+        kids = [[] for _ in range(N)]
+        for i in range(1, int(n_nodes[b])):
+            kids[par[b, i]].append(i)
+        for j in range(N):
+            if kids[j] and rng.random() < force_p:
+                forced.append((b, j, int(tok[b, kids[j][int(rng.integers(len(kids[j])))]])))
+    g = _gen(seed, device)
+    z = torch.randn(B, N, V, generator=g, device=device, dtype=torch.float32) * sd
+    if forced:
+        bi = torch.tensor([f[0] for f in forced], device=device)
+        ji = torch.tensor([f[1] for f in forced], device=device)
+        ti = torch.tensor([f[2] for f in forced], device=device)
+        z[bi, ji, ti] = z[bi, ji].max(dim=1).values + 1.0
+    return z.contiguous()
+
+
 def algorithmic_bytes(kind, B, V, esize, gamma=0, N=0, temperature=1.0):
     """Bytes of logits one verification step must read (each row once).
 
     T > 0: all 2*gamma+1 rows; T = 0: the gamma+1 target rows; trees: N rows.
     """
-    if kind == "tree":
+    if kind in ("tree", "rest"):
         rows = N
     elif temperature == 0:
         rows = gamma + 1
@@ -201,8 +257,8 @@ def algorithmic_bytes(kind, B, V, esize, gamma=0, N=0, temperature=1.0):
 
 
 def verified_positions(kind, B, gamma=0, N=0):
-    """Positions a step verifies: B*gamma (linear), B*(N-1) (tree)."""
-    return B * (N - 1) if kind == "tree" else B * gamma
+    """Positions a step verifies: B*gamma (linear), B*(N-1) (tree, rest)."""
+    return B * (N - 1) if kind in ("tree", "rest") else B * gamma
 
 
 def l2_flush_bytes():
@@ -210,5 +266,6 @@ def l2_flush_bytes():
     return 512 * 1024 * 1024
 
 
-__all__ = ["CONFIGS", "linear_logits", "config_logits", "gumbel_drafts", "tree_inputs",
+__all__ = ["CONFIGS", "linear_logits", "config_logits", "gumbel_drafts", "tree_inputs", "rest_candidates",
+           "forced_tree_logits",
            "algorithmic_bytes", "verified_positions", "l2_flush_bytes"]
