@@ -13,15 +13,17 @@
 // than l), its weight the multiplicities summed over the run, its children
 // the nodes of depth l + 1 that start inside the run. So:
 //   1. candidates into shared memory, each ended at its first -1;
-//   2. bitonic sort of the candidate indices (lexicographic, index on ties);
+//   2. bitonic sort of the candidate indices (lexicographic, index on ties;
+//      each comparison made by 8 lanes reading positions in parallel);
 //   3. common-prefix length with the previous sorted candidate, prefix sums
 //      of the multiplicities, a sparse table of range minima of the common
 //      prefixes, and every node (l, k) with its run's end e (the first later
 //      candidate whose common prefix is shorter than l, found by descending
 //      the table) and its weight;
-//   4. bitonic sort of the 64-bit node keys (weight descending, length, k,
-//      then e, which (l, k) determines): the first N - 1 are the chosen nodes
-//      (k order is path order);
+//   4. the (N - 1)-th largest weight by a radix select (three 10-bit digits),
+//      then a bitonic sort of the 64-bit keys of the nodes at least that heavy
+//      (weight descending, length, k, then e, which (l, k) determines): the
+//      first N - 1 are the chosen nodes (k order is path order);
 //   5. bitonic sort of their (l, k, e) words: breadth-first positions; a
 //      node's parent is the last chosen node of depth l - 1 starting at or
 //      before k;
@@ -38,7 +40,7 @@
 namespace sv {
 namespace {
 
-constexpr int TB = 512;
+constexpr int TB = 1024;  // one radix bin per thread in the weight selection
 constexpr int TW = TB / 32;
 constexpr int kMaxC = SPEC_MAX_TREE_C;
 constexpr int kMaxCL = SPEC_MAX_TREE_CL;
@@ -81,7 +83,9 @@ struct TreeSmem {
             int32_t l[kMaxN], k[kMaxN], e[kMaxN];  // position -> depth, run start, run end
         } pos;
     } u;
+    uint32_t hist[TB];           // weight selection: digit counts
     int32_t scan[TW + 1];
+    int32_t sel[4];
     int32_t flag;
 };
 
@@ -93,13 +97,6 @@ SV_DEV int cmp_prefix(const TreeSmem& s, int LS, int a, int b, int l) {
         if (x != y) return x < y ? -1 : 1;
     }
     return 0;
-}
-
-// Candidate order: tokens, then index (a strict total order). Indices >= C pad.
-SV_DEV bool cand_less(const TreeSmem& s, int C, int L, int LS, int a, int b) {
-    if (a >= C || b >= C) return a < b;
-    const int c = cmp_prefix(s, LS, a, b, L);
-    return c != 0 ? c < 0 : a < b;
 }
 
 // Ascending bitonic sort of n (a power of two) elements; every thread calls.
@@ -167,6 +164,109 @@ SV_DEV int run_end(const TreeSmem& s, int C, int k, int l) {
     return pos;
 }
 
+// Inclusive scan of one value per thread over the CTA.
+SV_DEV int block_incl_scan(TreeSmem& s, int v) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) s.scan[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int w = lane < TW ? s.scan[lane] : 0;
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+            if (lane >= o) wi += y;
+        }
+        if (lane < TW) s.scan[lane] = wi - w;
+    }
+    __syncthreads();
+    const int r = incl + s.scan[warp];
+    __syncthreads();
+    return r;
+}
+
+SV_DEV uint32_t weight_of(unsigned long long key) { return ((1u << 30) - 1u) - (uint32_t)(key >> kKeyW); }
+
+// The R-th largest weight among the M node keys (1 <= R <= M), digit by digit
+// from the top (three 10-bit digits of the 30-bit weights).
+SV_DEV uint32_t kth_weight(TreeSmem& s, int M, int R) {
+    static_assert(TB == 1024, "one bin per thread");
+    const int tid = threadIdx.x;
+    uint32_t prefix = 0;
+    int r = R;
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = 20 - 10 * pass;
+        s.hist[tid] = 0u;
+        __syncthreads();
+        for (int o = tid; o < M; o += TB) {
+            const uint32_t w = weight_of(s.u.key[o]);
+            if (pass == 0 || (w >> (shift + 10)) == (prefix >> (shift + 10)))
+                atomicAdd(&s.hist[(w >> shift) & 1023u], 1u);
+        }
+        __syncthreads();
+        const int c = (int)s.hist[1023 - tid];  // thread t: digit 1023 - t (descending)
+        const int incl = block_incl_scan(s, c);
+        if (incl - c < r && incl >= r) {
+            s.sel[0] = 1023 - tid;
+            s.sel[1] = r - (incl - c);
+        }
+        __syncthreads();
+        prefix |= (uint32_t)s.sel[0] << shift;
+        r = s.sel[1];
+        __syncthreads();
+    }
+    return prefix;
+}
+
+// Bitonic sort of the candidate indices (lexicographic, index on ties). Each
+// comparison is made by a group of 8 lanes: lane r reads positions r, r + 8,
+// ...; the group's first differing position decides.
+SV_DEV void sort_candidates(TreeSmem& s, int C, int L, int LS, int CP) {
+    constexpr int G = TB / 8;
+    const int tid = threadIdx.x, r = tid & 7, g = tid >> 3;
+    const int pairs = CP >> 1;
+    for (int k = 2; k <= CP; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int t0 = 0; t0 < pairs; t0 += G) {  // the same trip count in every lane
+                const int t = t0 + g;
+                const bool act = t < pairs;
+                const int i = act ? (((t & ~(j - 1)) << 1) | (t & (j - 1))) : 0;  // bit j of i clear
+                const int q = i + j;
+                const int a = act ? s.ord[i] : 0, c = act ? s.ord[q] : 0;
+                const bool real = a < C && c < C;
+                int fd = L;
+                if (real) {
+                    for (int x = r; x < L; x += 8) {
+                        if (s.tok[a * LS + x] != s.tok[c * LS + x]) {
+                            fd = x;
+                            break;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) fd = min(fd, __shfl_xor_sync(0xFFFFFFFFu, fd, o, 8));
+                int cmp;
+                if (real && fd < L)
+                    cmp = s.tok[a * LS + fd] < s.tok[c * LS + fd] ? -1 : 1;
+                else
+                    cmp = a < c ? -1 : (a > c ? 1 : 0);
+                const bool swap = (i & k) == 0 ? cmp > 0 : cmp < 0;
+                if (act && r == 0 && swap) {
+                    s.ord[i] = c;
+                    s.ord[q] = a;
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
 SV_DEV int pow2_at_least(int n) {
     int p = 1;
     while (p < n) p <<= 1;
@@ -213,7 +313,7 @@ __global__ void __launch_bounds__(TB) tree_build_kernel(const __grid_constant__ 
         __syncthreads();
 
         // 2. candidates in lexicographic order
-        bitonic(s.ord, CP, [&](int a, int c) { return cand_less(s, C, L, LS, a, c); });
+        sort_candidates(s, C, L, LS, CP);
 
         // 3. common prefixes, multiplicity sums, nodes
         for (int k = tid; k < C; k += TB) {
@@ -250,11 +350,36 @@ __global__ void __launch_bounds__(TB) tree_build_kernel(const __grid_constant__ 
                 s.u.key[o] = ((unsigned long long)((1u << 30) - 1u - w) << kKeyW) | word_of(l, k, e);
             }
         }
-        const int MP = pow2_at_least(max(M, 1));
-        for (int i = M + tid; i < MP; i += TB) s.u.key[i] = ~0ull;
         __syncthreads();
 
-        // 4. the heaviest N - 1 nodes
+        // 4. the heaviest N - 1 nodes: only those at least as heavy as the
+        // (N - 1)-th are sorted
+        int Mk = M;
+        if (M > N - 1) {
+            const uint32_t tau = kth_weight(s, M, N - 1);
+            constexpr int kPer = kMaxCL / TB;
+            unsigned long long mine[kPer];
+            bool keep[kPer];
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {
+                const int o = tid + u * TB;
+                keep[u] = o < M;
+                if (keep[u]) {
+                    mine[u] = s.u.key[o];
+                    keep[u] = weight_of(mine[u]) >= tau;
+                }
+            }
+            if (tid == 0) s.sel[2] = 0;
+            __syncthreads();
+#pragma unroll
+            for (int u = 0; u < kPer; ++u)
+                if (keep[u]) s.u.key[atomicAdd(&s.sel[2], 1)] = mine[u];
+            __syncthreads();
+            Mk = s.sel[2];
+        }
+        const int MP = pow2_at_least(max(Mk, 1));
+        for (int i = Mk + tid; i < MP; i += TB) s.u.key[i] = ~0ull;
+        __syncthreads();
         bitonic(s.u.key, MP, [](unsigned long long x, unsigned long long y) { return x < y; });
         const int S = min(N - 1, M);
         const int SP = pow2_at_least(max(S, 1));
