@@ -54,5 +54,7 @@ from .spec import (
     expected_tokens,
     walltime_factor,
     ops_factor,
+    best_gamma,
+    estimate_alpha,
 )
 from .rest import MAX_COUNT as REST_MAX_COUNT, rest_tree, rest_tree_batch

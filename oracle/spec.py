@@ -659,3 +659,30 @@ def ops_factor(alpha, gamma, c_hat):
     [SD] "运算量分析"; c_hat is the draft-to-target cost ratio per token.
     """
     return (gamma * c_hat + gamma + 1.0) / expected_tokens(alpha, gamma)
+
+
+
+def best_gamma(alpha, c, gamma_max):
+    """The draft length in 1..gamma_max with the largest walltime factor
+    (the smallest such length on ties).
+
+    [SD] "方法细节" and its FAQ on choosing gamma: alpha is measured, c is
+    the draft-to-target cost ratio, and gamma is chosen by maximising
+    (1 - alpha^(gamma+1)) / ((1 - alpha)(gamma c + 1)) numerically.
+    """
+    best, arg = -1.0, 1
+    for g in range(1, gamma_max + 1):
+        f = walltime_factor(alpha, g, c)
+        if f > best:
+            best, arg = f, g
+    return arg
+
+
+def estimate_alpha(beta):
+    """alpha = E(beta): the mean of per-position acceptance probabilities.
+
+    [SD] "接受率精确刻画": alpha is the expectation of beta = sum_x min(p, q)
+    over the positions (the page measures it over 10K tokens).
+    """
+    b = np.asarray(beta, np.float64)
+    return float(b.mean())
