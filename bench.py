@@ -50,8 +50,10 @@ WORKLOADS = {
     "mentor": ("mentor", 12, None),
     "rest": ("rest", 4, None),
     "nucleus_lenient": ("nucleus", 1000, None),
+    "nucleus_alpha": ("nucleus", 1000, None),
 }
 LENIENCE = {"nucleus_lenient": 0.5}   # lenient verification (l < 1); others are exact
+OPS = {"nucleus_alpha": "alpha"}      # measured acceptance probabilities instead of verification
 
 # The timed unit is one library call; where a call launches several kernels the
 # label names them all (the row or argmax kernel reads every logit byte).
@@ -60,7 +62,8 @@ KERNEL_OF = {"nucleus": "row_kernel<bf16,transform> + draw_kernel", "tiny": "row
              "tree": "argmax_kernel<f32>",
              "mentor": "row_kernel<f32> + mentor_kernel + mentor_resolve_kernel",
              "nucleus_lenient": "row_kernel<bf16,transform> + draw_kernel",
-             "rest": "tree_build_kernel + argmax_kernel<f32>"}
+             "rest": "tree_build_kernel + argmax_kernel<f32>",
+             "nucleus_alpha": "row_kernel<bf16,transform> (records) + beta_kernel"}
 
 
 def dist_env():
@@ -172,6 +175,8 @@ def make_inputs(name, steps_stacked, temperature, device, seed=2024, lenience=1.
 def run_step(inp):
     import speculative_decoding_verification_05_gb300 as sv
 
+    if inp.get("op") == "alpha":
+        return sv.acceptance_rate(inp["zt"], inp["zd"], inp["T"], inp["top_p"], 0)
     if inp["kind"] == "rest":
         t = sv.tree_build(inp["cand"], inp["root"], inp["V"], inp["N"])
         return sv.verify_tree(inp["z"], t["node_tokens"], t["parent"], t["depth"], inp["max_depth"])
@@ -186,6 +191,8 @@ def run_step_host(inp, host):
     """End-to-end through the public API: pinned host inputs in, host outputs back."""
     import speculative_decoding_verification_05_gb300 as sv
 
+    if inp.get("op") == "alpha":
+        return sv.acceptance_rate(host["zt"], host["zd"], inp["T"], inp["top_p"], 0)
     if inp["kind"] == "rest":
         # two public calls on host buffers: the tree (and its mask) comes back in between
         t = sv.tree_build(host["cand"], host["root"], inp["V"], inp["N"])
@@ -201,6 +208,10 @@ def run_step_host(inp, host):
 
 def algorithmic(inp):
     """(bytes, verified positions) one step must read / decides."""
+    if inp.get("op") == "alpha":
+        # each of the 2 gamma rows of a position pair read once (the bonus row is not needed)
+        B, G = inp["B"], inp["gamma"]
+        return B * 2 * G * inp["V"] * inp["esize"], B * G
     if inp["kind"] == "rest":
         # logits once, the candidates once, the tree arrays and mask written once
         B, N = inp["B"], inp["N"]
@@ -220,18 +231,33 @@ def launches_per_step(inp):
     (mentor); the argmax kernel (tree, T = 0); rows and draws otherwise."""
     if inp["kind"] == "mentor":
         return 3
-    if inp["kind"] == "rest":
+    if inp["kind"] == "rest" or inp.get("op") == "alpha":
         return 2
     if inp["kind"] == "tree" or inp["T"] == 0:
         return 1
     return 2
 
 
-def cpu_baseline(name, temperature, budget_s=12.0, lenience=1.0):
+def cpu_baseline(name, temperature, budget_s=12.0, lenience=1.0, op="verify"):
     """The oracle, as it stands, on a bounded sample of the workload (host cores)."""
     import oracle
 
     c = dict(workloads.CONFIGS[name])
+    if op == "alpha":
+        B, G, V = c["B"], c["gamma"], c["V"]
+        zt, zd = workloads.config_logits(name, 99, steps=1)
+        zt, zd = zt.float().numpy(), zd.float().numpy()
+        T, tp = c["temperature"], c.get("top_p", 1.0)
+        t0 = time.perf_counter()
+        n = 0
+        while time.perf_counter() - t0 < budget_s:
+            q, _ = oracle.transformed_probs(zt[:, :G].reshape(-1, V), T, 0, tp)
+            p, _ = oracle.transformed_probs(zd.reshape(-1, V), T, 0, tp)
+            oracle.acceptance_rate(q, p)
+            n += 1
+        dt = time.perf_counter() - t0
+        return {"value": n * B * G / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": f"{n} steps of B={B} ({n * B * G} positions' beta, V={V}) in {dt:.1f} s"}
     if c["kind"] == "rest":
         B = c["B"]
         cand = workloads.rest_candidates(B, c["C"], c["L"], c["V"], 99, bases=c["bases"], diverge=c["diverge"])
@@ -286,8 +312,9 @@ def reference_arm(args):
     cfg, _, temp = WORKLOADS[args.workload]
     lv = LENIENCE.get(args.workload, 1.0)
     for _ in range(args.warmup):
-        cpu_baseline(cfg, temp, budget_s=1.0, lenience=lv)
-    vals = [cpu_baseline(cfg, temp, budget_s=max(2.0, 60.0 / max(1, args.steps)), lenience=lv)
+        cpu_baseline(cfg, temp, budget_s=1.0, lenience=lv, op=OPS.get(args.workload, "verify"))
+    vals = [cpu_baseline(cfg, temp, budget_s=max(2.0, 60.0 / max(1, args.steps)), lenience=lv,
+                         op=OPS.get(args.workload, "verify"))
             for _ in range(args.steps)]
     v = statistics.median(x["value"] for x in vals)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
@@ -329,6 +356,7 @@ def main():
     if args.stack > 0:
         stacked = args.stack
     inp = make_inputs(cfg, stacked, temp, device, seed=2024 + rank, lenience=LENIENCE.get(args.workload, 1.0))
+    inp["op"] = OPS.get(args.workload, "verify")
     nbytes, npos = algorithmic(inp)
     stream = torch.cuda.current_stream(device)
 
@@ -379,6 +407,7 @@ def main():
         acc_mean = float(out["accepted"].float().mean().item())
     elif "accept_len" in out:
         acc_mean = float(out["accept_len"].float().mean().item())
+    alpha_est = float(out["beta"].float().mean().item()) if "beta" in out else None
 
     e2e = None
     if not args.no_e2e:
@@ -407,7 +436,8 @@ def main():
             "traffic": recorded_traffic(args.workload) if args.stack in (0, WORKLOADS[args.workload][1]) else None,
             "kernel": KERNEL_OF[args.workload], "algorithmic_bytes_per_launch": nbytes,
             "peak_source": f"{peak_kind} hbm_gbs (copy)", "frac_of_nominal_8TBps": achieved / 8000.0}
-    cpu = None if args.no_cpu else cpu_baseline(cfg, temp, lenience=LENIENCE.get(args.workload, 1.0))
+    cpu = None if args.no_cpu else cpu_baseline(cfg, temp, lenience=LENIENCE.get(args.workload, 1.0),
+                                                op=OPS.get(args.workload, "verify"))
     c = workloads.CONFIGS[cfg]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -423,7 +453,7 @@ def main():
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step(inp) * args.steps,
         "clocks": dict(clk.summary(), window="warm-up + timed steps (+ untimed steps up to 0.3 s)"),
-        "hbm_gbs": achieved, "mean_accepted": acc_mean,
+        "hbm_gbs": achieved, "mean_accepted": acc_mean, **({"alpha": alpha_est} if alpha_est is not None else {}),
     }
     print(json.dumps(line))
     return 0

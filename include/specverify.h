@@ -229,6 +229,46 @@ spec_status spec_tree_build(const int32_t* candidates, const int32_t* counts, co
                             int32_t* n_nodes, int32_t* status, spec_stream stream);
 
 /* ------------------------------------------------------------------------
+ * spec_acceptance_rate - the probability that each draft position is
+ * accepted ([SD] "方法细节", 接受率精确刻画; [SpS] appendix proof of Theorem
+ * 1): beta[b, k] = sum_x min(q_k(x), p_k(x)) for target row k and draft row
+ * k (k < gamma) of sequence b, under the same temperature / top-k / top-p
+ * transform as spec_verify. The mean of beta over positions estimates the
+ * acceptance rate alpha that spec_expected_tokens and spec_best_gamma take.
+ *
+ * Arguments as spec_verify (no draft tokens are needed); temperature must be
+ * > 0 (at temperature 0, beta is 1 where the two argmaxes agree and 0
+ * elsewhere; that case returns SPEC_EINVAL).
+ *   beta          [B, gamma] float (device); NaN for a pair with a non-finite
+ *                 row
+ *   status        [B] SPEC_OK / SPEC_EDATA; NULL allowed
+ *   workspace     >= spec_verify_workspace_size(B, gamma, V, dtype) bytes
+ * ---------------------------------------------------------------------- */
+spec_status spec_acceptance_rate(const void* target, const void* draft, spec_dtype dtype, int B, int gamma,
+                                 int V, spec_sampling sampling, float* beta, int32_t* status,
+                                 void* workspace, size_t ws_bytes, spec_stream stream);
+
+/* ------------------------------------------------------------------------
+ * The alpha / gamma planner ([SD] "方法细节": 期望生成 token 数, 墙钟加速因子,
+ * 运算量分析, and its FAQ on choosing gamma). Host arithmetic, no GPU:
+ *   spec_expected_tokens  E[#tokens per target call] =
+ *                         (1 - alpha^(gamma+1)) / (1 - alpha), gamma + 1 at
+ *                         alpha = 1 (i.i.d. acceptance with rate alpha)
+ *   spec_walltime_factor  spec_expected_tokens / (gamma c + 1), c the cost of
+ *                         one draft call relative to one target call
+ *   spec_ops_factor       (gamma c_hat + gamma + 1) / spec_expected_tokens,
+ *                         c_hat the draft-to-target cost ratio per token
+ *   spec_best_gamma       the gamma in 1..gamma_max with the largest
+ *                         walltime factor (the smallest on ties)
+ * alpha must lie in [0, 1], gamma >= 0, c and c_hat finite and >= 0;
+ * otherwise the factors are NaN and spec_best_gamma returns -1.
+ * ---------------------------------------------------------------------- */
+double spec_expected_tokens(double alpha, int gamma);
+double spec_walltime_factor(double alpha, int gamma, double c);
+double spec_ops_factor(double alpha, int gamma, double c_hat);
+int spec_best_gamma(double alpha, double c, int gamma_max);
+
+/* ------------------------------------------------------------------------
  * spec_verify_mentor - lossy "mentor" verification ([Mentor] "导师解码",
  * "解决优化问题").
  *

@@ -31,7 +31,8 @@ PURPOSE_ACCEPT, PURPOSE_RESAMPLE, PURPOSE_DRAFT = 0, 1, 2
 
 EXPORTED = [
     "spec_verify_workspace_size", "spec_verify", "spec_verify_lenient",
-    "spec_verify_tree_workspace_size", "spec_verify_tree", "spec_tree_build",
+    "spec_verify_tree_workspace_size", "spec_verify_tree", "spec_tree_build", "spec_acceptance_rate",
+    "spec_expected_tokens", "spec_walltime_factor", "spec_ops_factor", "spec_best_gamma",
     "spec_verify_mentor_workspace_size", "spec_verify_mentor",
     "spec_sample_workspace_size", "spec_sample",
     "spec_philox_uniform", "spec_verify_noalloc", "spec_status_string", "spec_last_cuda_error",
@@ -79,6 +80,17 @@ def load_library(path=LIB_PATH):
         lib.spec_verify_tree.restype = _I
         lib.spec_tree_build.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]
         lib.spec_tree_build.restype = _I
+        lib.spec_acceptance_rate.argtypes = [_P, _P, _I, _I, _I, _I, SpecSampling, _P, _P, _P, _SZ, _P]
+        lib.spec_acceptance_rate.restype = _I
+        _D = ctypes.c_double
+        lib.spec_expected_tokens.argtypes = [_D, _I]
+        lib.spec_expected_tokens.restype = _D
+        lib.spec_walltime_factor.argtypes = [_D, _I, _D]
+        lib.spec_walltime_factor.restype = _D
+        lib.spec_ops_factor.argtypes = [_D, _I, _D]
+        lib.spec_ops_factor.restype = _D
+        lib.spec_best_gamma.argtypes = [_D, _D, _I]
+        lib.spec_best_gamma.restype = _I
         lib.spec_verify_mentor_workspace_size.argtypes = [_I, _I, _I, _I]
         lib.spec_verify_mentor_workspace_size.restype = _SZ
         lib.spec_verify_mentor.argtypes = [_P, _P, _I, _P, _I, _I, _I, ctypes.c_float, ctypes.c_float,
@@ -273,6 +285,48 @@ def tree_build(candidates, root_token, V, N, counts=None, with_mask=True):
     return sg.back(o)
 
 
+def acceptance_rate(target, draft, temperature=1.0, top_p=1.0, top_k=0):
+    """beta [B, gamma] = sum_x min(q_k(x), p_k(x)) per position (temperature > 0),
+    and status [B]; the mean of beta estimates the acceptance rate alpha."""
+    lib = load_library()
+    sg = _Staging(target)
+    target, draft = sg.dev(target), sg.dev(draft)
+    B, G1, V = target.shape
+    gamma = G1 - 1
+    if draft.shape != (B, gamma, V) or draft.dtype != target.dtype:
+        raise SpecError("shape or dtype mismatch between target and draft")
+    o = {"beta": sg.out((B, gamma), torch.float32), "status": sg.out((B,))}
+    dt = _dtype_code(target)
+    stream = torch.cuda.current_stream(sg.device)
+    ws = workspace(lib.spec_verify_workspace_size(B, gamma, V, dt), sg.device, stream)
+    rc = lib.spec_acceptance_rate(_ptr(target), _ptr(draft), dt, B, gamma, V,
+                                  SpecSampling(float(temperature), float(top_p), int(top_k)),
+                                  _ptr(o["beta"]), _ptr(o["status"]), _ptr(ws), ws.numel(),
+                                  ctypes.c_void_p(stream.cuda_stream))
+    _check(rc)
+    return sg.back(o)
+
+
+def expected_tokens(alpha, gamma):
+    """E[#tokens per target call] for acceptance rate alpha and draft length gamma."""
+    return load_library().spec_expected_tokens(float(alpha), int(gamma))
+
+
+def walltime_factor(alpha, gamma, c):
+    """Expected walltime improvement for draft cost ratio c."""
+    return load_library().spec_walltime_factor(float(alpha), int(gamma), float(c))
+
+
+def ops_factor(alpha, gamma, c_hat):
+    """Expected factor on the total number of operations."""
+    return load_library().spec_ops_factor(float(alpha), int(gamma), float(c_hat))
+
+
+def best_gamma(alpha, c, gamma_max):
+    """The draft length in 1..gamma_max with the largest walltime factor."""
+    return load_library().spec_best_gamma(float(alpha), float(c), int(gamma_max))
+
+
 def verify_mentor(target, draft, draft_tokens, temperature=1.0, kl_bound=0.0, bisect_iters=30,
                   seed=0, offset=0, debug=False):
     """Lossy mentor verification; returns the ``verify`` outputs plus alpha and beta [B, gamma]."""
@@ -331,5 +385,6 @@ def philox_uniform(seed, row0, position, purpose, n, device=None):
     return out
 
 
-__all__ = ["philox_uniform", "verify", "verify_tree", "tree_build", "verify_mentor", "sample", "load_library", "workspace",
+__all__ = ["philox_uniform", "verify", "verify_tree", "tree_build", "acceptance_rate", "expected_tokens",
+           "walltime_factor", "ops_factor", "best_gamma", "verify_mentor", "sample", "load_library", "workspace",
            "SpecError", "SpecSampling", "EXPORTED", "LIB_PATH"]

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspecverify.so")
 SOURCES = ["csrc/api.cu", "csrc/rows.cu", "csrc/argmax.cu", "csrc/mentor.cu", "csrc/noalloc.cu",
-           "csrc/tree_build.cu"]
+           "csrc/tree_build.cu", "csrc/beta.cu", "csrc/planner.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
           "-Xptxas", "-v", "-I", os.path.join(ROOT, "include"), "-I", os.path.join(HERE, "csrc")]

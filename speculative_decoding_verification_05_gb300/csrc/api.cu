@@ -371,6 +371,44 @@ spec_status spec_tree_build(const int32_t* candidates, const int32_t* counts, co
     return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
 }
 
+spec_status spec_acceptance_rate(const void* target, const void* draft, spec_dtype dtype, int B, int gamma,
+                                 int V, spec_sampling sampling, float* beta, int32_t* status,
+                                 void* workspace, size_t ws_bytes, spec_stream stream) {
+    if (!dtype_ok(dtype) || !sampling_ok(sampling) || sampling.temperature <= 0.f) return SPEC_EINVAL;
+    if (B < 1 || B > (1 << 24) || gamma < 1 || gamma > SPEC_MAX_GAMMA || V < 1 || V > SPEC_MAX_V)
+        return SPEC_EINVAL;
+    if (!target || !draft || !beta || !workspace) return SPEC_EINVAL;
+    const int es = esize(dtype);
+    if (!aligned(target, es) || !aligned(draft, es) || !aligned(beta, 4) || !aligned(status, 4) ||
+        !aligned(workspace, kAlign))
+        return SPEC_EINVAL;
+    const Ws w = ws_layout(B, 2 * gamma + 1, V);
+    if (ws_bytes < w.total) return SPEC_EINVAL;
+    const float c2 = kLog2e / sampling.temperature;
+    if (!std::isfinite(c2)) return SPEC_EINVAL;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int dt = dtype == SPEC_F32 ? 0 : 1;
+    sv::RowParams p = {};
+    p.target = target;
+    p.draft = draft;
+    p.draft_tokens = nullptr;  // records only: no acceptance test
+    p.B = B;
+    p.gamma = gamma;
+    p.V = V;
+    p.rows_per_b = 2 * gamma + 1;
+    p.mode = sv::kModeMentor;  // the row kernel writes the records and nothing else
+    p.lenience = 1.f;
+    p.transform = transform_bits(sampling, V);
+    p.top_k = sampling.top_k;
+    p.top_p = sampling.top_p;
+    p.c2 = c2;
+    p.status = status;
+    spec_status s = run_rows(p, dt, workspace, w, st);
+    if (s != SPEC_OK) return s;
+    const cudaError_t e = sv::launch_beta(p, dt, beta, device_sms(), st);
+    return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
+}
+
 size_t spec_verify_mentor_workspace_size(int B, int gamma, int V, spec_dtype dtype) {
     (void)dtype;
     if (B < 1 || gamma < 1 || V < 1) return 0;

@@ -350,6 +350,9 @@ cudaError_t launch_draws(const RowParams& p, int dtype, int sms, cudaStream_t st
 cudaError_t launch_argmax(const ArgmaxParams& p, int dtype, int grid, cudaStream_t stream);
 // Position kernel on `grid` persistent CTAs, then the per-sequence resolve.
 cudaError_t launch_mentor(const MentorParams& p, int grid, int resolve_grid, cudaStream_t stream);
+// beta[b, k] = sum_x min(q(x), p(x)) of every target / draft row pair, from
+// the row records (persistent CTAs over the B * gamma pairs).
+cudaError_t launch_beta(const RowParams& p, int dtype, float* beta, int sms, cudaStream_t stream);
 // REST draft-tree construction: one CTA per sequence.
 size_t tree_build_smem_bytes();
 cudaError_t launch_tree_build(const int32_t* cand, const int32_t* counts, const int32_t* root, int B, int C,

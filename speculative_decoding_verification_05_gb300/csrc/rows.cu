@@ -385,11 +385,11 @@ SV_DEV RowRef<E> row_ref(const RowParams& p, int b, int r) {
     } else if (r <= p.gamma) {
         rr.ptr = reinterpret_cast<const E*>(p.target) + ((size_t)b * (p.gamma + 1) + r) * p.V;
         rr.k = r;
-        rr.has_x = r < p.gamma;
+        rr.has_x = r < p.gamma && p.draft_tokens != nullptr;  // records without tokens: no test
     } else {
         rr.k = r - p.gamma - 1;
         rr.ptr = reinterpret_cast<const E*>(p.draft) + ((size_t)b * p.gamma + rr.k) * p.V;
-        rr.has_x = true;
+        rr.has_x = p.draft_tokens != nullptr;
     }
     return rr;
 }

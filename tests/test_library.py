@@ -112,3 +112,39 @@ def test_tree_build_rejects_bad_arguments(lib):
                dict(V=0), dict(N=1), dict(N=1025), dict(cand=None), dict(tok=None), dict(nn=None),
                dict(cand=ctypes.c_void_p((1 << 20) + 2))):
         assert T(**kw) == EINVAL, kw
+
+
+def test_planner_matches_oracle(lib):
+    import math
+
+    import numpy as np
+
+    import oracle
+    rng = np.random.default_rng(4)
+    for _ in range(300):
+        a = float(rng.choice([0.0, 1.0, rng.random()]))
+        g = int(rng.integers(0, 40))
+        c = float(rng.choice([0.0, rng.random(), 10 * rng.random()]))
+        assert sv.expected_tokens(a, g) == pytest.approx(oracle.expected_tokens(a, g), rel=1e-14)
+        assert sv.walltime_factor(a, g, c) == pytest.approx(oracle.walltime_factor(a, g, c), rel=1e-14)
+        assert sv.ops_factor(a, g, c) == pytest.approx(oracle.ops_factor(a, g, c), rel=1e-14)
+        if g >= 1 and a < 0.999:
+            assert sv.best_gamma(a, c, g) == oracle.best_gamma(a, c, g)
+    # the appendix E worked example: zero-cost draft, alpha 0.9, gamma 10
+    assert round(sv.walltime_factor(0.9, 10, 0.0), 2) == 6.86 and round(sv.ops_factor(0.9, 10, 0.0), 1) == 1.6
+    for bad in ((-0.1, 3), (1.1, 3), (float("nan"), 3), (0.5, -1)):
+        assert math.isnan(sv.expected_tokens(*bad))
+    assert math.isnan(sv.walltime_factor(0.5, 3, -1.0)) and math.isnan(sv.ops_factor(0.5, 3, float("inf")))
+    assert sv.best_gamma(0.5, 0.1, 0) == -1 and sv.best_gamma(2.0, 0.1, 5) == -1 and sv.best_gamma(0.5, -1, 5) == -1
+
+
+def test_acceptance_rate_rejects_bad_arguments(lib):
+    def A(**k):
+        a = dict(t=FAKE, d=FAKE, B=2, G=3, V=100, s=SpecSampling(1.0, 1.0, 0), beta=FAKE, ws=FAKE)
+        a.update(k)
+        return lib.spec_acceptance_rate(a["t"], a["d"], 0, a["B"], a["G"], a["V"], a["s"], a["beta"], None,
+                                        a["ws"], 1 << 30, None)
+    for kw in (dict(B=0), dict(G=0), dict(V=0), dict(t=None), dict(d=None), dict(beta=None), dict(ws=None),
+               dict(s=SpecSampling(0.0, 1.0, 0)), dict(s=SpecSampling(1.0, 0.0, 0)),
+               dict(beta=ctypes.c_void_p((1 << 20) + 2))):
+        assert A(**kw) == EINVAL, kw
