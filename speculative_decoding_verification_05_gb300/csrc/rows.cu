@@ -51,7 +51,7 @@ constexpr int NW = NT / 32;
 constexpr int kMaxRows = 2 * 255 + 1;  // rows per sequence (verification, gamma <= 255)
 constexpr int kU = 4;                  // 16-byte vectors in flight per thread
 constexpr int kWin = 13;               // stored keys: within 2^-kWin of the row max (plus one octave)
-constexpr int kSlotBytes = 96;         // key slots per thread, in bytes
+constexpr int kSlotBytes = 128;        // key slots per thread, in bytes
 constexpr int kSel = 256;              // keys compared exactly inside the crossing bin
 constexpr int kOrd = 2048;             // bf16 ordinal histogram: bins
 constexpr uint32_t kPrefetchBytes = 65536;  // next units up to this size are prefetched into L2
@@ -75,7 +75,8 @@ struct Shared {
     unsigned long long ured2[NW];
     int bi[8];
     float bf[8];
-    unsigned short hn[NT];            // stored keys per thread
+    unsigned short hn[NT];            // stored keys (fp32) or key pairs (bf16) per thread
+    float cut;                        // the row's storage cut
     union {
         GenSel g;                     // binned selection (fp32 rows, global fallback)
         unsigned ocnt[kOrd];          // bf16 rows: stored keys per distinct value
@@ -144,6 +145,27 @@ struct Collect {
     }
 };
 
+// bf16 rows: the 32-bit word of two adjacent logits goes to the thread's
+// slots when either of them is above `cut` (one store per pair); the reader
+// checks both halves against the cut again.
+struct PairCollect {
+    static constexpr int kPer = kSlotBytes / 4;
+    uint32_t* base;  // slot 0 of this thread; slot c at base[c * NT]
+    float cut;
+    int hc;
+    // branch-free, for when a slot is free
+    SV_DEV void put(float lo, float hi, uint32_t w) {
+        base[hc * NT] = w;
+        hc += (lo > cut) | (hi > cut);
+    }
+    SV_DEV void safe(float lo, float hi, uint32_t w) {
+        if ((lo > cut) | (hi > cut)) {
+            if (hc < kPer) base[hc * NT] = w;
+            ++hc;
+        }
+    }
+};
+
 template <typename E>
 struct Core;
 
@@ -151,8 +173,8 @@ struct Core;
 template <>
 struct Core<bf16_t> {
     static constexpr int VE = 8;
-    using Key = uint16_t;
-    static constexpr int kPer = kSlotBytes / (int)sizeof(Key);
+    using Key = uint32_t;
+    using Col = PairCollect;
     struct St {
         uint32_t pm;
         float2 s0, s1;
@@ -168,24 +190,16 @@ struct Core<bf16_t> {
         float2 a0 = make_float2(bf_lo(v.x), bf_hi(v.x)), a1 = make_float2(bf_lo(v.y), bf_hi(v.y));
         float2 a2 = make_float2(bf_lo(v.z), bf_hi(v.z)), a3 = make_float2(bf_lo(v.w), bf_hi(v.w));
         if (COL) {
-            if (col.hc <= C::kPer - 8) {  // room for the whole vector
-                col.put(a0.x, v.x);
-                col.put(a0.y, v.x >> 16);
-                col.put(a1.x, v.y);
-                col.put(a1.y, v.y >> 16);
-                col.put(a2.x, v.z);
-                col.put(a2.y, v.z >> 16);
-                col.put(a3.x, v.w);
-                col.put(a3.y, v.w >> 16);
+            if (col.hc <= PairCollect::kPer - 4) {  // room for the whole vector
+                col.put(a0.x, a0.y, v.x);
+                col.put(a1.x, a1.y, v.y);
+                col.put(a2.x, a2.y, v.z);
+                col.put(a3.x, a3.y, v.w);
             } else {
-                col(a0.x, v.x & 0xFFFFu);
-                col(a0.y, v.x >> 16);
-                col(a1.x, v.y & 0xFFFFu);
-                col(a1.y, v.y >> 16);
-                col(a2.x, v.z & 0xFFFFu);
-                col(a2.y, v.z >> 16);
-                col(a3.x, v.w & 0xFFFFu);
-                col(a3.y, v.w >> 16);
+                col.safe(a0.x, a0.y, v.x);
+                col.safe(a1.x, a1.y, v.y);
+                col.safe(a2.x, a2.y, v.z);
+                col.safe(a3.x, a3.y, v.w);
             }
         }
         a0 = __ffma2_rn(a0, c2v, nr2);
@@ -210,7 +224,7 @@ struct Core<bf16_t> {
         const uint32_t raw = __ldg(reinterpret_cast<const unsigned short*>(p));
         st.pm = bmax2(st.pm, raw | (raw << 16));
         const float x = __uint_as_float(raw << 16);
-        if (COL) col(x, raw);
+        if (COL) col.safe(x, -INFINITY, raw | 0xFF800000u);  // the other half -inf
         st.s0.x += ex2(fmaf(x, c2, nref));
     }
     SV_DEV static float maxof(const St& st) { return max_nan(bf_lo(st.pm), bf_hi(st.pm)); }
@@ -225,6 +239,7 @@ template <>
 struct Core<float> {
     static constexpr int VE = 4;
     using Key = uint32_t;
+    using Col = Collect<uint32_t>;
     struct St {
         float pm;
         float2 s0, s1;
@@ -310,7 +325,7 @@ __device__ __noinline__ RowStats stream_row(Shared& s, const E* row, int i0, int
     const float2 c2v = make_float2(c2, c2), nr2 = make_float2(nref, nref);
     typename C::St st = C::init();
     using K = typename C::Key;
-    Collect<K> col{reinterpret_cast<K*>(s.u.slots) + tid, ref - wc, 0};
+    typename C::Col col{reinterpret_cast<K*>(s.u.slots) + tid, ref - wc, 0};
     if (tid < head) C::template one<COL>(st, row + i0 + tid, c2, nref, col);
 #pragma unroll
     for (int u = 0; u < kU; ++u)
@@ -326,8 +341,9 @@ __device__ __noinline__ RowStats stream_row(Shared& s, const E* row, int i0, int
     const int t = base + nb * VE + tid;
     if (t < i1) C::template one<COL>(st, row + t, c2, nref, col);
     if (COL) {
-        s.hn[tid] = (unsigned short)min(col.hc, Collect<K>::kPer);
-        if (col.hc > Collect<K>::kPer) s.ovf = 1;
+        s.hn[tid] = (unsigned short)min(col.hc, C::Col::kPer);
+        if (col.hc > C::Col::kPer) s.ovf = 1;
+        if (tid == 0) s.cut = ref - wc;
     }
     // block reduction: maximum (NaN-propagating), sum in a fixed order
     float tm = C::maxof(st), ts = C::sumof(st);
@@ -706,15 +722,23 @@ __device__ __noinline__ bool bf16_threshold(Shared& s, const RowParams& p, float
         __syncthreads();
         if (tid == 0) s.odirty = 0;
     }
-    const uint16_t* slots = reinterpret_cast<const uint16_t*>(s.u.slots);
+    const uint32_t* slots = reinterpret_cast<const uint32_t*>(s.u.slots);
     const int n = s.hn[tid];
+    const float cut = s.cut;
     int jm = -1;
+    auto count = [&](uint32_t raw) {
+        if (__uint_as_float(raw << 16) > cut) {
+            const int j = top - (int)ord16(raw);
+            if (j < kOrd) {
+                atomicAdd(&s.h.ocnt[j], 1u);
+                jm = max(jm, j);
+            }  // below it: not needed, the counted values stay an upper set
+        }
+    };
     for (int c = 0; c < n; ++c) {
-        const int j = top - (int)ord16(slots[c * NT + tid]);
-        if (j < kOrd) {
-            atomicAdd(&s.h.ocnt[j], 1u);
-            jm = max(jm, j);
-        }  // below it: not needed, the counted values stay an upper set
+        const uint32_t w = slots[c * NT + tid];
+        count(w & 0xFFFFu);
+        count(w >> 16);
     }
     jm = __reduce_max_sync(0xFFFFFFFFu, jm);
     if (lane == 0 && jm >= 0) atomicMax(&s.jmax, jm);
@@ -810,6 +834,29 @@ __device__ __noinline__ bool bf16_threshold(Shared& s, const RowParams& p, float
     return ok;
 }
 
+// Stores the pairs of a bf16 row again, with the cut of the finished row (its
+// maximum minus the window), after a thread's slots overflowed under the
+// provisional cut of the streaming pass. The row was just read, so this pass
+// mostly hits L2. Every thread must call it.
+SV_DEV void recollect_bf16(Shared& s, const bf16_t* row, int V, float cut) {
+    const int tid = threadIdx.x;
+    const unsigned short* rs = reinterpret_cast<const unsigned short*>(row);
+    __syncthreads();  // every thread has read the overflow flag
+    if (tid == 0) {
+        s.ovf = 0;
+        s.cut = cut;
+    }
+    PairCollect col{reinterpret_cast<uint32_t*>(s.u.slots) + tid, cut, 0};
+    for (int i = 2 * tid; i < V; i += 2 * NT) {
+        const uint32_t lo = __ldg(rs + i), hi = i + 1 < V ? (uint32_t)__ldg(rs + i + 1) : 0xFF80u;
+        col.safe(__uint_as_float(lo << 16), __uint_as_float(hi << 16), lo | (hi << 16));
+    }
+    __syncthreads();  // the flag's reset before any thread sets it
+    s.hn[tid] = (unsigned short)min(col.hc, PairCollect::kPer);
+    if (col.hc > PairCollect::kPer) s.ovf = 1;
+    __syncthreads();
+}
+
 // Threshold and kept mass of a row: from the stored keys when they decide it,
 // else from the row in global memory.
 template <typename E>
@@ -818,8 +865,14 @@ __device__ __noinline__ void row_threshold(Shared& s, const RowParams& p, const 
     const int tid = threadIdx.x;
     const float c2 = p.c2, mc = m * c2;
     constexpr int npass = sizeof(E) == 4 ? 4 : 2;
-    if (use_slots && !s.ovf) {
-        if (sizeof(E) == 2 && bf16_threshold(s, p, m, S, thr, sk)) return;
+    if constexpr (sizeof(E) == 2) {
+        if (use_slots) {
+            if (s.ovf) recollect_bf16(s, row, p.V, m - (float)(kWin + 1) / c2);
+            // the stored pairs hold every value above the cut: when they do
+            // not decide the threshold, only the row itself can
+            if (!s.ovf && bf16_threshold(s, p, m, S, thr, sk)) return;
+        }
+    } else if (use_slots && !s.ovf) {
         using K = typename Core<E>::Key;
         const K* slots = reinterpret_cast<const K*>(s.u.slots);
         const int n = s.hn[tid];
