@@ -15,18 +15,20 @@
 // reference is summed again against m). The last segment of a row to finish
 // writes the row's record (maximum, sum, top-k / top-p threshold and kept
 // mass); the last row of a sequence to finish resolves the sequence (no
-// thread ever waits for another CTA):
-//
-//   * acceptance left to right, u_k < min(1, q(x_k)/p(x_k)), stopping at the
-//     first rejection n ("改进的拒绝采样");
-//   * exactly one draw: from max(0, q_n - p_n) after a rejection, or the bonus
-//     token from q_gamma when all gamma were accepted. The draw re-reads that
-//     one row pair (fresh in L2) with the CTA-wide inverse CDF of draw.cuh.
+// thread ever waits for another CTA): acceptance left to right,
+// u_k < min(1, q(x_k)/p(x_k)), stopping at the first rejection n
+// ("改进的拒绝采样"), the accepted prefix, and n. The draw kernel then makes
+// each sequence's one draw: from max(0, q_n - p_n) after a rejection, or the
+// bonus token from q_gamma when all gamma were accepted, with the CTA-wide
+// inverse CDF of draw.cuh over that one row pair. Five 256-thread CTAs run
+// per SM.
 //
 // Thresholds (top-k, top-p). While streaming, each thread stores in its own
-// shared-memory slots the logits above (reference - (kWin + 1) octaves); they
-// form an upper set in key order that holds every logit whose mass is within
-// 2^-kWin of the largest. tau is the largest key whose weight from the top (a
+// shared-memory slots the logits above (reference - (kWin + 1) octaves) (fp32:
+// the keys; bf16: the 32-bit word of each adjacent pair with a logit above);
+// they form an upper set in key order that holds every logit whose mass is
+// within 2^-kWin of the largest. A bf16 row whose slots overflow is stored
+// again from L2 with the cut of its finished maximum. tau is the largest key whose weight from the top (a
 // count for top-k, the fixed-point mass * 2^40 for top-p: exact integers, so
 // independent of summation order) reaches the target. bf16 rows count the
 // stored keys per distinct bf16 value (a histogram over the ordinals of the
@@ -51,7 +53,7 @@ constexpr int NW = NT / 32;
 constexpr int kMaxRows = 2 * 255 + 1;  // rows per sequence (verification, gamma <= 255)
 constexpr int kU = 4;                  // 16-byte vectors in flight per thread
 constexpr int kWin = 13;               // stored keys: within 2^-kWin of the row max (plus one octave)
-constexpr int kSlotBytes = 128;        // key slots per thread, in bytes
+constexpr int kSlotBytes = 96;         // key slots per thread, in bytes (five CTAs per SM fit)
 constexpr int kSel = 256;              // keys compared exactly inside the crossing bin
 constexpr int kOrd = 2048;             // bf16 ordinal histogram: bins
 constexpr uint32_t kPrefetchBytes = 65536;  // next units up to this size are prefetched into L2
@@ -1017,7 +1019,7 @@ SV_DEV void prefetch_l2(const E* row, int i0, int i1) {
 // --- the kernel -----------------------------------------------------------------
 
 template <typename E, bool XF>
-__global__ void __launch_bounds__(NT, 4) row_kernel(const __grid_constant__ RowParams p) {
+__global__ void __launch_bounds__(NT, 5) row_kernel(const __grid_constant__ RowParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Shared& s = *reinterpret_cast<Shared*>(smem_raw);
     const int tid = threadIdx.x;
