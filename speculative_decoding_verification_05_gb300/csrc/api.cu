@@ -174,7 +174,7 @@ spec_status launch_argmax_checked(sv::ArgmaxParams& p, int dtype, void* ws, cons
     p.cnt = at<unsigned long long>(ws, w.cnt64);
     if (spec_status c = clear(ws, w.cnt64, w.arg_end, st)) return c;
     const long long total = (long long)p.B * p.rows_per_b * p.V;
-    long long grid = std::min<long long>((long long)device_sms() * 4, (total + 8191) / 8192);
+    long long grid = std::min<long long>((long long)device_sms() * sv::argmax_ctas_per_sm(dtype), (total + 8191) / 8192);
     if (grid < 1) grid = 1;
     long long chunk = (total + grid - 1) / grid;
     chunk = (chunk + 63) & ~63LL;

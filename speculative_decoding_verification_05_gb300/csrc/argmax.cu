@@ -14,8 +14,9 @@
 // into equal contiguous chunks, one per CTA, so every SM streams the same
 // number of bytes whatever B, N or V are. Each row segment's argmax (lowest
 // index on ties) is folded into a packed 64-bit word (key << 32 | ~index) with
-// atomicMax; the CTA that completes the last element of a sequence (element
-// counter, no waiting) resolves that sequence and clears its workspace.
+// one atomicMax per warp and segment (no CTA barrier between segments); the
+// CTA that completes the last element of a sequence (element counter, no
+// waiting) resolves that sequence and clears its workspace.
 
 #include "common.cuh"
 
@@ -57,8 +58,6 @@ SV_DEV Best warp_best(Best b) {
 }
 
 struct SharedA {
-    Best red[NW];
-    int bad_red[NW];
     int am[kMaxN];
     int bad[kMaxN];
     int tok[kMaxN];
@@ -89,11 +88,11 @@ SV_DEV float vec_max(const uint4& v, bf16_t) {
 }
 
 template <typename E>
-SV_DEV void segment(const ArgmaxParams& p, SharedA& s, long long r, int i0, int i1) {
+SV_DEV void segment(const ArgmaxParams& p, long long r, int i0, int i1) {
     using T = VecTraits<E>;
     constexpr int es = sizeof(E);
     constexpr int VE = T::kN;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x, lane = tid & 31;
     const E* row = reinterpret_cast<const E*>(p.logits) + r * (long long)p.V;
     Best best{-INFINITY, -1};
     bool bad = false;
@@ -107,7 +106,7 @@ SV_DEV void segment(const ArgmaxParams& p, SharedA& s, long long r, int i0, int 
     const int base = i0 + head;
     const int nb = (i1 - base) / VE;
     const uint4* vp = reinterpret_cast<const uint4*>(row + base);
-    constexpr int U = 4;
+    constexpr int U = 8;  // 16-byte vectors in flight per thread
     for (int j = tid; j < nb; j += NT * U) {
         uint4 v[U];
 #pragma unroll
@@ -139,28 +138,18 @@ SV_DEV void segment(const ArgmaxParams& p, SharedA& s, long long r, int i0, int 
         bad |= !(x < INFINITY);
         take(best, x, t);
     }
+    // each warp folds its best into the row's word: no CTA barrier, so the
+    // warps run on into the next segment independently
     best = warp_best(best);
     const int wbad = __any_sync(0xFFFFFFFFu, bad);
     if (lane == 0) {
-        s.red[warp] = best;
-        s.bad_red[warp] = wbad;
-    }
-    __syncthreads();
-    if (tid == 0) {
-        Best b = s.red[0];
-        int anybad = s.bad_red[0];
-        for (int w = 1; w < NW; ++w) {
-            b = better(b, s.red[w]);
-            anybad |= s.bad_red[w];
-        }
-        if (b.i >= 0) {
+        if (best.i >= 0) {
             const unsigned long long packed =
-                ((unsigned long long)f32_key(b.v) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)b.i);
+                ((unsigned long long)f32_key(best.v) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)best.i);
             atomicMax(&p.rowbest[r], packed);
         }
-        if (anybad) atomicOr(&p.rowbad[r], 1u);
+        if (wbad) atomicOr(&p.rowbad[r], 1u);
     }
-    __syncthreads();
 }
 
 // Resolve sequence b from the per-row argmaxes; the whole CTA takes part.
@@ -290,10 +279,11 @@ __global__ void __launch_bounds__(NT) argmax_kernel(const __grid_constant__ Argm
         const long long r = e / p.V;
         const int i0 = (int)(e - r * p.V);
         const int i1 = (int)min((long long)p.V, i0 + (e1 - e));
-        segment<E>(p, s, r, i0, i1);
+        segment<E>(p, r, i0, i1);
         e += i1 - i0;
     }
-    if (threadIdx.x == 0) __threadfence();  // order this CTA's atomicMax before its arrivals
+    if ((threadIdx.x & 31) == 0) __threadfence();  // order every warp's atomicMax before the arrivals
+    __syncthreads();
     const long long bfirst = e0 / per_b, blast = (e1 - 1) / per_b;
     for (long long b = bfirst; b <= blast; ++b) {
         if (threadIdx.x == 0) {
@@ -314,6 +304,20 @@ __global__ void __launch_bounds__(NT) argmax_kernel(const __grid_constant__ Argm
 }
 
 }  // namespace
+
+int argmax_ctas_per_sm(int dtype) {
+    static const int f32 = [] {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, argmax_kernel<float>, NT, 0) != cudaSuccess || n < 1) n = 1;
+        return n;
+    }();
+    static const int b16 = [] {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, argmax_kernel<bf16_t>, NT, 0) != cudaSuccess || n < 1) n = 1;
+        return n;
+    }();
+    return dtype == 0 ? f32 : b16;
+}
 
 cudaError_t launch_argmax(const ArgmaxParams& p, int dtype, int grid, cudaStream_t stream) {
     if (dtype == 0)

@@ -347,6 +347,8 @@ struct MentorParams {
 cudaError_t launch_rows(const RowParams& p, int dtype, int sms, cudaStream_t stream);
 // The one draw of every sequence the row kernel resolved (verification).
 cudaError_t launch_draws(const RowParams& p, int dtype, int sms, cudaStream_t stream);
+// Resident argmax CTAs per SM (occupancy of the kernel as built).
+int argmax_ctas_per_sm(int dtype);
 cudaError_t launch_argmax(const ArgmaxParams& p, int dtype, int grid, cudaStream_t stream);
 // Position kernel on `grid` persistent CTAs, then the per-sequence resolve.
 cudaError_t launch_mentor(const MentorParams& p, int grid, int resolve_grid, cudaStream_t stream);
