@@ -68,7 +68,6 @@ def test_mentor_12_steps_in_one_call():
     assert ((r["alpha"] > 0) & (r["alpha"] < 1)).any(), "no sampled position reached the solver"
 
 
-
 def test_tree_4_steps_in_one_call():
     c = workloads.CONFIGS["tree"]
     B = c["B"] * 4
