@@ -73,6 +73,29 @@ def dist_env():
     return ws, rank, local
 
 
+def shard_offset(rank, batch):
+    """Philox row base of a rank's sequences: rank r verifies global sequences
+    [r * batch, (r + 1) * batch), so every random number is the one a single
+    device verifying the whole job would draw for that sequence."""
+    return rank * batch
+
+
+def max_over_ranks(ms, device):
+    """The slowest rank's time (the job is as fast as its slowest replica)."""
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world, positions_per_step, steps, total_ms):
+    """Whole-job throughput: every rank's positions over the slowest rank's time."""
+    return world * positions_per_step * steps / (total_ms / 1e3)
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -140,7 +163,7 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(self.rows)}
 
 
-def make_inputs(name, steps_stacked, temperature, device, seed=2024, lenience=1.0):
+def make_inputs(name, steps_stacked, temperature, device, seed=2024, lenience=1.0, rank=0):
     """Synthetic inputs of a workload on the device (generator: workloads.py)."""
     import speculative_decoding_verification_05_gb300 as sv
 
@@ -166,8 +189,10 @@ def make_inputs(name, steps_stacked, temperature, device, seed=2024, lenience=1.
     B = zt.shape[0]
     top_p = c.get("top_p", 1.0)
     # drafts: the library's own sampler on the transformed draft distribution
-    drafts = sv.sample(zd, T, top_p, 0, seed=seed, offset=0, purpose=sv.PURPOSE_DRAFT)["tokens"]
+    offset = shard_offset(rank, B)
+    drafts = sv.sample(zd, T, top_p, 0, seed=seed, offset=offset, purpose=sv.PURPOSE_DRAFT)["tokens"]
     return dict(kind=c["kind"], zt=zt, zd=zd, drafts=drafts, B=B, gamma=c["gamma"], V=c["V"], T=T, lenience=lenience,
+                offset=offset,
                 top_p=top_p, kl_bound=c.get("kl_bound", 0.0), iters=c.get("iters", 30),
                 esize=zt.element_size())
 
@@ -183,8 +208,10 @@ def run_step(inp):
     if inp["kind"] == "tree":
         return sv.verify_tree(inp["z"], inp["tok"], inp["par"], inp["dep"], inp["max_depth"])
     if inp["kind"] == "mentor":
-        return sv.verify_mentor(inp["zt"], inp["zd"], inp["drafts"], inp["T"], inp["kl_bound"], inp["iters"])
-    return sv.verify(inp["zt"], inp["zd"], inp["drafts"], inp["T"], inp["top_p"], 0, 0, 0, lenience=inp["lenience"])
+        return sv.verify_mentor(inp["zt"], inp["zd"], inp["drafts"], inp["T"], inp["kl_bound"], inp["iters"],
+                                0, inp["offset"])
+    return sv.verify(inp["zt"], inp["zd"], inp["drafts"], inp["T"], inp["top_p"], 0, 0, inp["offset"],
+                     lenience=inp["lenience"])
 
 
 def run_step_host(inp, host):
@@ -201,8 +228,9 @@ def run_step_host(inp, host):
     if inp["kind"] == "tree":
         return sv.verify_tree(host["z"], host["tok"], host["par"], host["dep"], inp["max_depth"])
     if inp["kind"] == "mentor":
-        return sv.verify_mentor(host["zt"], host["zd"], host["drafts"], inp["T"], inp["kl_bound"], inp["iters"])
-    return sv.verify(host["zt"], host["zd"], host["drafts"], inp["T"], inp["top_p"], 0, 0, 0,
+        return sv.verify_mentor(host["zt"], host["zd"], host["drafts"], inp["T"], inp["kl_bound"], inp["iters"],
+                                0, inp["offset"])
+    return sv.verify(host["zt"], host["zd"], host["drafts"], inp["T"], inp["top_p"], 0, 0, inp["offset"],
                      lenience=inp["lenience"])
 
 
@@ -311,9 +339,10 @@ def reference_arm(args):
         return 0
     cfg, _, temp = WORKLOADS[args.workload]
     lv = LENIENCE.get(args.workload, 1.0)
+    budget = args.ref_budget if args.ref_budget > 0 else max(2.0, 60.0 / max(1, args.steps))
     for _ in range(args.warmup):
-        cpu_baseline(cfg, temp, budget_s=1.0, lenience=lv, op=OPS.get(args.workload, "verify"))
-    vals = [cpu_baseline(cfg, temp, budget_s=max(2.0, 60.0 / max(1, args.steps)), lenience=lv,
+        cpu_baseline(cfg, temp, budget_s=min(1.0, budget), lenience=lv, op=OPS.get(args.workload, "verify"))
+    vals = [cpu_baseline(cfg, temp, budget_s=budget, lenience=lv,
                          op=OPS.get(args.workload, "verify"))
             for _ in range(args.steps)]
     v = statistics.median(x["value"] for x in vals)
@@ -337,6 +366,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--stack", type=int, default=0, help="stacked steps per call (default: the workload's)")
+    ap.add_argument("--ref-budget", type=float, default=0.0,
+                    help="reference arm: seconds of oracle work per step (default: about 60 s over all steps)")
     args = ap.parse_args()
     if args.impl == "reference":
         return reference_arm(args)
@@ -355,7 +386,8 @@ def main():
     cfg, stacked, temp = WORKLOADS[args.workload]
     if args.stack > 0:
         stacked = args.stack
-    inp = make_inputs(cfg, stacked, temp, device, seed=2024 + rank, lenience=LENIENCE.get(args.workload, 1.0))
+    inp = make_inputs(cfg, stacked, temp, device, seed=2024 + rank, lenience=LENIENCE.get(args.workload, 1.0),
+                      rank=rank)
     inp["op"] = OPS.get(args.workload, "verify")
     nbytes, npos = algorithmic(inp)
     stream = torch.cuda.current_stream(device)
@@ -390,14 +422,9 @@ def main():
             run_step(inp)
             torch.cuda.synchronize(device)
     per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = sum(per_launch_ms)
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(per_launch_ms), device)
     ms_per_step = total_ms / args.steps
-    value = ws * npos * args.steps / (total_ms / 1e3)
+    value = job_value(ws, npos, args.steps, total_ms)
 
     # acceptance statistics of one step (a property of the synthetic inputs)
     out = run_step(inp)
@@ -420,7 +447,7 @@ def main():
         t0 = time.perf_counter()
         for _ in range(n_e2e):
             r = run_step_host(inp, host)
-        dt = time.perf_counter() - t0
+        dt = max_over_ranks((time.perf_counter() - t0) * 1e3, device) / 1e3
         d2h = sum(v.numel() * v.element_size() for v in r.values() if isinstance(v, torch.Tensor))
         e2e = {"value": ws * npos * n_e2e / dt, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "steps": n_e2e}
