@@ -170,19 +170,6 @@ SV_DEV int block_draw(DrawShared& ds, const E* rt, const E* rd, int V, float u, 
     return tok;
 }
 
-// Asks L2 to fetch the 16-byte-aligned interior of [p, p + bytes) (a hint:
-// nothing moves into the SM). The sequence resolve calls it for the rows its
-// draw reads as soon as it knows them.
-SV_DEV void prefetch_span_l2(const void* p, size_t bytes) {
-    uintptr_t a = ((uintptr_t)p + 15) & ~(uintptr_t)15;
-    const uintptr_t e = ((uintptr_t)p + bytes) & ~(uintptr_t)15;
-    while (e > a) {
-        const uint32_t n = (uint32_t)(e - a < (1u << 20) ? e - a : (1u << 20));
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(n) : "memory");
-        a += n;
-    }
-}
-
 // exp2((z - m) log2e / T) for a kept logit (z >= thr), times `scale`; 0 otherwise.
 struct KeptExp {
     float thr, c2, mc, scale;

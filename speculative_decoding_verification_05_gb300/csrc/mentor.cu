@@ -49,12 +49,10 @@ struct SharedM {
     uint32_t dstart[256];
     uint32_t gofs[256];
     double dred[NW];
-    float fred[NW];
     float wsum[5][NW];           // solve: per-warp chunk totals
     float woff[5][NW];           //        and chunk offsets
     int ibuf[NW];
     int bi[8];
-    float bf[8];
     double bd[8];
     DrawShared draw;
 };
