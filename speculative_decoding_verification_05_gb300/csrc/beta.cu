@@ -47,7 +47,37 @@ __global__ void __launch_bounds__(BT) beta_kernel(const __grid_constant__ RowPar
         const E* rt = tgt + ((size_t)b * G1 + k) * V;
         const E* rd = dft + ((size_t)b * G + k) * V;
         float acc = 0.f;
-        if (!bad) {
+        constexpr int VE = 16 / (int)sizeof(E);
+        constexpr int U = 4;  // 16-byte vectors of each row in flight per thread
+        const bool vec = (((uintptr_t)rt | (uintptr_t)rd) & 15) == 0;
+        if (!bad && vec) {
+            // both rows start on 16 bytes: raw vectors, U of each in flight
+            const int nb = V / VE;
+            const uint4* vt = reinterpret_cast<const uint4*>(rt);
+            const uint4* vd = reinterpret_cast<const uint4*>(rd);
+            for (int j = tid; j < nb; j += BT * U) {
+                uint4 a[U], c[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    if (j + u * BT < nb) {
+                        a[u] = ld_stream_v4(vt + j + u * BT);
+                        c[u] = ld_stream_v4(vd + j + u * BT);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    if (j + u * BT < nb) {
+                        float xt[VE], xd[VE];
+                        VecTraits<E>::unpack(a[u], xt);
+                        VecTraits<E>::unpack(c[u], xd);
+#pragma unroll
+                        for (int e = 0; e < VE; ++e) acc += fminf(qf(xt[e]), pf(xd[e]));
+                    }
+                }
+            }
+            for (int i = nb * VE + tid; i < V; i += BT)
+                acc += fminf(qf(VecTraits<E>::load1(rt + i)), pf(VecTraits<E>::load1(rd + i)));
+        } else if (!bad) {
             for (int i0 = tid * PER; i0 < V; i0 += BT * PER) {
                 float xt[PER], xd[PER];
                 draw_load<E>(rt, i0, V, xt);
