@@ -24,6 +24,11 @@ namespace sv {
 constexpr int kDrawNT = 256;
 constexpr int kDrawNW = kDrawNT / 32;
 constexpr int kDrawMaxRounds = 128;  // covers V <= SPEC_MAX_V for every element size
+// Vectors per row, thread and round in the kernels that only draw: four for
+// fp32 rows (long rows, fewer rounds), two for bf16 (shorter rows, fewer
+// registers). The verification draw and the mentor resolve use the same.
+template <typename E>
+constexpr int draw_vec() { return sizeof(E) == 4 ? 4 : 2; }
 
 struct DrawShared {
     float wt[kDrawMaxRounds][kDrawNW];  // per-round, per-warp totals
@@ -33,19 +38,19 @@ struct DrawShared {
     int token;
 };
 
-// Elements per thread per round (two 16-byte vectors).
-template <typename E>
-constexpr int draw_per() { return 2 * (16 / (int)sizeof(E)); }
+// Elements per thread per round (kVec 16-byte vectors).
+template <typename E, int kVec = 2>
+constexpr int draw_per() { return kVec * (16 / (int)sizeof(E)); }
 
 // Loads the PER logits of (row, i0 .. i0 + PER) as fp32 (-inf beyond V).
-template <typename E>
-SV_DEV void draw_load(const E* row, int i0, int V, float (&x)[draw_per<E>()]) {
-    constexpr int PER = draw_per<E>();
+template <typename E, int kVec = 2>
+SV_DEV void draw_load(const E* row, int i0, int V, float (&x)[draw_per<E, kVec>()]) {
+    constexpr int PER = draw_per<E, kVec>();
     constexpr int VE = 16 / (int)sizeof(E);
     const uintptr_t a = (uintptr_t)(row + i0);
     if (i0 + PER <= V && (a & 15) == 0) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < kVec; ++h) {
             const uint4 r = __ldg(reinterpret_cast<const uint4*>(row + i0) + h);
             float y[VE];
             VecTraits<E>::unpack(r, y);
@@ -64,17 +69,20 @@ SV_DEV void draw_load(const E* row, int i0, int V, float (&x)[draw_per<E>()]) {
 // All threads of the CTA must call it; a CTA wider than kDrawNT threads works
 // with its first kDrawNT threads (the others only join the barriers), so the
 // summation order and the result do not depend on the caller's CTA size.
-template <typename E, typename WF>
+// kVec: 16-byte vectors of each row per thread and round. 4 (the kernels that
+// only draw) keeps more loads in flight; 2 (draws inside the streaming
+// kernel) needs fewer registers. Equal kVec gives bit-identical results.
+template <typename E, typename WF, int kVec = 2>
 SV_DEV int block_draw(DrawShared& ds, const E* rt, const E* rd, int V, float u, WF wf, float* W_out) {
-    constexpr int PER = draw_per<E>();
+    constexpr int PER = draw_per<E, kVec>();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const bool act = tid < kDrawNT;
     const int rounds = (V + kDrawNT * PER - 1) / (kDrawNT * PER);
     auto thread_sum = [&](int r, float (&w)[PER]) {
         const int i0 = r * kDrawNT * PER + tid * PER;
         float xt[PER], xd[PER];
-        draw_load<E>(rt, i0, V, xt);
-        if (rd) draw_load<E>(rd, i0, V, xd);
+        draw_load<E, kVec>(rt, i0, V, xt);
+        if (rd) draw_load<E, kVec>(rd, i0, V, xd);
         float acc = 0.f;
 #pragma unroll
         for (int e = 0; e < PER; ++e) {
@@ -85,8 +93,37 @@ SV_DEV int block_draw(DrawShared& ds, const E* rt, const E* rd, int V, float u, 
     };
     // pass 1: per-round, per-warp totals
     for (int r = 0; act && r < rounds; ++r) {
-        float w[PER];
-        float wsum = thread_sum(r, w);
+        float wsum;
+        if constexpr (kVec == 2) {
+            float w[PER];
+            wsum = thread_sum(r, w);
+        } else {
+            // as thread_sum (same elements, same order) from the raw vectors,
+            // all kVec vectors of both rows in flight, the weights not kept
+            constexpr int VE = 16 / (int)sizeof(E);
+            const int i0 = r * kDrawNT * PER + tid * PER;
+            const uintptr_t at = (uintptr_t)(rt + i0), ad = rd ? (uintptr_t)(rd + i0) : 0;
+            if (i0 + PER <= V && ((at | ad) & 15) == 0) {
+                uint4 vt[kVec], vd[kVec];
+#pragma unroll
+                for (int h = 0; h < kVec; ++h) {
+                    vt[h] = __ldg(reinterpret_cast<const uint4*>(rt + i0) + h);
+                    if (rd) vd[h] = __ldg(reinterpret_cast<const uint4*>(rd + i0) + h);
+                }
+                wsum = 0.f;
+#pragma unroll
+                for (int h = 0; h < kVec; ++h) {
+                    float yt[VE], yd[VE];
+                    VecTraits<E>::unpack(vt[h], yt);
+                    if (rd) VecTraits<E>::unpack(vd[h], yd);
+#pragma unroll
+                    for (int e = 0; e < VE; ++e) wsum += wf(yt[e], rd ? yd[e] : -INFINITY);
+                }
+            } else {
+                float w[PER];
+                wsum = thread_sum(r, w);
+            }
+        }
         // butterfly: every lane ends with the same warp total, in a fixed order
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) wsum += __shfl_xor_sync(0xFFFFFFFFu, wsum, o);
@@ -195,23 +232,24 @@ SV_DEV bool accept_test(float u, float q, float p) {
 
 // Inverse-CDF draw from the (transformed) row's probabilities q (sampling and
 // the bonus token).
-template <typename E>
+template <typename E, int kVec = 2>
 SV_DEV int draw_q(DrawShared& ds, const E* row, int V, const RowRec& r, float c2, float u) {
     const KeptExp q{r.thr, c2, r.m * c2, 1.f};
     float W;
-    return block_draw<E>(ds, row, (const E*)nullptr, V, u, [&](float zt, float) { return q(zt); }, &W);
+    auto wq = [&](float zt, float) { return q(zt); };
+    return block_draw<E, decltype(wq), kVec>(ds, row, (const E*)nullptr, V, u, wq, &W);
 }
 
 // Residual draw x ~ max(0, q - l p) over a target/draft row pair (l = 1: the
 // exact residual); from q when the residual vanishes (q = l p to rounding).
-template <typename E>
+template <typename E, int kVec = 2>
 SV_DEV int draw_residual(DrawShared& ds, const E* rt, const E* rd, int V, const RowRec& t, const RowRec& d,
                          float c2, float u, float l = 1.f) {
     const ResidualW w = residual_weight(t, d, c2, l);
     float W;
-    const int tok = block_draw<E>(ds, rt, rd, V, u, w, &W);
+    const int tok = block_draw<E, ResidualW, kVec>(ds, rt, rd, V, u, w, &W);
     if (W > 0.f) return tok;
-    return draw_q<E>(ds, rt, V, t, c2, u);
+    return draw_q<E, kVec>(ds, rt, V, t, c2, u);
 }
 
 SV_DEV RowRec load_rec(const RowRec* src) {

@@ -641,19 +641,19 @@ __global__ void __launch_bounds__(kDrawNT) mentor_resolve_kernel(const __grid_co
             const RowRec t = load_rec(rb + n);
             const E* rt = tgt + ((size_t)b * G1 + n) * V;
             if (n == G) {
-                tok = draw_q<E>(ds, rt, V, t, c2, u2);
+                tok = draw_q<E, draw_vec<E>()>(ds, rt, V, t, c2, u2);
             } else {
                 const RowRec d = load_rec(rb + G1 + n);
                 const E* rd = dft + ((size_t)b * G + n) * V;
                 if (st == kPosRejected) {
-                    tok = draw_residual<E>(ds, rt, rd, V, t, d, c2, u2);
+                    tok = draw_residual<E, draw_vec<E>()>(ds, rt, rd, V, t, d, c2, u2);
                 } else {
                     const float beta = __ldcg(p.pos_beta + (size_t)b * G + n);
                     const ResidualW w{KeptExp{t.thr, c2, t.m * c2, (1.f / t.S) * (1.f / beta)},
                                       KeptExp{d.thr, c2, d.m * c2, 1.f / d.S}};
                     float W;
-                    tok = block_draw<E>(ds, rt, rd, V, u2, w, &W);
-                    if (!(W > 0.f)) tok = draw_q<E>(ds, rt, V, t, c2, u2);
+                    tok = block_draw<E, ResidualW, draw_vec<E>()>(ds, rt, rd, V, u2, w, &W);
+                    if (!(W > 0.f)) tok = draw_q<E, draw_vec<E>()>(ds, rt, V, t, c2, u2);
                 }
             }
         }

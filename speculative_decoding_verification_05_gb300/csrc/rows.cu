@@ -971,7 +971,7 @@ __device__ __noinline__ void resolve_sequence(Shared& s, const RowParams& p, int
 // as every other draw). Persistent CTAs take sequences from a counter; many
 // sequences are drawn at once, so the rounds' memory latency overlaps.
 template <typename E>
-__global__ void __launch_bounds__(NT, 6) draw_kernel(const __grid_constant__ RowParams p) {
+__global__ void __launch_bounds__(NT, sizeof(E) == 4 ? 4 : 6) draw_kernel(const __grid_constant__ RowParams p) {
     __shared__ DrawShared ds;
     __shared__ RowRec rec[2];
     __shared__ int job;
@@ -992,10 +992,10 @@ __global__ void __launch_bounds__(NT, 6) draw_kernel(const __grid_constant__ Row
             const E* rt = row_ref<E>(p, b, n).ptr;
             int tok;
             if (n < G)
-                tok = draw_residual<E>(ds, rt, row_ref<E>(p, b, G + 1 + n).ptr, p.V, rec[0], rec[1], p.c2, u2,
-                                       p.lenience);
+                tok = draw_residual<E, draw_vec<E>()>(ds, rt, row_ref<E>(p, b, G + 1 + n).ptr, p.V, rec[0], rec[1],
+                                                 p.c2, u2, p.lenience);
             else
-                tok = draw_q<E>(ds, rt, p.V, rec[0], p.c2, u2);
+                tok = draw_q<E, draw_vec<E>()>(ds, rt, p.V, rec[0], p.c2, u2);
             if (tid == 0) {
                 p.next_token[b] = tok;
                 p.tokens[(size_t)b * (G + 1) + n] = tok;
