@@ -106,7 +106,7 @@ SV_DEV void segment(const ArgmaxParams& p, long long r, int i0, int i1) {
     const int base = i0 + head;
     const int nb = (i1 - base) / VE;
     const uint4* vp = reinterpret_cast<const uint4*>(row + base);
-    constexpr int U = 8;  // 16-byte vectors in flight per thread
+    constexpr int U = 4;  // 16-byte vectors in flight per thread
     for (int j = tid; j < nb; j += NT * U) {
         uint4 v[U];
 #pragma unroll
