@@ -27,8 +27,10 @@
 // shared-memory slots the logits above (reference - (kWin + 1) octaves) (fp32:
 // the keys; bf16: the 32-bit word of each adjacent pair with a logit above);
 // they form an upper set in key order that holds every logit whose mass is
-// within 2^-kWin of the largest. A bf16 row whose slots overflow is stored
-// again from L2 with the cut of its finished maximum. tau is the largest key whose weight from the top (a
+// within 2^-kWin of the largest (bf16 rows: kWinB while streaming). A bf16
+// row whose stored keys do not decide the threshold, or whose slots
+// overflow, is stored again from the row with the cut of its finished
+// maximum minus kWinWide + 1 octaves;// again from L2 with the cut of its finished maximum. tau is the largest key whose weight from the top (a
 // count for top-k, the fixed-point mass * 2^40 for top-p: exact integers, so
 // independent of summation order) reaches the target. bf16 rows count the
 // stored keys per distinct bf16 value (a histogram over the ordinals of the
@@ -53,6 +55,8 @@ constexpr int NW = NT / 32;
 constexpr int kMaxRows = 2 * 255 + 1;  // rows per sequence (verification, gamma <= 255)
 constexpr int kU = 4;                  // 16-byte vectors in flight per thread
 constexpr int kWin = 13;               // stored keys: within 2^-kWin of the row max (plus one octave)
+constexpr int kWinB = 11;              // bf16 rows while streaming (a second, wider pass if needed)
+constexpr int kWinWide = 15;           // bf16 second pass: the ordinal histogram's reach
 constexpr int kSlotBytes = 96;         // key slots per thread, in bytes (five CTAs per SM fit)
 constexpr int kSel = 256;              // keys compared exactly inside the crossing bin
 constexpr int kOrd = 2048;             // bf16 ordinal histogram: bins
@@ -836,22 +840,46 @@ __device__ __noinline__ bool bf16_threshold(Shared& s, const RowParams& p, float
     return ok;
 }
 
-// Stores the pairs of a bf16 row again, with the cut of the finished row (its
-// maximum minus the window), after a thread's slots overflowed under the
-// provisional cut of the streaming pass. The row was just read, so this pass
-// mostly hits L2. Every thread must call it.
+// bf16 rows: stores the candidate pairs of the row again, with a cut below
+// its finished maximum (a second, wider collection when the keys stored
+// while streaming do not decide the threshold or overflowed). Four 16-byte
+// vectors in flight per thread; the 32-bit word of each adjacent pair with a
+// logit above the cut goes to the thread's slots. Every thread must call it;
+// it sets s.hn, s.cut and s.ovf.
 SV_DEV void recollect_bf16(Shared& s, const bf16_t* row, int V, float cut) {
     const int tid = threadIdx.x;
     const unsigned short* rs = reinterpret_cast<const unsigned short*>(row);
-    __syncthreads();  // every thread has read the overflow flag
+    __syncthreads();  // every thread is past its last use of the slots and the flag
     if (tid == 0) {
         s.ovf = 0;
         s.cut = cut;
     }
     PairCollect col{reinterpret_cast<uint32_t*>(s.u.slots) + tid, cut, 0};
-    for (int i = 2 * tid; i < V; i += 2 * NT) {
-        const uint32_t lo = __ldg(rs + i), hi = i + 1 < V ? (uint32_t)__ldg(rs + i + 1) : 0xFF80u;
-        col.safe(__uint_as_float(lo << 16), __uint_as_float(hi << 16), lo | (hi << 16));
+    const int head = min(V, (int)(((16 - ((uintptr_t)row & 15)) & 15) / 2));
+    if (tid < head) {
+        const uint32_t raw = __ldg(rs + tid);
+        col.safe(__uint_as_float(raw << 16), -INFINITY, raw | 0xFF800000u);
+    }
+    const int nb = (V - head) / 8;
+    const uint4* vp = reinterpret_cast<const uint4*>(row + head);
+    for (int j = tid; j < nb; j += NT * kU) {
+        uint4 v[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+            if (j + u * NT < nb) v[u] = __ldcg(vp + j + u * NT);
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            if (j + u * NT < nb) {
+                const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) col.safe(bf_lo(w[q]), bf_hi(w[q]), w[q]);
+            }
+        }
+    }
+    const int t = head + nb * 8 + tid;
+    if (t < V) {
+        const uint32_t raw = __ldg(rs + t);
+        col.safe(__uint_as_float(raw << 16), -INFINITY, raw | 0xFF800000u);
     }
     __syncthreads();  // the flag's reset before any thread sets it
     s.hn[tid] = (unsigned short)min(col.hc, PairCollect::kPer);
@@ -869,9 +897,11 @@ __device__ __noinline__ void row_threshold(Shared& s, const RowParams& p, const 
     constexpr int npass = sizeof(E) == 4 ? 4 : 2;
     if constexpr (sizeof(E) == 2) {
         if (use_slots) {
-            if (s.ovf) recollect_bf16(s, row, p.V, m - (float)(kWin + 1) / c2);
-            // the stored pairs hold every value above the cut: when they do
-            // not decide the threshold, only the row itself can
+            // the stored pairs hold every value above the cut; when they do
+            // not decide the threshold, a wider collection from the row, then
+            // the selection over the whole row
+            if (!s.ovf && bf16_threshold(s, p, m, S, thr, sk)) return;
+            recollect_bf16(s, row, p.V, m - (float)(kWinWide + 1) / c2);
             if (!s.ovf && bf16_threshold(s, p, m, S, thr, sk)) return;
         }
     } else if (use_slots && !s.ovf) {
@@ -1026,7 +1056,7 @@ __global__ void __launch_bounds__(NT, 5) row_kernel(const __grid_constant__ RowP
     const int R = p.rows_per_b;
     const int nunits = p.B * R * p.nseg;
     const bool col = XF && p.nseg == 1;
-    const float wc = (float)(kWin + 1) / p.c2;
+    const float wc = (float)((sizeof(E) == 2 ? kWinB : kWin) + 1) / p.c2;
     auto locate = [&](int u, int* b, int* r, int* i0, int* i1) {
         const int rowid = u / p.nseg, seg = u - rowid * p.nseg;
         *b = rowid / R;
