@@ -28,9 +28,9 @@
 // the keys; bf16: the 32-bit word of each adjacent pair with a logit above);
 // they form an upper set in key order that holds every logit whose mass is
 // within 2^-kWin of the largest (bf16 rows: kWinB while streaming). A bf16
-// row whose stored keys do not decide the threshold, or whose slots
-// overflow, is stored again from the row with the cut of its finished
-// maximum minus kWinWide + 1 octaves;// again from L2 with the cut of its finished maximum. tau is the largest key whose weight from the top (a
+// row whose slots overflow is stored again from the row with the same window
+// below its finished maximum; one whose stored keys still do not decide the
+// threshold is stored again with kWinWide + 1 octaves below it;// again from L2 with the cut of its finished maximum. tau is the largest key whose weight from the top (a
 // count for top-k, the fixed-point mass * 2^40 for top-p: exact integers, so
 // independent of summation order) reaches the target. bf16 rows count the
 // stored keys per distinct bf16 value (a histogram over the ordinals of the
@@ -897,10 +897,16 @@ __device__ __noinline__ void row_threshold(Shared& s, const RowParams& p, const 
     constexpr int npass = sizeof(E) == 4 ? 4 : 2;
     if constexpr (sizeof(E) == 2) {
         if (use_slots) {
-            // the stored pairs hold every value above the cut; when they do
-            // not decide the threshold, a wider collection from the row, then
-            // the selection over the whole row
+            // the stored pairs hold every value above the cut. Slots that
+            // overflowed are filled again with the same window below the
+            // finished maximum (tighter than below the reference); a window
+            // that held too little is widened; then the selection over the
+            // whole row
             if (!s.ovf && bf16_threshold(s, p, m, S, thr, sk)) return;
+            if (s.ovf) {
+                recollect_bf16(s, row, p.V, m - (float)(kWinB + 1) / c2);
+                if (!s.ovf && bf16_threshold(s, p, m, S, thr, sk)) return;
+            }
             recollect_bf16(s, row, p.V, m - (float)(kWinWide + 1) / c2);
             if (!s.ovf && bf16_threshold(s, p, m, S, thr, sk)) return;
         }
