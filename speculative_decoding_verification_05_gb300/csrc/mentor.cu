@@ -39,6 +39,8 @@ constexpr int kIPT = 8;          // items per thread per sort tile
 constexpr int kTile = NT * kIPT; // 8192
 constexpr int kCoarse = 32;      // coarse index stride
 
+// Large arrays of the sorting solve (dynamic shared memory, overlaid by the
+// histogram solve's arrays: the two never run at the same time).
 struct SharedM {
     uint32_t wcnt[NW][256];      // per-warp digit counts, then offsets
     uint32_t stk[kTile];         // one tile in digit order (keys, indices)
@@ -48,16 +50,26 @@ struct SharedM {
     uint32_t dtot[256];          // tile: per-digit count, start, global offset
     uint32_t dstart[256];
     uint32_t gofs[256];
+};
+
+// Small per-CTA state (static shared memory).
+struct SmallM {
     double dred[NW];
-    float wsum[5][NW];           // solve: per-warp chunk totals
-    float woff[5][NW];           //        and chunk offsets
+    float wsum[5][NW];           // sorting solve: per-warp chunk totals
+    float woff[5][NW];           //                and chunk offsets
     int ibuf[NW];
     int bi[8];
     double bd[8];
-    DrawShared draw;
+    long long wtot[3][NW];       // histogram solve: block scans
+    long long wall[3];
+    long long tA[3], tB[3];      // totals of the two histograms (q, p, q ln rho)
+    long long base[3], above[3]; // sums below the alpha window, above the beta window
+    long long ltot;              // sum of q ln rho over the row
+    int hflag, ihi, inf, cnt, nA, n, a_b0, a_b1, b_lo, b_hi, ok;
+    double ahi, abeta;
 };
 
-SV_DEV double block_sum_d(SharedM& s, double v) {
+SV_DEV double block_sum_d(SmallM& s, double v) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
@@ -79,12 +91,18 @@ struct Row {
     float lnr0;        // -(m_t - m_d)/T - ln S_t + ln S_d
 };
 
+// q, p and ln(q/p) of one index from its two logits. The rounding of every
+// step is pinned, so that the passes that recompute an index agree bit for bit.
+template <typename E>
+SV_DEV void qpl_of(const Row<E>& r, float zt, float zd, float& q, float& p, float& l) {
+    q = __fmul_rn(ex2(__fmaf_rn(zt, r.c2, -r.mtc)), r.iSt);
+    p = __fmul_rn(ex2(__fmaf_rn(zd, r.c2, -r.mdc)), r.iSd);
+    l = __fmaf_rn(__fsub_rn(zt, zd), r.inv_t, r.lnr0);
+}
+
 template <typename E>
 SV_DEV void qpl(const Row<E>& r, int i, float& q, float& p, float& l) {
-    const float zt = VecTraits<E>::load1(r.rt + i), zd = VecTraits<E>::load1(r.rd + i);
-    q = ex2(fmaf(zt, r.c2, -r.mtc)) * r.iSt;
-    p = ex2(fmaf(zd, r.c2, -r.mdc)) * r.iSd;
-    l = (zt - zd) * r.inv_t + r.lnr0;
+    qpl_of(r, VecTraits<E>::load1(r.rt + i), VecTraits<E>::load1(r.rd + i), q, p, l);
 }
 
 // Stable LSD radix sort of (key, idx) pairs, ascending, four 8-bit digits.
@@ -304,7 +322,7 @@ SV_DEV double kl_at(const Arrays& a, double alpha, double* beta_out) {
 
 // Solves one row pair: alpha (the bisection result) and beta. kl0 > D > 0.
 template <typename E>
-SV_DEV void solve(SharedM& s, float* coarse, const MentorParams& p, const Row<E>& r, uint32_t* k0,
+SV_DEV void solve(SharedM& s, SmallM& t, float* coarse, const MentorParams& p, const Row<E>& r, uint32_t* k0,
                   uint32_t* i0, uint32_t* k1, uint32_t* i1, float* A, double* alpha_out, float* beta_out) {
     const int tid = threadIdx.x;
     const int V = p.V;
@@ -401,11 +419,11 @@ SV_DEV void solve(SharedM& s, float* coarse, const MentorParams& p, const Row<E>
             sp += __shfl_sync(0xFFFFFFFFu, pp, 0);
         }
         if (lane == 0) {
-            s.wsum[0][warp] = cq;
-            s.wsum[1][warp] = cp;
-            s.wsum[2][warp] = cl;
-            s.wsum[3][warp] = sq;
-            s.wsum[4][warp] = sp;
+            t.wsum[0][warp] = cq;
+            t.wsum[1][warp] = cp;
+            t.wsum[2][warp] = cl;
+            t.wsum[3][warp] = sq;
+            t.wsum[4][warp] = sp;
         }
     }
     __syncthreads();
@@ -414,20 +432,20 @@ SV_DEV void solve(SharedM& s, float* coarse, const MentorParams& p, const Row<E>
         float acc = 0.f;
         if (tid < 3) {
             for (int w = 0; w < NW; ++w) {
-                s.woff[tid][w] = acc;
-                acc += s.wsum[tid][w];
+                t.woff[tid][w] = acc;
+                acc += t.wsum[tid][w];
             }
         } else {
             for (int w = NW - 1; w >= 0; --w) {
-                s.woff[tid][w] = acc;
-                acc += s.wsum[tid][w];
+                t.woff[tid][w] = acc;
+                acc += t.wsum[tid][w];
             }
         }
     }
     __syncthreads();
     {
-        const float oq = s.woff[0][warp], op = s.woff[1][warp], ol = s.woff[2][warp];
-        const float xq = s.woff[3][warp], xp = s.woff[4][warp];
+        const float oq = t.woff[0][warp], op = t.woff[1][warp], ol = t.woff[2][warp];
+        const float xq = t.woff[3][warp], xp = t.woff[4][warp];
         for (int j = w0 + lane; j < w1; j += 32) {
             CQ[j] = oq + __ldcg(CQ + j);
             CP[j] = op + __ldcg(CP + j);
@@ -460,15 +478,15 @@ SV_DEV void solve(SharedM& s, float* coarse, const MentorParams& p, const Row<E>
         }
         // smallest feasible interior point (monotone KL): first set bit
         const unsigned bal = __ballot_sync(0xFFFFFFFFu, feas);
-        if ((tid & 31) == 0) s.ibuf[tid >> 5] = bal ? (tid + __ffs(bal) - 1) : 0x7FFFFFFF;
+        if ((tid & 31) == 0) t.ibuf[tid >> 5] = bal ? (tid + __ffs(bal) - 1) : 0x7FFFFFFF;
         __syncthreads();
         if (tid == 0) {
             int f = 0x7FFFFFFF;
-            for (int w = 0; w < NW; ++w) f = min(f, s.ibuf[w]);
-            s.bi[2] = f;
+            for (int w = 0; w < NW; ++w) f = min(f, t.ibuf[w]);
+            t.bi[2] = f;
         }
         __syncthreads();
-        const int f = s.bi[2];
+        const int f = t.bi[2];
         __syncthreads();
         if (f == 0x7FFFFFFF) {
             lo = hi - step;  // only the upper end is feasible
@@ -485,12 +503,521 @@ SV_DEV void solve(SharedM& s, float* coarse, const MentorParams& p, const Row<E>
         if (tid == 0) {
             double bt;
             kl_at(ar, hi, &bt);
-            s.bd[0] = bt;
+            t.bd[0] = bt;
         }
         __syncthreads();
-        *beta_out = (float)s.bd[0];
+        *beta_out = (float)t.bd[0];
         __syncthreads();
     }
+}
+
+// ---------------------------------------------------------------------------
+// Histogram solve: the same bisection without sorting the row.
+//
+// KL(alpha) needs, at alpha, the sums of q, p and q ln rho over {rho < alpha},
+// and beta, where the decreasing function g(t) = sum_{rho >= t} (q/t - p)
+// meets R = sum_{rho < alpha} (p - q/alpha); the indices with rho >= beta are
+// the ones resampled from. alpha <= 1 <= beta always (at alpha = 1 both are
+// 1), so one pass over the row builds two histograms:
+//   * rho < 1: 1024 buckets of rho, width 2^-10, whose edges are the first
+//     ten bisection levels, so the sums below a grid point are exact;
+//   * rho >= 1: 4096 buckets of ln rho, width 1/128 (the last one open).
+// The sums are 64-bit fixed point (q, p in units of 2^-50, q ln rho in
+// 2^-46), so they are exact and independent of the order of the atomics.
+//
+// Round 0 evaluates the first bisection levels (up to 1023 grid points, one
+// thread each, in fp32): beta is placed in its bucket exactly (g is known at
+// every bucket edge), and the indices of that bucket are counted out of the
+// resampled set. That choice is still a feasible redistribution of the
+// rejected mass, so its KL is an upper bound of the true one, above it by at
+// most Q_b d^2/2 (1 + Q_b/Q_U) for a bucket of q-mass Q_b and log-width d,
+// plus the fp32 rounding of the three terms. Grid points whose bounds leave
+// the comparison with D open are settled exactly below; KL falls as alpha
+// grows, so they lie between the last surely infeasible point and the first
+// surely feasible one.
+//
+// The exact evaluations (those points, the remaining bisection levels, and
+// beta of the result) need only the indices whose rho falls in the alpha
+// interval left by round 0 and the beta buckets that interval maps to: a second
+// pass over the row (now in L2) collects them, they are sorted by ln rho in
+// shared memory and summed exactly, and one warp searches the remaining levels
+// 31 points at a time in double precision. Rows whose result lies below 2^-10,
+// whose ambiguous range or windows are too large, or whose terms overflow the
+// fixed point go to the sorting solve.
+// ---------------------------------------------------------------------------
+constexpr int kNA = 1024;             // alpha buckets of rho in [0, 1)
+constexpr int kNB = 4096;             // beta buckets of ln rho in [0, 32) (last one open)
+constexpr float kBScale = 128.f;      // beta buckets per unit of ln rho
+constexpr int kCap = 4096;            // window indices
+constexpr int kMaxAmb = 64;           // grid points left open by round 0
+constexpr int kQE = 50, kLE = 46;     // fixed-point exponents of q, p and of q ln rho
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct HistArrays {
+    long long hA[3][kNA];  // alpha buckets (q, p, q ln rho); then exclusive prefix sums
+    long long hB[3][kNB];  // beta buckets; then inclusive suffix sums
+    float gb[kNB];         // g at the lower edge of every beta bucket
+    short bb[kNA + 1];     // round 0: first beta edge with g <= R per grid point
+};
+struct WinArrays {
+    unsigned long long key[kCap];  // (ordered ln rho) << 32 | index, sorted
+    long long c[3][kCap];          // alpha part: prefix sums; beta part: suffix sums
+    float lw[kCap];                // ln rho
+    float gw[kCap];                // beta part: g at each index's rho
+};
+union SharedH {
+    HistArrays h;
+    WinArrays w;
+};
+
+// x * 2^e truncated toward zero, for |x| * 2^e < 2^62.
+SV_DEV long long to_fix(float x, int e) {
+    const uint32_t u = __float_as_uint(x);
+    const int ex = (int)((u >> 23) & 255u);
+    if (ex == 0) return 0;
+    const long long m = (long long)((u & 0x7FFFFFu) | 0x800000u);
+    const int sh = ex - 150 + e;
+    const long long v = sh >= 0 ? (m << sh) : (sh > -24 ? (m >> -sh) : 0);
+    return (u >> 31) ? -v : v;
+}
+
+SV_DEV float fix_f(long long v, float scale) { return __ll2float_rn(v) * scale; }
+
+SV_DEV int alpha_bucket(float l) {  // l < 0
+    const float rho = ex2(__fmul_rn(l, kLog2e));
+    return min(kNA - 1, (int)__fmul_rn(rho, (float)kNA));
+}
+
+SV_DEV int beta_bucket(float l) {   // l >= 0, possibly +inf
+    return l >= (float)kNB / kBScale ? kNB - 1 : (int)__fmul_rn(l, kBScale);
+}
+
+// Calls f(index, target logit, draft logit) for every index of the row pair,
+// two 16-byte vectors of each row in flight per thread when both rows are
+// 16-byte aligned.
+template <typename E, typename F>
+SV_DEV void for_each_pair(const Row<E>& r, int V, F&& f) {
+    constexpr int kN = VecTraits<E>::kN;
+    const int tid = threadIdx.x;
+    int tail = 0;
+    if (((reinterpret_cast<uintptr_t>(r.rt) | reinterpret_cast<uintptr_t>(r.rd)) & 15u) == 0) {
+        const int nv = V / kN;
+        const uint4* vt = reinterpret_cast<const uint4*>(r.rt);
+        const uint4* vd = reinterpret_cast<const uint4*>(r.rd);
+        for (int v = tid; v < nv; v += 2 * NT) {
+            const bool two = v + NT < nv;
+            const uint4 a0 = __ldg(vt + v), b0 = __ldg(vd + v);
+            const uint4 a1 = two ? __ldg(vt + v + NT) : a0, b1 = two ? __ldg(vd + v + NT) : b0;
+            float x[kN], y[kN];
+            VecTraits<E>::unpack(a0, x);
+            VecTraits<E>::unpack(b0, y);
+#pragma unroll
+            for (int u = 0; u < kN; ++u) f(v * kN + u, x[u], y[u]);
+            if (two) {
+                VecTraits<E>::unpack(a1, x);
+                VecTraits<E>::unpack(b1, y);
+#pragma unroll
+                for (int u = 0; u < kN; ++u) f((v + NT) * kN + u, x[u], y[u]);
+            }
+        }
+        tail = nv * kN;
+    }
+    for (int i = tail + tid; i < V; i += NT) f(i, VecTraits<E>::load1(r.rt + i), VecTraits<E>::load1(r.rd + i));
+}
+
+// Exclusive prefix (in thread order) of three 64-bit values; tot = the totals.
+SV_DEV void block_exscan3(SmallM& t, long long (&v)[3], long long (&tot)[3]) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    long long inc[3] = {v[0], v[1], v[2]};
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            const long long y = __shfl_up_sync(0xFFFFFFFFu, inc[k], o);
+            if (lane >= o) inc[k] += y;
+        }
+    }
+    if (lane == 31) {
+#pragma unroll
+        for (int k = 0; k < 3; ++k) t.wtot[k][warp] = inc[k];
+    }
+    __syncthreads();
+    if (warp == 0) {
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            const long long w0 = t.wtot[k][lane];
+            long long w = w0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const long long y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+                if (lane >= o) w += y;
+            }
+            t.wtot[k][lane] = w - w0;
+            if (lane == 31) t.wall[k] = w;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        v[k] = inc[k] - v[k] + t.wtot[k][warp];
+        tot[k] = t.wall[k];
+    }
+    __syncthreads();
+}
+
+// Pass 1: both histograms of the row pair. hflag bit 0: some index has q > 0
+// and p = 0 (KL(q || p) is infinite); bit 1: some |q ln rho| is too large for
+// the fixed point.
+template <typename E>
+SV_DEV void hist_pass(HistArrays& h, SmallM& t, const Row<E>& r, int V) {
+    const int tid = threadIdx.x;
+    for (int e = tid; e < 3 * kNA; e += NT) (&h.hA[0][0])[e] = 0;
+    for (int e = tid; e < 3 * kNB; e += NT) (&h.hB[0][0])[e] = 0;
+    if (tid == 0) t.hflag = 0;
+    __syncthreads();
+    int fl = 0;
+    for_each_pair<E>(r, V, [&](int, float zt, float zd) {
+        float q, p, l;
+        qpl_of(r, zt, zd, q, p, l);
+        if (!(q > 0.f) && !(p > 0.f)) return;
+        float ql = 0.f;
+        if (q > 0.f) {
+            if (l == INFINITY) {
+                fl |= 1;
+            } else {
+                ql = __fmul_rn(q, l);
+                if (!(fabsf(ql) < 65536.f)) fl |= 2;
+            }
+        }
+        long long* H;
+        int stride;
+        if (l < 0.f) {
+            H = &h.hA[0][alpha_bucket(l)];
+            stride = kNA;
+        } else {
+            H = &h.hB[0][beta_bucket(l)];
+            stride = kNB;
+        }
+        if (q > 0.f) atomicAdd(reinterpret_cast<unsigned long long*>(H), (unsigned long long)to_fix(q, kQE));
+        if (p > 0.f)
+            atomicAdd(reinterpret_cast<unsigned long long*>(H + stride), (unsigned long long)to_fix(p, kQE));
+        if (ql != 0.f && !(fl & 2))
+            atomicAdd(reinterpret_cast<unsigned long long*>(H + 2 * stride), (unsigned long long)to_fix(ql, kLE));
+    });
+    if (fl) atomicOr(&t.hflag, fl);
+    __syncthreads();
+}
+
+// Alpha buckets to exclusive prefix sums, beta buckets to inclusive suffix
+// sums, totals, and g at every beta edge.
+SV_DEV void scan_hist(HistArrays& h, SmallM& t) {
+    const int tid = threadIdx.x;
+    long long v[3], tot[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) v[k] = h.hA[k][tid];
+    block_exscan3(t, v, tot);
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        h.hA[k][tid] = v[k];
+        if (tid == 0) t.tA[k] = tot[k];
+    }
+    // thread tid owns beta buckets [4c, 4c + 4), c = NT - 1 - tid, so that
+    // thread order is descending bucket order
+    const int c0 = (NT - 1 - tid) * 4;
+    long long b[3][4];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        v[k] = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            b[k][u] = h.hB[k][c0 + u];
+            v[k] += b[k][u];
+        }
+    }
+    block_exscan3(t, v, tot);
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+        long long run = v[k];
+#pragma unroll
+        for (int u = 3; u >= 0; --u) {
+            run += b[k][u];
+            h.hB[k][c0 + u] = run;
+        }
+        if (tid == 0) t.tB[k] = tot[k];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int e = c0 + u;
+        h.gb[e] = fix_f(h.hB[0][e], 0x1p-50f) * ex2(-(float)e * (kLog2e / kBScale)) - fix_f(h.hB[1][e], 0x1p-50f);
+    }
+    if (tid == 0) t.ltot = t.tA[2] + t.tB[2];
+    __syncthreads();
+}
+
+// KL(alpha) and beta from the windows, in double precision. +inf when the
+// resampled set would be empty.
+SV_DEV double kl_exact(const WinArrays& w, const SmallM& t, double a, double* beta_out) {
+    const double la = log(a);
+    int lo = 0, hi = t.nA;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if ((double)w.lw[mid] < la) lo = mid + 1; else hi = mid;
+    }
+    const long long QLi = lo ? w.c[0][lo - 1] : t.base[0];
+    const long long PLi = lo ? w.c[1][lo - 1] : t.base[1];
+    const long long LLi = lo ? w.c[2][lo - 1] : t.base[2];
+    const double QL = (double)QLi * 0x1p-50, PL = (double)PLi * 0x1p-50;
+    const double R = PL - QL / a;
+    const float Rf = (float)R;
+    lo = t.nA;
+    hi = t.n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (w.gw[mid] <= Rf) hi = mid; else lo = mid + 1;
+    }
+    const long long QUi = lo < t.n ? w.c[0][lo] : t.above[0];
+    const long long PUi = lo < t.n ? w.c[1][lo] : t.above[1];
+    const long long LUi = lo < t.n ? w.c[2][lo] : t.above[2];
+    if (QUi <= 0) return HUGE_VAL;
+    const double QU = (double)QUi * 0x1p-50, den = R + (double)PUi * 0x1p-50;
+    if (!(den > 0.0)) return HUGE_VAL;
+    const double beta = QU / den;
+    if (beta_out) *beta_out = beta;
+    return la * QL + (double)(t.ltot - LLi - LUi) * 0x1p-46 + log(beta) * QU;
+}
+
+// Rounds 0..: returns false when the row has to go to the sorting solve.
+template <typename E>
+SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<E>& r, double* alpha_out,
+                       float* beta_out) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int V = p.V;
+    const float D = p.kl_bound;
+    const int bits0 = min(10, p.iters), npts = 1 << bits0, stp = kNA >> bits0;
+    const bool rounds = p.iters > bits0;
+    HistArrays& h = sh.h;
+    // round 0
+    if (tid == 0) {
+        t.ihi = npts;
+        t.inf = 0;
+        h.bb[npts] = 0;  // alpha = 1: beta = 1, bucket 0
+    }
+    __syncthreads();
+    const int i = tid + 1;
+    bool maybe = true;
+    if (i < npts) {
+        const int j = i * stp;
+        const float a = (float)j * (1.f / kNA);
+        const long long LLi = h.hA[2][j];
+        const float QL = fix_f(h.hA[0][j], 0x1p-50f), PL = fix_f(h.hA[1][j], 0x1p-50f);
+        const float R = PL - QL / a;
+        int lo = 0, hi = kNB;  // first edge with g <= R (kNB: none)
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (h.gb[mid] <= R) hi = mid; else lo = mid + 1;
+        }
+        const int b = lo;
+        h.bb[i] = (short)b;
+        bool sure = false;
+        if (b < kNB && h.hB[0][b] > 0) {
+            const float QU = fix_f(h.hB[0][b], 0x1p-50f), den = R + fix_f(h.hB[1][b], 0x1p-50f);
+            if (den > 0.f) {
+                const float beta = QU / den;
+                const float LM = fix_f(t.ltot - LLi - h.hB[2][b], 0x1p-46f);
+                const float t1 = logf(a) * QL, t3 = logf(beta) * QU;
+                const float kl = t1 + LM + t3;
+                const float QB = b > 0 ? fix_f(h.hB[0][b - 1] - h.hB[0][b], 0x1p-50f) : 0.f;
+                const float efp = 4e-7f * (fabsf(t1) + fabsf(LM) + fabsf(t3)) + 1e-9f;
+                const float err = QB * (0.5f / (kBScale * kBScale)) * (1.f + QB / QU) * 1.01f + efp;
+                sure = kl + efp <= D;
+                maybe = !(kl - err > D);
+            }
+        }
+        if (sure) atomicMin(&t.ihi, i);
+    }
+    __syncthreads();
+    if (i < t.ihi && !maybe) atomicMax(&t.inf, i);
+    __syncthreads();
+    if (tid == 0) {
+        const int ihi = t.ihi, ilo = t.inf + 1;
+        bool ok = !(t.hflag & 2) && !(rounds && ilo == 1) && ihi - ilo <= kMaxAmb;
+        const int a_b0 = (rounds ? ilo - 1 : ilo) * stp, a_b1 = ihi * stp;
+        const int b_lo = ihi < npts ? max(0, h.bb[ihi] - 2) : 0;
+        const int b_hi = min(kNB - 1, (int)h.bb[rounds ? ilo - 1 : ilo]);
+        t.inf = ilo;
+        t.a_b0 = a_b0;
+        t.a_b1 = a_b1;
+        t.b_lo = b_lo;
+        t.b_hi = b_hi;
+        for (int k = 0; k < 3; ++k) {
+            t.base[k] = a_b0 < kNA ? h.hA[k][a_b0] : t.tA[k];
+            t.above[k] = b_hi + 1 < kNB ? h.hB[k][b_hi + 1] : 0;
+        }
+        t.cnt = 0;
+        t.ok = ok;
+        t.ahi = (double)(ihi * stp) * (1.0 / kNA);
+    }
+    __syncthreads();
+    if (!t.ok) return false;
+    const int ilo = t.inf, ihi = t.ihi;
+    if (!rounds && ilo == ihi && ihi == npts) {  // alpha = 1 (every grid point below is infeasible)
+        *alpha_out = 1.0;
+        *beta_out = 1.f;
+        return true;
+    }
+    // pass 2: the window indices
+    WinArrays& w = sh.w;
+    {
+        const int a_b0 = t.a_b0, a_b1 = t.a_b1, b_lo = t.b_lo, b_hi = t.b_hi;
+        for_each_pair<E>(r, V, [&](int idx, float zt, float zd) {
+            float q, pp, l;
+            qpl_of(r, zt, zd, q, pp, l);
+            if (!(q > 0.f) && !(pp > 0.f)) return;
+            bool sel;
+            if (l < 0.f) {
+                const int j = alpha_bucket(l);
+                sel = j >= a_b0 && j < a_b1;
+            } else {
+                const int b = beta_bucket(l);
+                sel = b >= b_lo && b <= b_hi;
+            }
+            if (sel) {
+                const unsigned s = atomicAdd(reinterpret_cast<unsigned*>(&t.cnt), 1u);
+                if (s < (unsigned)kCap) w.key[s] = ((unsigned long long)f32_key(l) << 32) | (unsigned)idx;
+            }
+        });
+    }
+    __syncthreads();
+    const int n = t.cnt;
+    if (n > kCap) return false;
+    int n2 = 2;
+    while (n2 < n) n2 <<= 1;
+    for (int s = n + tid; s < n2; s += NT) w.key[s] = ~0ull;
+    __syncthreads();
+    for (int k = 2; k <= n2; k <<= 1) {
+        for (int jj = k >> 1; jj > 0; jj >>= 1) {
+            for (int x = tid; x < n2; x += NT) {
+                const int y = x ^ jj;
+                if (y > x) {
+                    const unsigned long long ka = w.key[x], kb = w.key[y];
+                    if ((ka > kb) == ((x & k) == 0)) {
+                        w.key[x] = kb;
+                        w.key[y] = ka;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    // the window's values in sorted order (recomputed exactly as in pass 1)
+    if (tid == 0) {
+        t.n = n;
+        t.nA = n;
+    }
+    __syncthreads();
+    for (int s = tid; s < n; s += NT) {
+        const unsigned long long kv = w.key[s];
+        const int idx = (int)(unsigned)kv;
+        float q, pp, l;
+        qpl(r, idx, q, pp, l);
+        const float ql = (q > 0.f && l != INFINITY) ? __fmul_rn(q, l) : 0.f;
+        w.c[0][s] = q > 0.f ? to_fix(q, kQE) : 0;
+        w.c[1][s] = pp > 0.f ? to_fix(pp, kQE) : 0;
+        w.c[2][s] = ql != 0.f ? to_fix(ql, kLE) : 0;
+        w.lw[s] = l;
+        const bool pos = (uint32_t)(kv >> 32) >= 0x80000000u;
+        if (pos && (s == 0 || (uint32_t)(w.key[s - 1] >> 32) < 0x80000000u)) t.nA = s;
+    }
+    __syncthreads();
+    // alpha part [0, nA): inclusive prefix sums from base; beta part [nA, n):
+    // inclusive suffix sums from above. Warps 0-2 and 3-5, one sum each.
+    if (warp < 6) {
+        const int k = warp % 3;
+        const bool suf = warp >= 3;
+        const int s0 = suf ? t.nA : 0, s1 = suf ? n : t.nA;
+        const int per = (s1 - s0 + 31) / 32;
+        const int c0 = suf ? max(s0, s1 - (lane + 1) * per) : min(s1, s0 + lane * per);
+        const int c1 = suf ? max(s0, s1 - lane * per) : min(s1, c0 + per);
+        long long sum = 0;
+        for (int x = c0; x < c1; ++x) sum += w.c[k][x];
+        long long inc = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        long long run = (suf ? t.above[k] : t.base[k]) + inc - sum;
+        if (!suf) {
+            for (int x = c0; x < c1; ++x) {
+                run += w.c[k][x];
+                w.c[k][x] = run;
+            }
+        } else {
+            for (int x = c1 - 1; x >= c0; --x) {
+                run += w.c[k][x];
+                w.c[k][x] = run;
+            }
+        }
+    }
+    __syncthreads();
+    for (int s = t.nA + tid; s < n; s += NT)
+        w.gw[s] = fix_f(w.c[0][s], 0x1p-50f) * ex2(-w.lw[s] * kLog2e) - fix_f(w.c[1][s], 0x1p-50f);
+    __syncthreads();
+    // exact search: the open grid points of round 0, then the remaining
+    // levels 31 points at a time
+    if (warp == 0) {
+        const double Dd = (double)D;
+        int it = ihi;
+        for (int b0 = ilo; b0 < ihi; b0 += 32) {
+            const int ii = b0 + lane;
+            const bool f = ii < ihi && kl_exact(w, t, (double)(ii * stp) * (1.0 / kNA), nullptr) <= Dd;
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, f);
+            if (bal) {
+                it = b0 + __ffs(bal) - 1;
+                break;
+            }
+        }
+        double hi = (double)(it * stp) * (1.0 / kNA), lo = hi - (double)stp * (1.0 / kNA);
+        for (int left = p.iters - bits0; left > 0;) {
+            const int bits = min(5, left), nn = 1 << bits;
+            const double step = (hi - lo) / (double)nn;
+            const bool f = lane >= 1 && lane < nn && kl_exact(w, t, lo + (double)lane * step, nullptr) <= Dd;
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, f);
+            if (bal) hi = lo + (double)(__ffs(bal) - 1) * step;
+            lo = hi - step;
+            left -= bits;
+        }
+        if (lane == 0) {
+            double bt = 1.0;
+            if (hi < 1.0) kl_exact(w, t, hi, &bt);
+            t.ahi = hi;
+            t.abeta = bt;
+        }
+    }
+    __syncthreads();
+    *alpha_out = t.ahi;
+    *beta_out = (float)t.abeta;
+    __syncthreads();
+    return true;
+}
+
+// The sorting solve's input: sort keys of ln rho, indices, and q, p, ln rho
+// per index in the scratch arrays; returns KL(q || p).
+template <typename E>
+SV_DEV double sort_pass(SmallM& t, const Row<E>& r, int V, uint32_t* k0, uint32_t* i0, float* A) {
+    float acc_kl = 0.f;
+    for (int i = threadIdx.x; i < V; i += NT) {
+        float qq, pp, l;
+        qpl(r, i, qq, pp, l);
+        if (qq > 0.f) acc_kl += qq * l;
+        k0[i] = f32_key(l);
+        i0[i] = (uint32_t)i;
+        A[V + i] = qq;
+        A[2 * (size_t)V + i] = pp;
+        A[3 * (size_t)V + i] = l;
+    }
+    return block_sum_d(t, (double)acc_kl);
 }
 
 // Position states left for the resolve kernel.
@@ -507,7 +1034,9 @@ constexpr int kPosRejectedScaled = 2;  // rejected with alpha < 1: resample from
 template <typename E>
 __global__ void __launch_bounds__(NT, 1) mentor_kernel(const __grid_constant__ MentorParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
+    __shared__ SmallM sm;
     SharedM& s = *reinterpret_cast<SharedM*>(smem_raw);
+    SharedH& sh = *reinterpret_cast<SharedH*>(smem_raw);
     float* coarse = reinterpret_cast<float*>(smem_raw + ((sizeof(SharedM) + 15) & ~size_t(15)));
     const int tid = threadIdx.x;
     const int V = p.V, G = p.gamma, G1 = G + 1, R = 2 * G + 1;
@@ -523,9 +1052,9 @@ __global__ void __launch_bounds__(NT, 1) mentor_kernel(const __grid_constant__ M
     const long long jobs = (long long)p.B * G;
 
     for (;;) {
-        if (tid == 0) s.bi[4] = (int)atomicAdd(p.work, 1u);
+        if (tid == 0) sm.bi[4] = (int)atomicAdd(p.work, 1u);
         __syncthreads();
-        const long long job = s.bi[4];
+        const long long job = sm.bi[4];
         if (job >= jobs) break;
         const int k = (int)(job / p.B), b = (int)(job % p.B);
         const size_t pos = (size_t)b * G + k;
@@ -540,9 +1069,9 @@ __global__ void __launch_bounds__(NT, 1) mentor_kernel(const __grid_constant__ M
         int fl = 0;
         for (int i = tid; i < R; i += NT) fl |= __ldcg(&rb[i].flags);
         const bool bad = __syncthreads_or(fl & kRecEData) != 0;
-        if (tid == 0) s.bi[5] = G - (int)__ldcg(p.rejmark + b) < k;
+        if (tid == 0) sm.bi[5] = G - (int)__ldcg(p.rejmark + b) < k;
         __syncthreads();
-        const bool skip = s.bi[5] != 0;
+        const bool skip = sm.bi[5] != 0;
         __syncthreads();
         if (bad || skip) continue;
 
@@ -561,29 +1090,23 @@ __global__ void __launch_bounds__(NT, 1) mentor_kernel(const __grid_constant__ M
             r.iSt = 1.f / t.S;
             r.iSd = 1.f / d.S;
             r.lnr0 = -(t.m - d.m) * p.inv_t - logf(t.S) + logf(d.S);
-            // KL(q || p), the sort keys, and q, p, ln rho per index for the solve
-            float acc_kl = 0.f;
-            for (int i = tid; i < V; i += NT) {
-                float qq, pp, l;
-                qpl(r, i, qq, pp, l);
-                acc_kl += qq * l;
-                k0[i] = f32_key(l);
-                i0[i] = (uint32_t)i;
-                A[V + i] = qq;
-                A[2 * (size_t)V + i] = pp;
-                A[3 * (size_t)V + i] = l;
-            }
-            const double kl0 = block_sum_d(s, (double)acc_kl);
+            // KL(q || p) from the histogram pass (exact sum of the fp32 terms)
+            hist_pass<E>(sh.h, sm, r, V);
+            scan_hist(sh.h, sm);
+            const bool big = (sm.hflag & 2) != 0;
+            double kl0 = (sm.hflag & 1) ? HUGE_VAL : (double)sm.ltot * 0x1p-46;
+            if (big) kl0 = sort_pass<E>(sm, r, V, k0, i0, A);
             if (kl0 <= (double)p.kl_bound) {
                 state = kPosAccepted;
                 alpha = 0.f;
             } else {
                 double a = 1.0;
                 beta = 1.f;
-                if (p.kl_bound > 0.f) {
+                if (p.kl_bound > 0.f && (big || !solve_hist<E>(sh, sm, p, r, &a, &beta))) {
+                    if (!big) sort_pass<E>(sm, r, V, k0, i0, A);
                     __threadfence_block();
                     __syncthreads();
-                    solve<E>(s, coarse, p, r, k0, i0, k1, i1, A, &a, &beta);
+                    solve<E>(s, sm, coarse, p, r, k0, i0, k1, i1, A, &a, &beta);
                 }
                 alpha = (float)a;
                 // alpha = 1 is the standard test, which failed
@@ -681,7 +1204,8 @@ __global__ void __launch_bounds__(kDrawNT) mentor_resolve_kernel(const __grid_co
 
 size_t mentor_smem_bytes(int V) {
     const int nc = (V + kCoarse - 1) / kCoarse;
-    return ((sizeof(SharedM) + 15) & ~size_t(15)) + 2 * (size_t)nc * sizeof(float);
+    const size_t sorting = ((sizeof(SharedM) + 15) & ~size_t(15)) + 2 * (size_t)nc * sizeof(float);
+    return sorting > sizeof(SharedH) ? sorting : sizeof(SharedH);
 }
 
 cudaError_t launch_mentor(const MentorParams& p, int grid, int resolve_grid, cudaStream_t stream) {
