@@ -66,6 +66,7 @@ struct SmallM {
     long long base[3], above[3]; // sums below the alpha window, above the beta window
     long long ltot;              // sum of q ln rho over the row
     int hflag, ihi, inf, cnt, nA, n, a_b0, a_b1, b_lo, b_hi, ok;
+    float la_lo, la_hi;
     double ahi, abeta;
 };
 
@@ -552,18 +553,30 @@ constexpr int kCap = 4096;            // window indices
 constexpr int kMaxAmb = 64;           // grid points left open by round 0
 constexpr int kQE = 50, kLE = 46;     // fixed-point exponents of q, p and of q ln rho
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kMaxAbsL = 65536.f;   // |ln rho| bound of the fixed point (q > 0)
 
+// A bucket's four 64-bit sums (q, p, and q ln rho split by sign) are kept as
+// pairs of 32-bit words, added to with 32-bit shared atomics plus a carry
+// (the value returned by the low word's atomic says whether it wrapped), then
+// folded to three signed 64-bit sums in place by the scans.
+constexpr int kWords = 8;
+template <int N>
+union HistSide {
+    uint32_t raw[kWords][N];  // (lo, hi) of q, p, q ln rho >= 0, -(q ln rho > 0)
+    long long s[3][N];        // after the scan: prefix (alpha) or suffix (beta) sums
+};
 struct HistArrays {
-    long long hA[3][kNA];  // alpha buckets (q, p, q ln rho); then exclusive prefix sums
-    long long hB[3][kNB];  // beta buckets; then inclusive suffix sums
+    HistSide<kNA> A;       // alpha buckets; then exclusive prefix sums
+    HistSide<kNB> B;       // beta buckets; then inclusive suffix sums
     float gb[kNB];         // g at the lower edge of every beta bucket
     short bb[kNA + 1];     // round 0: first beta edge with g <= R per grid point
 };
 struct WinArrays {
-    unsigned long long key[kCap];  // (ordered ln rho) << 32 | index, sorted
-    long long c[3][kCap];          // alpha part: prefix sums; beta part: suffix sums
-    float lw[kCap];                // ln rho
-    float gw[kCap];                // beta part: g at each index's rho
+    unsigned long long key[kCap];   // (ordered ln rho) << 32 | index, as collected
+    unsigned long long skey[kCap];  // sorted
+    long long c[3][kCap];           // alpha part: prefix sums; beta part: suffix sums
+    float lw[kCap];                 // ln rho
+    float gw[kCap];                 // beta part: g at each index's rho
 };
 union SharedH {
     HistArrays h;
@@ -583,6 +596,17 @@ SV_DEV long long to_fix(float x, int e) {
 
 SV_DEV float fix_f(long long v, float scale) { return __ll2float_rn(v) * scale; }
 
+// Adds v >= 0 to the 64-bit sum held as (lo, hi) words.
+SV_DEV void add64(uint32_t* lo, uint32_t* hi, unsigned long long v) {
+    const uint32_t vl = (uint32_t)v;
+    uint32_t vh = (uint32_t)(v >> 32);
+    if (vl) {
+        const uint32_t old = atomicAdd(lo, vl);
+        vh += (old + vl < old) ? 1u : 0u;
+    }
+    if (vh) atomicAdd(hi, vh);
+}
+
 SV_DEV int alpha_bucket(float l) {  // l < 0
     const float rho = ex2(__fmul_rn(l, kLog2e));
     return min(kNA - 1, (int)__fmul_rn(rho, (float)kNA));
@@ -590,6 +614,12 @@ SV_DEV int alpha_bucket(float l) {  // l < 0
 
 SV_DEV int beta_bucket(float l) {   // l >= 0, possibly +inf
     return l >= (float)kNB / kBScale ? kNB - 1 : (int)__fmul_rn(l, kBScale);
+}
+
+// ln rho of one index (the same rounding as qpl_of).
+template <typename E>
+SV_DEV float l_of(const Row<E>& r, float zt, float zd) {
+    return __fmaf_rn(__fsub_rn(zt, zd), r.inv_t, r.lnr0);
 }
 
 // Calls f(index, target logit, draft logit) for every index of the row pair,
@@ -625,21 +655,13 @@ SV_DEV void for_each_pair(const Row<E>& r, int V, F&& f) {
     for (int i = tail + tid; i < V; i += NT) f(i, VecTraits<E>::load1(r.rt + i), VecTraits<E>::load1(r.rd + i));
 }
 
-// Exclusive prefix (in thread order) of three 64-bit values; tot = the totals.
-SV_DEV void block_exscan3(SmallM& t, long long (&v)[3], long long (&tot)[3]) {
+// Exclusive prefix over the 32 warps (in warp order) of three 64-bit warp
+// totals, given on every lane; tot = the block totals.
+SV_DEV void warp_offsets3(SmallM& t, long long (&v)[3], long long (&tot)[3]) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    long long inc[3] = {v[0], v[1], v[2]};
+    if (lane == 0) {
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-#pragma unroll
-        for (int k = 0; k < 3; ++k) {
-            const long long y = __shfl_up_sync(0xFFFFFFFFu, inc[k], o);
-            if (lane >= o) inc[k] += y;
-        }
-    }
-    if (lane == 31) {
-#pragma unroll
-        for (int k = 0; k < 3; ++k) t.wtot[k][warp] = inc[k];
+        for (int k = 0; k < 3; ++k) t.wtot[k][warp] = v[k];
     }
     __syncthreads();
     if (warp == 0) {
@@ -659,20 +681,30 @@ SV_DEV void block_exscan3(SmallM& t, long long (&v)[3], long long (&tot)[3]) {
     __syncthreads();
 #pragma unroll
     for (int k = 0; k < 3; ++k) {
-        v[k] = inc[k] - v[k] + t.wtot[k][warp];
+        v[k] = t.wtot[k][warp];
         tot[k] = t.wall[k];
     }
     __syncthreads();
 }
 
+template <int N>
+SV_DEV void load_bucket(const HistSide<N>& H, int b, long long (&v)[3]) {
+    const auto w64 = [&](int k) {
+        return (long long)(((unsigned long long)H.raw[2 * k + 1][b] << 32) | H.raw[2 * k][b]);
+    };
+    v[0] = w64(0);
+    v[1] = w64(1);
+    v[2] = w64(2) - w64(3);
+}
+
 // Pass 1: both histograms of the row pair. hflag bit 0: some index has q > 0
-// and p = 0 (KL(q || p) is infinite); bit 1: some |q ln rho| is too large for
-// the fixed point.
+// and p = 0 (KL(q || p) is infinite); bit 1: some index with q > 0 has
+// |ln rho| too large for the fixed point.
 template <typename E>
 SV_DEV void hist_pass(HistArrays& h, SmallM& t, const Row<E>& r, int V) {
     const int tid = threadIdx.x;
-    for (int e = tid; e < 3 * kNA; e += NT) (&h.hA[0][0])[e] = 0;
-    for (int e = tid; e < 3 * kNB; e += NT) (&h.hB[0][0])[e] = 0;
+    for (int e = tid; e < kWords * kNA; e += NT) (&h.A.raw[0][0])[e] = 0u;
+    for (int e = tid; e < kWords * kNB; e += NT) (&h.B.raw[0][0])[e] = 0u;
     if (tid == 0) t.hflag = 0;
     __syncthreads();
     int fl = 0;
@@ -684,110 +716,178 @@ SV_DEV void hist_pass(HistArrays& h, SmallM& t, const Row<E>& r, int V) {
         if (q > 0.f) {
             if (l == INFINITY) {
                 fl |= 1;
+            } else if (!(fabsf(l) < kMaxAbsL)) {
+                fl |= 2;
             } else {
                 ql = __fmul_rn(q, l);
-                if (!(fabsf(ql) < 65536.f)) fl |= 2;
             }
         }
-        long long* H;
-        int stride;
+        uint32_t* H;
+        int st;
         if (l < 0.f) {
-            H = &h.hA[0][alpha_bucket(l)];
-            stride = kNA;
+            H = &h.A.raw[0][alpha_bucket(l)];
+            st = kNA;
         } else {
-            H = &h.hB[0][beta_bucket(l)];
-            stride = kNB;
+            H = &h.B.raw[0][beta_bucket(l)];
+            st = kNB;
         }
-        if (q > 0.f) atomicAdd(reinterpret_cast<unsigned long long*>(H), (unsigned long long)to_fix(q, kQE));
-        if (p > 0.f)
-            atomicAdd(reinterpret_cast<unsigned long long*>(H + stride), (unsigned long long)to_fix(p, kQE));
-        if (ql != 0.f && !(fl & 2))
-            atomicAdd(reinterpret_cast<unsigned long long*>(H + 2 * stride), (unsigned long long)to_fix(ql, kLE));
+        if (q > 0.f) add64(H, H + st, (unsigned long long)to_fix(q, kQE));
+        if (p > 0.f) add64(H + 2 * st, H + 3 * st, (unsigned long long)to_fix(p, kQE));
+        if (ql > 0.f) add64(H + 4 * st, H + 5 * st, (unsigned long long)to_fix(ql, kLE));
+        if (ql < 0.f) add64(H + 6 * st, H + 7 * st, (unsigned long long)to_fix(-ql, kLE));
     });
     if (fl) atomicOr(&t.hflag, fl);
     __syncthreads();
 }
 
 // Alpha buckets to exclusive prefix sums, beta buckets to inclusive suffix
-// sums, totals, and g at every beta edge.
+// sums (both in place), totals, and g at every beta edge. Every word access
+// is a row of 32 consecutive buckets.
 SV_DEV void scan_hist(HistArrays& h, SmallM& t) {
-    const int tid = threadIdx.x;
-    long long v[3], tot[3];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    long long tot[3];
+    {   // alpha: bucket tid
+        long long v[3];
+        load_bucket(h.A, tid, v);
+        long long inc[3] = {v[0], v[1], v[2]};
 #pragma unroll
-    for (int k = 0; k < 3; ++k) v[k] = h.hA[k][tid];
-    block_exscan3(t, v, tot);
+        for (int o = 1; o < 32; o <<= 1) {
 #pragma unroll
-    for (int k = 0; k < 3; ++k) {
-        h.hA[k][tid] = v[k];
-        if (tid == 0) t.tA[k] = tot[k];
-    }
-    // thread tid owns beta buckets [4c, 4c + 4), c = NT - 1 - tid, so that
-    // thread order is descending bucket order
-    const int c0 = (NT - 1 - tid) * 4;
-    long long b[3][4];
+            for (int k = 0; k < 3; ++k) {
+                const long long y = __shfl_up_sync(0xFFFFFFFFu, inc[k], o);
+                if (lane >= o) inc[k] += y;
+            }
+        }
+        long long wt[3];
 #pragma unroll
-    for (int k = 0; k < 3; ++k) {
-        v[k] = 0;
+        for (int k = 0; k < 3; ++k) wt[k] = __shfl_sync(0xFFFFFFFFu, inc[k], 31);
+        warp_offsets3(t, wt, tot);  // its barriers also order the reads above before the writes below
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            b[k][u] = h.hB[k][c0 + u];
-            v[k] += b[k][u];
+        for (int k = 0; k < 3; ++k) {
+            h.A.s[k][tid] = wt[k] + inc[k] - v[k];
+            if (tid == 0) t.tA[k] = tot[k];
         }
     }
-    block_exscan3(t, v, tot);
-#pragma unroll
-    for (int k = 0; k < 3; ++k) {
-        long long run = v[k];
+    {   // beta: warp w owns the 128 buckets [seg, seg + 128), seg = (NW - 1 - w) 128,
+        // as four rows of 32; lane l holds bucket seg + 32u + l of row u
+        const int seg = (NW - 1 - warp) * 128;
+        long long suf[4][3];
+        long long carry[3] = {0, 0, 0};
 #pragma unroll
         for (int u = 3; u >= 0; --u) {
-            run += b[k][u];
-            h.hB[k][c0 + u] = run;
+            long long v[3];
+            load_bucket(h.B, seg + 32 * u + lane, v);
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+                for (int k = 0; k < 3; ++k) {
+                    const long long y = __shfl_down_sync(0xFFFFFFFFu, v[k], o);
+                    if (lane + o < 32) v[k] += y;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 3; ++k) {
+                suf[u][k] = v[k] + carry[k];
+                carry[k] += __shfl_sync(0xFFFFFFFFu, v[k], 0);
+            }
         }
-        if (tid == 0) t.tB[k] = tot[k];
+        warp_offsets3(t, carry, tot);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+#pragma unroll
+            for (int k = 0; k < 3; ++k) h.B.s[k][seg + 32 * u + lane] = suf[u][k] + carry[k];
+        }
+        if (tid == 0) {
+#pragma unroll
+            for (int k = 0; k < 3; ++k) t.tB[k] = tot[k];
+        }
     }
     __syncthreads();
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const int e = c0 + u;
-        h.gb[e] = fix_f(h.hB[0][e], 0x1p-50f) * ex2(-(float)e * (kLog2e / kBScale)) - fix_f(h.hB[1][e], 0x1p-50f);
-    }
+    for (int e = tid; e < kNB; e += NT)
+        h.gb[e] = fix_f(h.B.s[0][e], 0x1p-50f) * ex2(-(float)e * (kLog2e / kBScale)) - fix_f(h.B.s[1][e], 0x1p-50f);
     if (tid == 0) t.ltot = t.tA[2] + t.tB[2];
     __syncthreads();
 }
 
-// KL(alpha) and beta from the windows, in double precision. +inf when the
-// resampled set would be empty.
-SV_DEV double kl_exact(const WinArrays& w, const SmallM& t, double a, double* beta_out) {
-    const double la = log(a);
+// |n| as a float (about one rounding).
+SV_DEV float i128_abs_f(__int128 n) {
+    const unsigned __int128 u = n < 0 ? (unsigned __int128)(-n) : (unsigned __int128)n;
+    return fmaf((float)(unsigned long long)(u >> 64), 0x1p64f, (float)(unsigned long long)u);
+}
+
+// The window search at alpha = J 2^-K (K <= 30): the sums below alpha, R
+// exactly (as the integer (PL - QL/alpha) J = PL J - QL 2^K in units of
+// 2^-50), and the first window index of the resampled set.
+struct WinEval {
+    long long QL, PL, LL, QU, PU, LU;
+    __int128 RJ;      // (PL - QL/alpha) * J, in units of 2^-50
+    bool ok;          // the resampled set is not empty and R + PU > 0
+};
+
+SV_DEV WinEval win_eval(const WinArrays& w, const SmallM& t, uint64_t J, int K, float la) {
+    WinEval e;
     int lo = 0, hi = t.nA;
     while (lo < hi) {
         const int mid = (lo + hi) >> 1;
-        if ((double)w.lw[mid] < la) lo = mid + 1; else hi = mid;
+        if (w.lw[mid] < la) lo = mid + 1; else hi = mid;
     }
-    const long long QLi = lo ? w.c[0][lo - 1] : t.base[0];
-    const long long PLi = lo ? w.c[1][lo - 1] : t.base[1];
-    const long long LLi = lo ? w.c[2][lo - 1] : t.base[2];
-    const double QL = (double)QLi * 0x1p-50, PL = (double)PLi * 0x1p-50;
-    const double R = PL - QL / a;
-    const float Rf = (float)R;
+    e.QL = lo ? w.c[0][lo - 1] : t.base[0];
+    e.PL = lo ? w.c[1][lo - 1] : t.base[1];
+    e.LL = lo ? w.c[2][lo - 1] : t.base[2];
+    e.RJ = (__int128)e.PL * J - ((__int128)e.QL << K);
+    const float R = (e.RJ < 0 ? -1.f : 1.f) * i128_abs_f(e.RJ) / __ull2float_rn(J) * 0x1p-50f;
     lo = t.nA;
     hi = t.n;
     while (lo < hi) {
         const int mid = (lo + hi) >> 1;
-        if (w.gw[mid] <= Rf) hi = mid; else lo = mid + 1;
+        if (w.gw[mid] <= R) hi = mid; else lo = mid + 1;
     }
-    const long long QUi = lo < t.n ? w.c[0][lo] : t.above[0];
-    const long long PUi = lo < t.n ? w.c[1][lo] : t.above[1];
-    const long long LUi = lo < t.n ? w.c[2][lo] : t.above[2];
-    if (QUi <= 0) return HUGE_VAL;
-    const double QU = (double)QUi * 0x1p-50, den = R + (double)PUi * 0x1p-50;
-    if (!(den > 0.0)) return HUGE_VAL;
-    const double beta = QU / den;
-    if (beta_out) *beta_out = beta;
-    return la * QL + (double)(t.ltot - LLi - LUi) * 0x1p-46 + log(beta) * QU;
+    e.QU = lo < t.n ? w.c[0][lo] : t.above[0];
+    e.PU = lo < t.n ? w.c[1][lo] : t.above[1];
+    e.LU = lo < t.n ? w.c[2][lo] : t.above[2];
+    e.ok = e.QU > 0 && e.RJ + (__int128)e.PU * J > 0;
+    return e;
 }
 
-// Rounds 0..: returns false when the row has to go to the sorting solve.
+// ln(J 2^-K) in fp32: J = m 2^e with m in [1/2, 1), so the log is
+// ln m + (e - K) ln 2 without cancellation, and the rounding of J to fp32 is
+// corrected to first order.
+SV_DEV float ln_grid(uint64_t J, int K) {
+    const float jf = __ull2float_rn(J);
+    const float res = __ll2float_rn((long long)(J - (uint64_t)jf));  // J - jf
+    int e;
+    const float m = frexpf(jf, &e);
+    return logf(m) + (float)(e - K) * 0.69314718055994531f + res / jf;
+}
+
+// KL(alpha) from the windows in fp32 (the sums are exact integers, R is
+// exact before its one rounding); +inf when the resampled set is empty.
+SV_DEV float kl_win(const WinArrays& w, const SmallM& t, uint64_t J, int K) {
+    const float la = ln_grid(J, K);
+    const WinEval e = win_eval(w, t, J, K, la);
+    if (!e.ok) return INFINITY;
+    const __int128 den = e.RJ + (__int128)e.PU * J;  // (R + PU) J, fixed-point units
+    const float QU = fix_f(e.QU, 0x1p-50f);
+    const float beta = __ll2float_rn(e.QU) * __ull2float_rn(J) / i128_abs_f(den);
+    return la * fix_f(e.QL, 0x1p-50f) + fix_f(t.ltot - e.LL - e.LU, 0x1p-46f) + logf(beta) * QU;
+}
+
+// n as a double (about one rounding).
+SV_DEV double i128_d(__int128 n) {
+    const bool neg = n < 0;
+    const unsigned __int128 u = neg ? (unsigned __int128)(-n) : (unsigned __int128)n;
+    const double d = (double)(unsigned long long)(u >> 64) * 0x1p64 + (double)(unsigned long long)u;
+    return neg ? -d : d;
+}
+
+// beta at alpha = J 2^-K, in double (one division).
+SV_DEV double beta_win(const WinArrays& w, const SmallM& t, uint64_t J, int K) {
+    const WinEval e = win_eval(w, t, J, K, ln_grid(J, K));
+    if (!e.ok) return 1.0;
+    return i128_d((__int128)e.QU * J) / i128_d(e.RJ + (__int128)e.PU * J);
+}
+
+// Returns false when the row has to go to the sorting solve.
 template <typename E>
 SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<E>& r, double* alpha_out,
                        float* beta_out) {
@@ -801,7 +901,8 @@ SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<
     if (tid == 0) {
         t.ihi = npts;
         t.inf = 0;
-        h.bb[npts] = 0;  // alpha = 1: beta = 1, bucket 0
+        h.bb[0] = (short)kNB;  // alpha -> 0: beta above every edge
+        h.bb[npts] = 0;        // alpha = 1: beta = 1, bucket 0
     }
     __syncthreads();
     const int i = tid + 1;
@@ -809,9 +910,9 @@ SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<
     if (i < npts) {
         const int j = i * stp;
         const float a = (float)j * (1.f / kNA);
-        const long long LLi = h.hA[2][j];
-        const float QL = fix_f(h.hA[0][j], 0x1p-50f), PL = fix_f(h.hA[1][j], 0x1p-50f);
-        const float R = PL - QL / a;
+        const long long QLi = h.A.s[0][j], PLi = h.A.s[1][j], LLi = h.A.s[2][j];
+        const long long RJ = PLi * j - QLi * kNA;  // (PL - QL/a) j, exact (< 2^61)
+        const float R = __ll2float_rn(RJ) / (float)j * 0x1p-50f;
         int lo = 0, hi = kNB;  // first edge with g <= R (kNB: none)
         while (lo < hi) {
             const int mid = (lo + hi) >> 1;
@@ -820,19 +921,19 @@ SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<
         const int b = lo;
         h.bb[i] = (short)b;
         bool sure = false;
-        if (b < kNB && h.hB[0][b] > 0) {
-            const float QU = fix_f(h.hB[0][b], 0x1p-50f), den = R + fix_f(h.hB[1][b], 0x1p-50f);
-            if (den > 0.f) {
-                const float beta = QU / den;
-                const float LM = fix_f(t.ltot - LLi - h.hB[2][b], 0x1p-46f);
-                const float t1 = logf(a) * QL, t3 = logf(beta) * QU;
-                const float kl = t1 + LM + t3;
-                const float QB = b > 0 ? fix_f(h.hB[0][b - 1] - h.hB[0][b], 0x1p-50f) : 0.f;
-                const float efp = 4e-7f * (fabsf(t1) + fabsf(LM) + fabsf(t3)) + 1e-9f;
-                const float err = QB * (0.5f / (kBScale * kBScale)) * (1.f + QB / QU) * 1.01f + efp;
-                sure = kl + efp <= D;
-                maybe = !(kl - err > D);
-            }
+        if (b < kNB && h.B.s[0][b] > 0 && RJ + h.B.s[1][b] * j > 0) {
+            const float QU = fix_f(h.B.s[0][b], 0x1p-50f);
+            // QU / (R + PU) with both sides in fixed-point units
+            const float beta = __ll2float_rn(h.B.s[0][b]) * (float)j / __ll2float_rn(RJ + h.B.s[1][b] * j);
+            const float QL = fix_f(QLi, 0x1p-50f);
+            const float LM = fix_f(t.ltot - LLi - h.B.s[2][b], 0x1p-46f);
+            const float t1 = logf(a) * QL, t3 = logf(beta) * QU;
+            const float kl = t1 + LM + t3;
+            const float QB = b > 0 ? fix_f(h.B.s[0][b - 1] - h.B.s[0][b], 0x1p-50f) : 0.f;
+            const float efp = 4e-7f * (fabsf(t1) + fabsf(LM) + fabsf(t3)) + 1e-9f;
+            const float err = QB * (0.5f / (kBScale * kBScale)) * (1.f + QB / QU) * 1.01f + efp;
+            sure = kl + efp <= D;
+            maybe = !(kl - err > D);
         }
         if (sure) atomicMin(&t.ihi, i);
     }
@@ -841,22 +942,30 @@ SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<
     __syncthreads();
     if (tid == 0) {
         const int ihi = t.ihi, ilo = t.inf + 1;
-        bool ok = !(t.hflag & 2) && !(rounds && ilo == 1) && ihi - ilo <= kMaxAmb;
-        const int a_b0 = (rounds ? ilo - 1 : ilo) * stp, a_b1 = ihi * stp;
-        const int b_lo = ihi < npts ? max(0, h.bb[ihi] - 2) : 0;
-        const int b_hi = min(kNB - 1, (int)h.bb[rounds ? ilo - 1 : ilo]);
+        const bool ok = !(t.hflag & 2) && !(rounds && ilo == 1) && ihi - ilo <= kMaxAmb;
         t.inf = ilo;
-        t.a_b0 = a_b0;
-        t.a_b1 = a_b1;
-        t.b_lo = b_lo;
-        t.b_hi = b_hi;
-        for (int k = 0; k < 3; ++k) {
-            t.base[k] = a_b0 < kNA ? h.hA[k][a_b0] : t.tA[k];
-            t.above[k] = b_hi + 1 < kNB ? h.hB[k][b_hi + 1] : 0;
-        }
         t.cnt = 0;
+        t.nA = 0;
         t.ok = ok;
-        t.ahi = (double)(ihi * stp) * (1.0 / kNA);
+        if (ok) {
+            // every grid point in [ilo - 1, ihi] was evaluated above (bb
+            // holds its beta edge); clamps keep the indexes in range
+            const int a_b0 = (rounds ? ilo - 1 : ilo) * stp, a_b1 = ihi * stp;
+            const int b_lo = ihi < npts ? max(0, (int)h.bb[ihi] - 2) : 0;
+            const int b_hi = max(0, min(kNB - 1, (int)h.bb[rounds ? ilo - 1 : ilo]));
+            t.a_b0 = a_b0;
+            t.a_b1 = a_b1;
+            t.b_lo = b_lo;
+            t.b_hi = b_hi;
+            for (int k = 0; k < 3; ++k) {
+                t.base[k] = a_b0 < kNA ? h.A.s[k][a_b0] : t.tA[k];
+                t.above[k] = b_hi + 1 < kNB ? h.B.s[k][b_hi + 1] : 0;
+            }
+            // ln rho range of the alpha window's buckets (a margin covers the
+            // rounding of the bucket function; the bucket itself decides)
+            t.la_lo = a_b0 > 0 ? logf((float)a_b0 * (1.f / kNA)) - 1e-4f : -INFINITY;
+            t.la_hi = a_b1 < kNA ? logf((float)a_b1 * (1.f / kNA)) + 1e-4f : 0.f;
+        }
     }
     __syncthreads();
     if (!t.ok) return false;
@@ -866,59 +975,77 @@ SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<
         *beta_out = 1.f;
         return true;
     }
-    // pass 2: the window indices
+    // pass 2: the window indices (the row pair is in L2 by now)
     WinArrays& w = sh.w;
     {
         const int a_b0 = t.a_b0, a_b1 = t.a_b1, b_lo = t.b_lo, b_hi = t.b_hi;
+        const float la_lo = t.la_lo, la_hi = t.la_hi;
         for_each_pair<E>(r, V, [&](int idx, float zt, float zd) {
-            float q, pp, l;
-            qpl_of(r, zt, zd, q, pp, l);
-            if (!(q > 0.f) && !(pp > 0.f)) return;
+            const float l = l_of(r, zt, zd);
             bool sel;
             if (l < 0.f) {
-                const int j = alpha_bucket(l);
-                sel = j >= a_b0 && j < a_b1;
+                sel = l >= la_lo && l < la_hi;
+                if (sel) {
+                    const int j = alpha_bucket(l);
+                    sel = j >= a_b0 && j < a_b1;
+                }
             } else {
                 const int b = beta_bucket(l);
                 sel = b >= b_lo && b <= b_hi;
             }
             if (sel) {
-                const unsigned s = atomicAdd(reinterpret_cast<unsigned*>(&t.cnt), 1u);
-                if (s < (unsigned)kCap) w.key[s] = ((unsigned long long)f32_key(l) << 32) | (unsigned)idx;
+                float q, pp, l2;
+                qpl_of(r, zt, zd, q, pp, l2);
+                if (q > 0.f || pp > 0.f) {
+                    const unsigned s = atomicAdd(reinterpret_cast<unsigned*>(&t.cnt), 1u);
+                    if (s < (unsigned)kCap) w.key[s] = ((unsigned long long)f32_key(l) << 32) | (unsigned)idx;
+                }
             }
         });
     }
     __syncthreads();
     const int n = t.cnt;
     if (n > kCap) return false;
-    int n2 = 2;
-    while (n2 < n) n2 <<= 1;
-    for (int s = n + tid; s < n2; s += NT) w.key[s] = ~0ull;
-    __syncthreads();
-    for (int k = 2; k <= n2; k <<= 1) {
-        for (int jj = k >> 1; jj > 0; jj >>= 1) {
-            for (int x = tid; x < n2; x += NT) {
-                const int y = x ^ jj;
-                if (y > x) {
-                    const unsigned long long ka = w.key[x], kb = w.key[y];
-                    if ((ka > kb) == ((x & k) == 0)) {
-                        w.key[x] = kb;
-                        w.key[y] = ka;
+    if (n <= NT) {
+        // rank sort (keys are distinct: the index is part of the key)
+        if (tid < n) {
+            const unsigned long long kv = w.key[tid];
+            int rank = 0;
+#pragma unroll 4
+            for (int j = 0; j < n; ++j) rank += w.key[j] < kv;
+            w.skey[rank] = kv;
+            if ((uint32_t)(kv >> 32) < 0x80000000u) atomicAdd(&t.nA, 1);
+        }
+    } else {
+        int n2 = 2;
+        while (n2 < n) n2 <<= 1;
+        for (int s = n + tid; s < n2; s += NT) w.key[s] = ~0ull;
+        __syncthreads();
+        for (int k = 2; k <= n2; k <<= 1) {
+            for (int jj = k >> 1; jj > 0; jj >>= 1) {
+                for (int x = tid; x < n2; x += NT) {
+                    const int y = x ^ jj;
+                    if (y > x) {
+                        const unsigned long long ka = w.key[x], kb = w.key[y];
+                        if ((ka > kb) == ((x & k) == 0)) {
+                            w.key[x] = kb;
+                            w.key[y] = ka;
+                        }
                     }
                 }
+                __syncthreads();
             }
-            __syncthreads();
+        }
+        for (int s = tid; s < n; s += NT) {
+            w.skey[s] = w.key[s];
+            if ((uint32_t)(w.key[s] >> 32) < 0x80000000u) atomicAdd(&t.nA, 1);
         }
     }
-    // the window's values in sorted order (recomputed exactly as in pass 1)
-    if (tid == 0) {
-        t.n = n;
-        t.nA = n;
-    }
+    if (tid == 0) t.n = n;
     __syncthreads();
+    // the window's values in sorted order (recomputed exactly as in pass 1)
     for (int s = tid; s < n; s += NT) {
-        const unsigned long long kv = w.key[s];
-        const int idx = (int)(unsigned)kv;
+        const int idx = (int)(uint32_t)w.skey[s];
         float q, pp, l;
         qpl(r, idx, q, pp, l);
         const float ql = (q > 0.f && l != INFINITY) ? __fmul_rn(q, l) : 0.f;
@@ -926,8 +1053,6 @@ SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<
         w.c[1][s] = pp > 0.f ? to_fix(pp, kQE) : 0;
         w.c[2][s] = ql != 0.f ? to_fix(ql, kLE) : 0;
         w.lw[s] = l;
-        const bool pos = (uint32_t)(kv >> 32) >= 0x80000000u;
-        if (pos && (s == 0 || (uint32_t)(w.key[s - 1] >> 32) < 0x80000000u)) t.nA = s;
     }
     __syncthreads();
     // alpha part [0, nA): inclusive prefix sums from base; beta part [nA, n):
@@ -964,35 +1089,37 @@ SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<
     for (int s = t.nA + tid; s < n; s += NT)
         w.gw[s] = fix_f(w.c[0][s], 0x1p-50f) * ex2(-w.lw[s] * kLog2e) - fix_f(w.c[1][s], 0x1p-50f);
     __syncthreads();
-    // exact search: the open grid points of round 0, then the remaining
-    // levels 31 points at a time
+    // exact search on the dyadic grid alpha = J 2^-K: the open points of
+    // round 0, then the remaining levels, 31 points at a time
     if (warp == 0) {
-        const double Dd = (double)D;
         int it = ihi;
         for (int b0 = ilo; b0 < ihi; b0 += 32) {
             const int ii = b0 + lane;
-            const bool f = ii < ihi && kl_exact(w, t, (double)(ii * stp) * (1.0 / kNA), nullptr) <= Dd;
+            const bool f = ii < ihi && kl_win(w, t, (uint64_t)(ii * stp), 10) <= D;
             const unsigned bal = __ballot_sync(0xFFFFFFFFu, f);
             if (bal) {
                 it = b0 + __ffs(bal) - 1;
                 break;
             }
         }
-        double hi = (double)(it * stp) * (1.0 / kNA), lo = hi - (double)stp * (1.0 / kNA);
-        for (int left = p.iters - bits0; left > 0;) {
+        // hi = J 2^-K; each level adds bits to K. Levels beyond 2^-60 move
+        // alpha by less than any tolerance and are not taken.
+        uint64_t J = (uint64_t)(it * stp);
+        int K = 10;
+        for (int left = min(p.iters, 60) - bits0; left > 0;) {
             const int bits = min(5, left), nn = 1 << bits;
-            const double step = (hi - lo) / (double)nn;
-            const bool f = lane >= 1 && lane < nn && kl_exact(w, t, lo + (double)lane * step, nullptr) <= Dd;
+            J <<= bits;
+            K += bits;
+            const uint64_t lo = J - (uint64_t)nn;  // hi - one step of the previous level
+            const bool f = lane >= 1 && lane < nn && kl_win(w, t, lo + (uint64_t)lane, K) <= D;
             const unsigned bal = __ballot_sync(0xFFFFFFFFu, f);
-            if (bal) hi = lo + (double)(__ffs(bal) - 1) * step;
-            lo = hi - step;
+            if (bal) J = lo + (uint64_t)(__ffs(bal) - 1);
             left -= bits;
         }
         if (lane == 0) {
-            double bt = 1.0;
-            if (hi < 1.0) kl_exact(w, t, hi, &bt);
-            t.ahi = hi;
-            t.abeta = bt;
+            const double a = ldexp((double)J, -K);
+            t.ahi = a;
+            t.abeta = a < 1.0 ? beta_win(w, t, J, K) : 1.0;
         }
     }
     __syncthreads();
