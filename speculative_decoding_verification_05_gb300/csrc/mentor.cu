@@ -66,7 +66,7 @@ struct SmallM {
     long long base[3], above[3]; // sums below the alpha window, above the beta window
     long long ltot;              // sum of q ln rho over the row
     int hflag, ihi, inf, cnt, nA, n, a_b0, a_b1, b_lo, b_hi, ok;
-    float la_lo, la_hi;
+    int iw[NW], scan_total;
     double ahi, abeta;
 };
 
@@ -547,18 +547,22 @@ SV_DEV void solve(SharedM& s, SmallM& t, float* coarse, const MentorParams& p, c
 // fixed point go to the sorting solve.
 // ---------------------------------------------------------------------------
 constexpr int kNA = 1024;             // alpha buckets of rho in [0, 1)
-constexpr int kNB = 4096;             // beta buckets of ln rho in [0, 32) (last one open)
-constexpr float kBScale = 128.f;      // beta buckets per unit of ln rho
-constexpr int kCap = 4096;            // window indices
+constexpr int kNB = 2048;             // beta buckets of ln rho in [0, 32) (last one open)
+constexpr float kBScale = 64.f;       // beta buckets per unit of ln rho
+constexpr int kCap = 2048;            // window indices
+constexpr int kIdsSmem = 32768;       // rows up to this length keep their bucket ids in shared memory
 constexpr int kMaxAmb = 64;           // grid points left open by round 0
-constexpr int kQE = 50, kLE = 46;     // fixed-point exponents of q, p and of q ln rho
+constexpr float kQF = 0x1p44f, kLF = 0x1p40f;    // fixed-point scales of q, p and of q ln rho
+constexpr float kQS = 0x1p-44f, kLS = 0x1p-40f;  // and their inverses
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kMaxAbsL = 65536.f;   // |ln rho| bound of the fixed point (q > 0)
+constexpr uint32_t kDead = 0xFFFFu;   // bucket id of an index with q = p = 0
 
 // A bucket's four 64-bit sums (q, p, and q ln rho split by sign) are kept as
 // pairs of 32-bit words, added to with 32-bit shared atomics plus a carry
 // (the value returned by the low word's atomic says whether it wrapped), then
-// folded to three signed 64-bit sums in place by the scans.
+// folded to three signed 64-bit sums in place by the scans. The scales keep
+// almost every term below 2^32, so the high word is rarely touched.
 constexpr int kWords = 8;
 template <int N>
 union HistSide {
@@ -566,43 +570,60 @@ union HistSide {
     long long s[3][N];        // after the scan: prefix (alpha) or suffix (beta) sums
 };
 struct HistArrays {
-    HistSide<kNA> A;       // alpha buckets; then exclusive prefix sums
-    HistSide<kNB> B;       // beta buckets; then inclusive suffix sums
-    float gb[kNB];         // g at the lower edge of every beta bucket
-    short bb[kNA + 1];     // round 0: first beta edge with g <= R per grid point
+    HistSide<kNA> A;          // alpha buckets; then exclusive prefix sums
+    HistSide<kNB> B;          // beta buckets; then inclusive suffix sums
+    float gb[kNB];            // g at the lower edge of every beta bucket
+    short bb[kNA + 8];        // round 0: first beta edge with g <= R per grid point
+    uint16_t ids[kIdsSmem];   // pass 1: bucket id of every index (V <= kIdsSmem)
 };
+// Overlays HistArrays once round 0 is done. Pass 2 writes only `key`, which
+// lies below `ids`; everything else is written after pass 2.
 struct WinArrays {
     unsigned long long key[kCap];   // (ordered ln rho) << 32 | index, as collected
     unsigned long long skey[kCap];  // sorted
     long long c[3][kCap];           // alpha part: prefix sums; beta part: suffix sums
     float lw[kCap];                 // ln rho
     float gw[kCap];                 // beta part: g at each index's rho
+    long long cu[3][kCap];          // the values in collection order
+    float lwu[kCap];
 };
 union SharedH {
     HistArrays h;
     WinArrays w;
 };
 
-// x * 2^e truncated toward zero, for |x| * 2^e < 2^62.
-SV_DEV long long to_fix(float x, int e) {
-    const uint32_t u = __float_as_uint(x);
-    const int ex = (int)((u >> 23) & 255u);
-    if (ex == 0) return 0;
-    const long long m = (long long)((u & 0x7FFFFFu) | 0x800000u);
-    const int sh = ex - 150 + e;
-    const long long v = sh >= 0 ? (m << sh) : (sh > -24 ? (m >> -sh) : 0);
-    return (u >> 31) ? -v : v;
+// x * scale (scale a power of two, 0 <= x scale < 2^56) rounded to the
+// nearest integer, as 32-bit words: hi = floor(v / 2^32) and v - hi 2^32 are
+// both exact in fp32, so two 32-bit conversions give the 64-bit integer.
+struct Fix2 {
+    uint32_t lo, hi;
+};
+SV_DEV Fix2 fix2(float x, float scale) {
+    const float v = x * scale;
+    const uint32_t hi = __float2uint_rd(v * 0x1p-32f);
+    return {__float2uint_rn(fmaf(-(float)hi, 0x1p32f, v)), hi};
 }
 
-SV_DEV float fix_f(long long v, float scale) { return __ll2float_rn(v) * scale; }
+// Signed fixed point of x (|x| scale < 2^56).
+SV_DEV long long to_fix(float x, float scale) {
+    const Fix2 f = fix2(fabsf(x), scale);
+    const long long v = (long long)(((unsigned long long)f.hi << 32) | f.lo);
+    return x < 0.f ? -v : v;
+}
 
-// Adds v >= 0 to the 64-bit sum held as (lo, hi) words.
-SV_DEV void add64(uint32_t* lo, uint32_t* hi, unsigned long long v) {
-    const uint32_t vl = (uint32_t)v;
-    uint32_t vh = (uint32_t)(v >> 32);
-    if (vl) {
-        const uint32_t old = atomicAdd(lo, vl);
-        vh += (old + vl < old) ? 1u : 0u;
+// 64-bit integers to fp32 through two 32-bit conversions (about one rounding).
+SV_DEV float ll2f(long long v) { return fmaf((float)(int)(v >> 32), 0x1p32f, __uint2float_rn((unsigned)v)); }
+SV_DEV float ull2f(unsigned long long v) {
+    return fmaf(__uint2float_rn((unsigned)(v >> 32)), 0x1p32f, __uint2float_rn((unsigned)v));
+}
+SV_DEV float fix_f(long long v, float scale) { return ll2f(v) * scale; }
+
+// Adds f to the 64-bit sum held as (lo, hi) words.
+SV_DEV void add64(uint32_t* lo, uint32_t* hi, Fix2 f) {
+    uint32_t vh = f.hi;
+    if (f.lo) {
+        const uint32_t old = atomicAdd(lo, f.lo);
+        vh += (old + f.lo < old) ? 1u : 0u;
     }
     if (vh) atomicAdd(hi, vh);
 }
@@ -620,39 +641,6 @@ SV_DEV int beta_bucket(float l) {   // l >= 0, possibly +inf
 template <typename E>
 SV_DEV float l_of(const Row<E>& r, float zt, float zd) {
     return __fmaf_rn(__fsub_rn(zt, zd), r.inv_t, r.lnr0);
-}
-
-// Calls f(index, target logit, draft logit) for every index of the row pair,
-// two 16-byte vectors of each row in flight per thread when both rows are
-// 16-byte aligned.
-template <typename E, typename F>
-SV_DEV void for_each_pair(const Row<E>& r, int V, F&& f) {
-    constexpr int kN = VecTraits<E>::kN;
-    const int tid = threadIdx.x;
-    int tail = 0;
-    if (((reinterpret_cast<uintptr_t>(r.rt) | reinterpret_cast<uintptr_t>(r.rd)) & 15u) == 0) {
-        const int nv = V / kN;
-        const uint4* vt = reinterpret_cast<const uint4*>(r.rt);
-        const uint4* vd = reinterpret_cast<const uint4*>(r.rd);
-        for (int v = tid; v < nv; v += 2 * NT) {
-            const bool two = v + NT < nv;
-            const uint4 a0 = __ldg(vt + v), b0 = __ldg(vd + v);
-            const uint4 a1 = two ? __ldg(vt + v + NT) : a0, b1 = two ? __ldg(vd + v + NT) : b0;
-            float x[kN], y[kN];
-            VecTraits<E>::unpack(a0, x);
-            VecTraits<E>::unpack(b0, y);
-#pragma unroll
-            for (int u = 0; u < kN; ++u) f(v * kN + u, x[u], y[u]);
-            if (two) {
-                VecTraits<E>::unpack(a1, x);
-                VecTraits<E>::unpack(b1, y);
-#pragma unroll
-                for (int u = 0; u < kN; ++u) f((v + NT) * kN + u, x[u], y[u]);
-            }
-        }
-        tail = nv * kN;
-    }
-    for (int i = tail + tid; i < V; i += NT) f(i, VecTraits<E>::load1(r.rt + i), VecTraits<E>::load1(r.rd + i));
 }
 
 // Exclusive prefix over the 32 warps (in warp order) of three 64-bit warp
@@ -687,8 +675,152 @@ SV_DEV void warp_offsets3(SmallM& t, long long (&v)[3], long long (&tot)[3]) {
     __syncthreads();
 }
 
+// Exclusive prefix in thread order of three 64-bit values; tot = totals.
+SV_DEV void block_exscan3(SmallM& t, long long (&v)[3], long long (&tot)[3]) {
+    const int lane = threadIdx.x & 31;
+    long long inc[3] = {v[0], v[1], v[2]};
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            const long long y = __shfl_up_sync(0xFFFFFFFFu, inc[k], o);
+            if (lane >= o) inc[k] += y;
+        }
+    }
+    long long wt[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) wt[k] = __shfl_sync(0xFFFFFFFFu, inc[k], 31);
+    warp_offsets3(t, wt, tot);
+#pragma unroll
+    for (int k = 0; k < 3; ++k) v[k] = wt[k] + inc[k] - v[k];
+}
+
+// Exclusive prefix in thread order of one int; the total lands in t.scan_total.
+SV_DEV int block_exscan_int(SmallM& t, int v) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if (lane >= o) inc += y;
+    }
+    if (lane == 31) t.iw[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        const int w0 = t.iw[lane];
+        int w = w0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+            if (lane >= o) w += y;
+        }
+        t.iw[lane] = w - w0;
+        if (lane == 31) t.scan_total = w;
+    }
+    __syncthreads();
+    return t.iw[warp] + inc - v;
+}
+
+// One index of pass 1: its bucket sums and its bucket id (alpha: 0..kNA-1,
+// beta: kNA + bucket, kDead when q = p = 0).
+template <typename E>
+SV_DEV uint32_t hist_elem(HistArrays& h, const Row<E>& r, float zt, float zd, int& fl) {
+    float q, p, l;
+    qpl_of(r, zt, zd, q, p, l);
+    if (!(q > 0.f) && !(p > 0.f)) return kDead;
+    float ql = 0.f;
+    if (q > 0.f) {
+        if (l == INFINITY) {
+            fl |= 1;
+        } else if (!(fabsf(l) < kMaxAbsL)) {
+            fl |= 2;
+        } else {
+            ql = __fmul_rn(q, l);
+        }
+    }
+    uint32_t* H;
+    int st;
+    uint32_t id;
+    if (l < 0.f) {
+        const int j = alpha_bucket(l);
+        H = &h.A.raw[0][j];
+        st = kNA;
+        id = (uint32_t)j;
+    } else {
+        const int b = beta_bucket(l);
+        H = &h.B.raw[0][b];
+        st = kNB;
+        id = (uint32_t)(kNA + b);
+    }
+    if (q > 0.f) add64(H, H + st, fix2(q, kQF));
+    if (p > 0.f) add64(H + 2 * st, H + 3 * st, fix2(p, kQF));
+    if (ql > 0.f) add64(H + 4 * st, H + 5 * st, fix2(ql, kLF));
+    if (ql < 0.f) add64(H + 6 * st, H + 7 * st, fix2(-ql, kLF));
+    return id;
+}
+
+// Pass 1: both histograms of the row pair, and every index's bucket id in
+// `ids` (16 bits per index, written with 8- or 16-byte stores). hflag bit 0:
+// some index has q > 0 and p = 0 (KL(q || p) is infinite); bit 1: some index
+// with q > 0 has |ln rho| too large for the fixed point.
+template <typename E>
+SV_DEV void hist_pass(HistArrays& h, SmallM& t, const Row<E>& r, int V, uint16_t* ids) {
+    constexpr int kN = VecTraits<E>::kN;
+    const int tid = threadIdx.x;
+    for (int e = tid; e < kWords * kNA; e += NT) (&h.A.raw[0][0])[e] = 0u;
+    for (int e = tid; e < kWords * kNB; e += NT) (&h.B.raw[0][0])[e] = 0u;
+    const bool vec = ((reinterpret_cast<uintptr_t>(r.rt) | reinterpret_cast<uintptr_t>(r.rd)) & 15u) == 0 &&
+                     (reinterpret_cast<uintptr_t>(ids) & (2 * kN - 1)) == 0;
+    if (vec && tid < 4) {  // the row pair into L2 (bulk prefetch, 64 KB pieces)
+        const size_t bytes = (size_t)(V / kN) * 16;
+        const char* base = reinterpret_cast<const char*>(tid < 2 ? (const void*)r.rt : (const void*)r.rd);
+        for (size_t o = (size_t)(tid & 1) * 65536; o < bytes; o += 131072) {
+            const uint32_t sz = (uint32_t)(bytes - o < 65536 ? bytes - o : 65536);
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + o), "r"(sz) : "memory");
+        }
+    }
+    if (tid == 0) t.hflag = 0;
+    __syncthreads();
+    int fl = 0;
+    int tail = 0;
+    if (vec) {
+        const int nv = V / kN;
+        const uint4* vt = reinterpret_cast<const uint4*>(r.rt);
+        const uint4* vd = reinterpret_cast<const uint4*>(r.rd);
+        const auto proc = [&](int vv, const uint4& a, const uint4& b) {
+            float x[kN], y[kN];
+            VecTraits<E>::unpack(a, x);
+            VecTraits<E>::unpack(b, y);
+            uint32_t pk[kN / 2];
+#pragma unroll
+            for (int u = 0; u < kN; u += 2) {
+                const uint32_t i0 = hist_elem(h, r, x[u], y[u], fl);
+                const uint32_t i1 = hist_elem(h, r, x[u + 1], y[u + 1], fl);
+                pk[u / 2] = i0 | (i1 << 16);
+            }
+            if constexpr (kN == 4) {
+                *reinterpret_cast<uint2*>(ids + (size_t)vv * kN) = make_uint2(pk[0], pk[1]);
+            } else {
+                *reinterpret_cast<uint4*>(ids + (size_t)vv * kN) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+        };
+        for (int v = tid; v < nv; v += 2 * NT) {
+            const bool two = v + NT < nv;
+            const uint4 a0 = __ldg(vt + v), b0 = __ldg(vd + v);
+            const uint4 a1 = two ? __ldg(vt + v + NT) : a0, b1 = two ? __ldg(vd + v + NT) : b0;
+            proc(v, a0, b0);
+            if (two) proc(v + NT, a1, b1);
+        }
+        tail = nv * kN;
+    }
+    for (int i = tail + tid; i < V; i += NT)
+        ids[i] = (uint16_t)hist_elem(h, r, VecTraits<E>::load1(r.rt + i), VecTraits<E>::load1(r.rd + i), fl);
+    if (fl) atomicOr(&t.hflag, fl);
+    __syncthreads();
+}
+
 template <int N>
-SV_DEV void load_bucket(const HistSide<N>& H, int b, long long (&v)[3]) {
+SV_DEV void bucket3(const HistSide<N>& H, int b, long long (&v)[3]) {
     const auto w64 = [&](int k) {
         return (long long)(((unsigned long long)H.raw[2 * k + 1][b] << 32) | H.raw[2 * k][b]);
     };
@@ -697,114 +829,62 @@ SV_DEV void load_bucket(const HistSide<N>& H, int b, long long (&v)[3]) {
     v[2] = w64(2) - w64(3);
 }
 
-// Pass 1: both histograms of the row pair. hflag bit 0: some index has q > 0
-// and p = 0 (KL(q || p) is infinite); bit 1: some index with q > 0 has
-// |ln rho| too large for the fixed point.
-template <typename E>
-SV_DEV void hist_pass(HistArrays& h, SmallM& t, const Row<E>& r, int V) {
-    const int tid = threadIdx.x;
-    for (int e = tid; e < kWords * kNA; e += NT) (&h.A.raw[0][0])[e] = 0u;
-    for (int e = tid; e < kWords * kNB; e += NT) (&h.B.raw[0][0])[e] = 0u;
-    if (tid == 0) t.hflag = 0;
-    __syncthreads();
-    int fl = 0;
-    for_each_pair<E>(r, V, [&](int, float zt, float zd) {
-        float q, p, l;
-        qpl_of(r, zt, zd, q, p, l);
-        if (!(q > 0.f) && !(p > 0.f)) return;
-        float ql = 0.f;
-        if (q > 0.f) {
-            if (l == INFINITY) {
-                fl |= 1;
-            } else if (!(fabsf(l) < kMaxAbsL)) {
-                fl |= 2;
-            } else {
-                ql = __fmul_rn(q, l);
-            }
-        }
-        uint32_t* H;
-        int st;
-        if (l < 0.f) {
-            H = &h.A.raw[0][alpha_bucket(l)];
-            st = kNA;
-        } else {
-            H = &h.B.raw[0][beta_bucket(l)];
-            st = kNB;
-        }
-        if (q > 0.f) add64(H, H + st, (unsigned long long)to_fix(q, kQE));
-        if (p > 0.f) add64(H + 2 * st, H + 3 * st, (unsigned long long)to_fix(p, kQE));
-        if (ql > 0.f) add64(H + 4 * st, H + 5 * st, (unsigned long long)to_fix(ql, kLE));
-        if (ql < 0.f) add64(H + 6 * st, H + 7 * st, (unsigned long long)to_fix(-ql, kLE));
-    });
-    if (fl) atomicOr(&t.hflag, fl);
-    __syncthreads();
-}
-
 // Alpha buckets to exclusive prefix sums, beta buckets to inclusive suffix
-// sums (both in place), totals, and g at every beta edge. Every word access
-// is a row of 32 consecutive buckets.
+// sums (both in place: every raw word is read before the first barrier of
+// the block scans, every sum is written after it), totals, and g at every
+// beta edge.
 SV_DEV void scan_hist(HistArrays& h, SmallM& t) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     long long tot[3];
-    {   // alpha: bucket tid
+    {   // alpha: one bucket per thread
         long long v[3];
-        load_bucket(h.A, tid, v);
-        long long inc[3] = {v[0], v[1], v[2]};
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-#pragma unroll
-            for (int k = 0; k < 3; ++k) {
-                const long long y = __shfl_up_sync(0xFFFFFFFFu, inc[k], o);
-                if (lane >= o) inc[k] += y;
-            }
-        }
-        long long wt[3];
-#pragma unroll
-        for (int k = 0; k < 3; ++k) wt[k] = __shfl_sync(0xFFFFFFFFu, inc[k], 31);
-        warp_offsets3(t, wt, tot);  // its barriers also order the reads above before the writes below
+        bucket3(h.A, tid, v);
+        block_exscan3(t, v, tot);
 #pragma unroll
         for (int k = 0; k < 3; ++k) {
-            h.A.s[k][tid] = wt[k] + inc[k] - v[k];
+            h.A.s[k][tid] = v[k];
             if (tid == 0) t.tA[k] = tot[k];
         }
     }
-    {   // beta: warp w owns the 128 buckets [seg, seg + 128), seg = (NW - 1 - w) 128,
-        // as four rows of 32; lane l holds bucket seg + 32u + l of row u
-        const int seg = (NW - 1 - warp) * 128;
-        long long suf[4][3];
-        long long carry[3] = {0, 0, 0};
+    {   // beta: thread tid owns the two buckets [c0, c0 + 2), c0 = 2 (NT - 1 - tid),
+        // so thread order is descending bucket order; 8- and 16-byte accesses
+        static_assert(kNB == 2 * NT, "two beta buckets per thread");
+        const int c0 = (NT - 1 - tid) * 2;
+        long long sf[3][2];
 #pragma unroll
-        for (int u = 3; u >= 0; --u) {
-            long long v[3];
-            load_bucket(h.B, seg + 32 * u + lane, v);
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-#pragma unroll
-                for (int k = 0; k < 3; ++k) {
-                    const long long y = __shfl_down_sync(0xFFFFFFFFu, v[k], o);
-                    if (lane + o < 32) v[k] += y;
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < 3; ++k) {
-                suf[u][k] = v[k] + carry[k];
-                carry[k] += __shfl_sync(0xFFFFFFFFu, v[k], 0);
-            }
+        for (int k = 0; k < 3; ++k) {
+            const uint2 lo = *reinterpret_cast<const uint2*>(&h.B.raw[2 * k][c0]);
+            const uint2 hi = *reinterpret_cast<const uint2*>(&h.B.raw[2 * k + 1][c0]);
+            sf[k][0] = (long long)(((unsigned long long)hi.x << 32) | lo.x);
+            sf[k][1] = (long long)(((unsigned long long)hi.y << 32) | lo.y);
         }
-        warp_offsets3(t, carry, tot);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-#pragma unroll
-            for (int k = 0; k < 3; ++k) h.B.s[k][seg + 32 * u + lane] = suf[u][k] + carry[k];
+        {
+            const uint2 lo = *reinterpret_cast<const uint2*>(&h.B.raw[6][c0]);
+            const uint2 hi = *reinterpret_cast<const uint2*>(&h.B.raw[7][c0]);
+            sf[2][0] -= (long long)(((unsigned long long)hi.x << 32) | lo.x);
+            sf[2][1] -= (long long)(((unsigned long long)hi.y << 32) | lo.y);
         }
-        if (tid == 0) {
+        long long v[3];
 #pragma unroll
-            for (int k = 0; k < 3; ++k) t.tB[k] = tot[k];
+        for (int k = 0; k < 3; ++k) {
+            sf[k][0] += sf[k][1];
+            v[k] = sf[k][0];
         }
+        block_exscan3(t, v, tot);  // v: the sums of all higher chunks
+        float g[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+#pragma unroll
+            for (int k = 0; k < 3; ++k) sf[k][u] += v[k];
+            g[u] = fix_f(sf[0][u], kQS) * ex2(-(float)(c0 + u) * (kLog2e / kBScale)) - fix_f(sf[1][u], kQS);
+        }
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            *reinterpret_cast<longlong2*>(&h.B.s[k][c0]) = make_longlong2(sf[k][0], sf[k][1]);
+            if (tid == 0) t.tB[k] = tot[k];
+        }
+        *reinterpret_cast<float2*>(&h.gb[c0]) = make_float2(g[0], g[1]);
     }
-    __syncthreads();
-    for (int e = tid; e < kNB; e += NT)
-        h.gb[e] = fix_f(h.B.s[0][e], 0x1p-50f) * ex2(-(float)e * (kLog2e / kBScale)) - fix_f(h.B.s[1][e], 0x1p-50f);
     if (tid == 0) t.ltot = t.tA[2] + t.tB[2];
     __syncthreads();
 }
@@ -812,15 +892,15 @@ SV_DEV void scan_hist(HistArrays& h, SmallM& t) {
 // |n| as a float (about one rounding).
 SV_DEV float i128_abs_f(__int128 n) {
     const unsigned __int128 u = n < 0 ? (unsigned __int128)(-n) : (unsigned __int128)n;
-    return fmaf((float)(unsigned long long)(u >> 64), 0x1p64f, (float)(unsigned long long)u);
+    return fmaf(ull2f((unsigned long long)(u >> 64)), 0x1p64f, ull2f((unsigned long long)u));
 }
 
-// The window search at alpha = J 2^-K (K <= 30): the sums below alpha, R
-// exactly (as the integer (PL - QL/alpha) J = PL J - QL 2^K in units of
-// 2^-50), and the first window index of the resampled set.
+// The window search at alpha = J 2^-K: the sums below alpha, R exactly (as
+// the integer (PL - QL/alpha) J = PL J - QL 2^K in fixed-point units), and
+// the first window index of the resampled set.
 struct WinEval {
     long long QL, PL, LL, QU, PU, LU;
-    __int128 RJ;      // (PL - QL/alpha) * J, in units of 2^-50
+    __int128 RJ;      // (PL - QL/alpha) J
     bool ok;          // the resampled set is not empty and R + PU > 0
 };
 
@@ -835,7 +915,7 @@ SV_DEV WinEval win_eval(const WinArrays& w, const SmallM& t, uint64_t J, int K, 
     e.PL = lo ? w.c[1][lo - 1] : t.base[1];
     e.LL = lo ? w.c[2][lo - 1] : t.base[2];
     e.RJ = (__int128)e.PL * J - ((__int128)e.QL << K);
-    const float R = (e.RJ < 0 ? -1.f : 1.f) * i128_abs_f(e.RJ) / __ull2float_rn(J) * 0x1p-50f;
+    const float R = (e.RJ < 0 ? -1.f : 1.f) * i128_abs_f(e.RJ) / ull2f(J) * kQS;
     lo = t.nA;
     hi = t.n;
     while (lo < hi) {
@@ -853,8 +933,8 @@ SV_DEV WinEval win_eval(const WinArrays& w, const SmallM& t, uint64_t J, int K, 
 // ln m + (e - K) ln 2 without cancellation, and the rounding of J to fp32 is
 // corrected to first order.
 SV_DEV float ln_grid(uint64_t J, int K) {
-    const float jf = __ull2float_rn(J);
-    const float res = __ll2float_rn((long long)(J - (uint64_t)jf));  // J - jf
+    const float jf = ull2f(J);
+    const float res = ll2f((long long)(J - (uint64_t)jf));  // J - jf
     int e;
     const float m = frexpf(jf, &e);
     return logf(m) + (float)(e - K) * 0.69314718055994531f + res / jf;
@@ -867,9 +947,8 @@ SV_DEV float kl_win(const WinArrays& w, const SmallM& t, uint64_t J, int K) {
     const WinEval e = win_eval(w, t, J, K, la);
     if (!e.ok) return INFINITY;
     const __int128 den = e.RJ + (__int128)e.PU * J;  // (R + PU) J, fixed-point units
-    const float QU = fix_f(e.QU, 0x1p-50f);
-    const float beta = __ll2float_rn(e.QU) * __ull2float_rn(J) / i128_abs_f(den);
-    return la * fix_f(e.QL, 0x1p-50f) + fix_f(t.ltot - e.LL - e.LU, 0x1p-46f) + logf(beta) * QU;
+    const float beta = ll2f(e.QU) * ull2f(J) / i128_abs_f(den);
+    return la * fix_f(e.QL, kQS) + fix_f(t.ltot - e.LL - e.LU, kLS) + logf(beta) * fix_f(e.QU, kQS);
 }
 
 // n as a double (about one rounding).
@@ -889,8 +968,8 @@ SV_DEV double beta_win(const WinArrays& w, const SmallM& t, uint64_t J, int K) {
 
 // Returns false when the row has to go to the sorting solve.
 template <typename E>
-SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<E>& r, double* alpha_out,
-                       float* beta_out) {
+SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<E>& r, const uint16_t* ids,
+                       double* alpha_out, float* beta_out) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int V = p.V;
     const float D = p.kl_bound;
@@ -911,8 +990,8 @@ SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<
         const int j = i * stp;
         const float a = (float)j * (1.f / kNA);
         const long long QLi = h.A.s[0][j], PLi = h.A.s[1][j], LLi = h.A.s[2][j];
-        const long long RJ = PLi * j - QLi * kNA;  // (PL - QL/a) j, exact (< 2^61)
-        const float R = __ll2float_rn(RJ) / (float)j * 0x1p-50f;
+        const long long RJ = PLi * j - QLi * kNA;  // (PL - QL/a) j, exact
+        const float R = ll2f(RJ) / (float)j * kQS;
         int lo = 0, hi = kNB;  // first edge with g <= R (kNB: none)
         while (lo < hi) {
             const int mid = (lo + hi) >> 1;
@@ -922,14 +1001,14 @@ SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<
         h.bb[i] = (short)b;
         bool sure = false;
         if (b < kNB && h.B.s[0][b] > 0 && RJ + h.B.s[1][b] * j > 0) {
-            const float QU = fix_f(h.B.s[0][b], 0x1p-50f);
+            const float QU = fix_f(h.B.s[0][b], kQS);
             // QU / (R + PU) with both sides in fixed-point units
-            const float beta = __ll2float_rn(h.B.s[0][b]) * (float)j / __ll2float_rn(RJ + h.B.s[1][b] * j);
-            const float QL = fix_f(QLi, 0x1p-50f);
-            const float LM = fix_f(t.ltot - LLi - h.B.s[2][b], 0x1p-46f);
+            const float beta = ll2f(h.B.s[0][b]) * (float)j / ll2f(RJ + h.B.s[1][b] * j);
+            const float QL = fix_f(QLi, kQS);
+            const float LM = fix_f(t.ltot - LLi - h.B.s[2][b], kLS);
             const float t1 = logf(a) * QL, t3 = logf(beta) * QU;
             const float kl = t1 + LM + t3;
-            const float QB = b > 0 ? fix_f(h.B.s[0][b - 1] - h.B.s[0][b], 0x1p-50f) : 0.f;
+            const float QB = b > 0 ? fix_f(h.B.s[0][b - 1] - h.B.s[0][b], kQS) : 0.f;
             const float efp = 4e-7f * (fabsf(t1) + fabsf(LM) + fabsf(t3)) + 1e-9f;
             const float err = QB * (0.5f / (kBScale * kBScale)) * (1.f + QB / QU) * 1.01f + efp;
             sure = kl + efp <= D;
@@ -961,10 +1040,6 @@ SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<
                 t.base[k] = a_b0 < kNA ? h.A.s[k][a_b0] : t.tA[k];
                 t.above[k] = b_hi + 1 < kNB ? h.B.s[k][b_hi + 1] : 0;
             }
-            // ln rho range of the alpha window's buckets (a margin covers the
-            // rounding of the bucket function; the bucket itself decides)
-            t.la_lo = a_b0 > 0 ? logf((float)a_b0 * (1.f / kNA)) - 1e-4f : -INFINITY;
-            t.la_hi = a_b1 < kNA ? logf((float)a_b1 * (1.f / kNA)) + 1e-4f : 0.f;
         }
     }
     __syncthreads();
@@ -975,46 +1050,110 @@ SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<
         *beta_out = 1.f;
         return true;
     }
-    // pass 2: the window indices (the row pair is in L2 by now)
+    // pass 2: the window indices, from the bucket ids of pass 1. Each thread
+    // counts its candidates, a block scan gives it its output offset, and a
+    // second walk writes them (ordered by thread, no atomics).
     WinArrays& w = sh.w;
     {
-        const int a_b0 = t.a_b0, a_b1 = t.a_b1, b_lo = t.b_lo, b_hi = t.b_hi;
-        const float la_lo = t.la_lo, la_hi = t.la_hi;
-        for_each_pair<E>(r, V, [&](int idx, float zt, float zd) {
-            const float l = l_of(r, zt, zd);
-            bool sel;
-            if (l < 0.f) {
-                sel = l >= la_lo && l < la_hi;
-                if (sel) {
-                    const int j = alpha_bucket(l);
-                    sel = j >= a_b0 && j < a_b1;
-                }
-            } else {
-                const int b = beta_bucket(l);
-                sel = b >= b_lo && b <= b_hi;
+        const uint32_t A0 = (uint32_t)t.a_b0, A1 = (uint32_t)t.a_b1;
+        const uint32_t B0 = (uint32_t)(kNA + t.b_lo), B1 = (uint32_t)(kNA + t.b_hi);
+        const auto sel = [&](uint32_t id) { return id < (uint32_t)kNA ? (id >= A0 && id < A1) : (id >= B0 && id <= B1); };
+        // instantiated for shared-memory and for global ids, so that each
+        // access uses its own address space
+        const auto collect = [&](const uint16_t* idp) {
+            const bool vec = (reinterpret_cast<uintptr_t>(idp) & 15u) == 0;
+            const int n8 = vec ? V / 8 : 0;
+            const uint4* iv = reinterpret_cast<const uint4*>(idp);
+            int cnt = 0;
+            for (int v = tid; v < n8; v += NT) {
+                const uint4 x = iv[v];
+                const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) cnt += (int)sel(wd[c] & 0xFFFFu) + (int)sel(wd[c] >> 16);
             }
-            if (sel) {
-                float q, pp, l2;
-                qpl_of(r, zt, zd, q, pp, l2);
-                if (q > 0.f || pp > 0.f) {
-                    const unsigned s = atomicAdd(reinterpret_cast<unsigned*>(&t.cnt), 1u);
-                    if (s < (unsigned)kCap) w.key[s] = ((unsigned long long)f32_key(l) << 32) | (unsigned)idx;
+            for (int idx = n8 * 8 + tid; idx < V; idx += NT) cnt += (int)sel(idp[idx]);
+            int off = block_exscan_int(t, cnt);
+            for (int v = tid; cnt && v < n8; v += NT) {
+                const uint4 x = iv[v];
+                const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    if (sel(c & 1 ? wd[c >> 1] >> 16 : wd[c >> 1] & 0xFFFFu)) {
+                        if (off < kCap) w.key[off] = (unsigned)(v * 8 + c);
+                        ++off;
+                    }
                 }
             }
-        });
+            for (int idx = n8 * 8 + tid; cnt && idx < V; idx += NT) {
+                if (sel(idp[idx])) {
+                    if (off < kCap) w.key[off] = (unsigned)idx;
+                    ++off;
+                }
+            }
+        };
+        if (V <= kIdsSmem) collect(sh.h.ids); else collect(ids);
     }
     __syncthreads();
-    const int n = t.cnt;
+    const int n = t.scan_total;
     if (n > kCap) return false;
+    // keys and values of the window indices (recomputed exactly as in pass 1)
+    for (int s = tid; s < n; s += NT) {
+        const int idx = (int)(uint32_t)w.key[s];
+        float q, pp, l;
+        qpl(r, idx, q, pp, l);
+        const float ql = (q > 0.f && l != INFINITY) ? __fmul_rn(q, l) : 0.f;
+        w.key[s] = ((unsigned long long)f32_key(l) << 32) | (unsigned)idx;
+        w.cu[0][s] = q > 0.f ? to_fix(q, kQF) : 0;
+        w.cu[1][s] = pp > 0.f ? to_fix(pp, kQF) : 0;
+        w.cu[2][s] = ql != 0.f ? to_fix(ql, kLF) : 0;
+        w.lwu[s] = l;
+    }
+    __syncthreads();
     if (n <= NT) {
-        // rank sort (keys are distinct: the index is part of the key)
+        // bitonic sort of one key per thread (keys are distinct: the index is
+        // part of the key), strides below 32 by shuffles, the rest through
+        // shared memory; each key carries its collection slot, so the values
+        // are placed directly
+        int n2 = 32;
+        while (n2 < n) n2 <<= 1;
+        const bool act = tid < n2;
+        unsigned long long x = tid < n ? w.key[tid] : ~0ull;
+        int slot = tid;
+        __syncthreads();
+        for (int k = 2; k <= n2; k <<= 1) {
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                unsigned long long y;
+                int ys;
+                if (j >= 32) {
+                    if (act) {
+                        w.skey[tid] = x;
+                        w.lw[tid] = __int_as_float(slot);
+                    }
+                    __syncthreads();
+                    if (act) {
+                        y = w.skey[tid ^ j];
+                        ys = __float_as_int(w.lw[tid ^ j]);
+                    }
+                    __syncthreads();
+                } else {
+                    y = __shfl_xor_sync(0xFFFFFFFFu, x, j);
+                    ys = __shfl_xor_sync(0xFFFFFFFFu, slot, j);
+                }
+                if (act) {
+                    const bool keep_min = ((tid & j) == 0) == ((tid & k) == 0);
+                    if ((y < x) == keep_min) {
+                        x = y;
+                        slot = ys;
+                    }
+                }
+            }
+        }
         if (tid < n) {
-            const unsigned long long kv = w.key[tid];
-            int rank = 0;
-#pragma unroll 4
-            for (int j = 0; j < n; ++j) rank += w.key[j] < kv;
-            w.skey[rank] = kv;
-            if ((uint32_t)(kv >> 32) < 0x80000000u) atomicAdd(&t.nA, 1);
+            w.skey[tid] = x;
+#pragma unroll
+            for (int k = 0; k < 3; ++k) w.c[k][tid] = w.cu[k][slot];
+            w.lw[tid] = w.lwu[slot];
+            if ((uint32_t)(x >> 32) < 0x80000000u) atomicAdd(&t.nA, 1);
         }
     } else {
         int n2 = 2;
@@ -1043,15 +1182,16 @@ SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<
     }
     if (tid == 0) t.n = n;
     __syncthreads();
-    // the window's values in sorted order (recomputed exactly as in pass 1)
-    for (int s = tid; s < n; s += NT) {
+    // the window's values in sorted order (already placed by the register
+    // sort; after the shared-memory sort, recomputed exactly as in pass 1)
+    for (int s = tid; n > NT && s < n; s += NT) {
         const int idx = (int)(uint32_t)w.skey[s];
         float q, pp, l;
         qpl(r, idx, q, pp, l);
         const float ql = (q > 0.f && l != INFINITY) ? __fmul_rn(q, l) : 0.f;
-        w.c[0][s] = q > 0.f ? to_fix(q, kQE) : 0;
-        w.c[1][s] = pp > 0.f ? to_fix(pp, kQE) : 0;
-        w.c[2][s] = ql != 0.f ? to_fix(ql, kLE) : 0;
+        w.c[0][s] = q > 0.f ? to_fix(q, kQF) : 0;
+        w.c[1][s] = pp > 0.f ? to_fix(pp, kQF) : 0;
+        w.c[2][s] = ql != 0.f ? to_fix(ql, kLF) : 0;
         w.lw[s] = l;
     }
     __syncthreads();
@@ -1087,10 +1227,10 @@ SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<
     }
     __syncthreads();
     for (int s = t.nA + tid; s < n; s += NT)
-        w.gw[s] = fix_f(w.c[0][s], 0x1p-50f) * ex2(-w.lw[s] * kLog2e) - fix_f(w.c[1][s], 0x1p-50f);
+        w.gw[s] = fix_f(w.c[0][s], kQS) * ex2(-w.lw[s] * kLog2e) - fix_f(w.c[1][s], kQS);
     __syncthreads();
     // exact search on the dyadic grid alpha = J 2^-K: the open points of
-    // round 0, then the remaining levels, 31 points at a time
+    // round 0 (warp 0), then the remaining levels, up to 1023 points at a time
     if (warp == 0) {
         int it = ihi;
         for (int b0 = ilo; b0 < ihi; b0 += 32) {
@@ -1102,30 +1242,36 @@ SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<
                 break;
             }
         }
-        // hi = J 2^-K; each level adds bits to K. Levels beyond 2^-60 move
-        // alpha by less than any tolerance and are not taken.
-        uint64_t J = (uint64_t)(it * stp);
-        int K = 10;
-        for (int left = min(p.iters, 60) - bits0; left > 0;) {
-            const int bits = min(5, left), nn = 1 << bits;
-            J <<= bits;
-            K += bits;
-            const uint64_t lo = J - (uint64_t)nn;  // hi - one step of the previous level
-            const bool f = lane >= 1 && lane < nn && kl_win(w, t, lo + (uint64_t)lane, K) <= D;
-            const unsigned bal = __ballot_sync(0xFFFFFFFFu, f);
-            if (bal) J = lo + (uint64_t)(__ffs(bal) - 1);
-            left -= bits;
-        }
-        if (lane == 0) {
-            const double a = ldexp((double)J, -K);
-            t.ahi = a;
-            t.abeta = a < 1.0 ? beta_win(w, t, J, K) : 1.0;
-        }
+        if (lane == 0) t.inf = it;
     }
     __syncthreads();
-    *alpha_out = t.ahi;
-    *beta_out = (float)t.abeta;
+    // hi = J 2^-K; each level adds bits to K. Levels beyond 2^-60 move alpha
+    // by less than any tolerance and are not taken.
+    uint64_t J = (uint64_t)(t.inf * stp);
+    int K = 10;
+    for (int left = min(p.iters, 60) - bits0; left > 0;) {
+        const int bits = min(10, left), nn = 1 << bits;
+        J <<= bits;
+        K += bits;
+        const uint64_t lo = J - (uint64_t)nn;  // hi - one step of the previous level
+        if (tid == 0) t.cnt = nn;
+        __syncthreads();
+        if (i < nn && kl_win(w, t, lo + (uint64_t)i, K) <= D) atomicMin(&t.cnt, i);
+        __syncthreads();
+        if (t.cnt < nn) J = lo + (uint64_t)t.cnt;
+        left -= bits;
+        __syncthreads();
+    }
+    if (tid == 0) {
+        const double a = ldexp((double)J, -K);
+        t.ahi = a;
+        t.abeta = a < 1.0 ? beta_win(w, t, J, K) : 1.0;
+    }
     __syncthreads();
+    if (tid == 0) {  // the caller reads the result on thread 0 only
+        *alpha_out = t.ahi;
+        *beta_out = (float)t.abeta;
+    }
     return true;
 }
 
@@ -1174,6 +1320,9 @@ __global__ void __launch_bounds__(NT, 1) mentor_kernel(const __grid_constant__ M
     uint32_t* i0 = p.idx + slot * 2 * (size_t)V;
     uint32_t* i1 = i0 + V;
     float* A = p.arr + slot * 7 * (size_t)V;
+    // pass-1 bucket ids: shared memory for rows up to kIdsSmem, else global
+    // scratch (which the sorting solve reuses afterwards)
+    uint16_t* ids = V <= kIdsSmem ? sh.h.ids : reinterpret_cast<uint16_t*>(k0);
     const E* tgt = reinterpret_cast<const E*>(p.target);
     const E* dft = reinterpret_cast<const E*>(p.draft);
     const long long jobs = (long long)p.B * G;
@@ -1218,28 +1367,35 @@ __global__ void __launch_bounds__(NT, 1) mentor_kernel(const __grid_constant__ M
             r.iSd = 1.f / d.S;
             r.lnr0 = -(t.m - d.m) * p.inv_t - logf(t.S) + logf(d.S);
             // KL(q || p) from the histogram pass (exact sum of the fp32 terms)
-            hist_pass<E>(sh.h, sm, r, V);
+            if (V <= kIdsSmem) hist_pass<E>(sh.h, sm, r, V, sh.h.ids); else hist_pass<E>(sh.h, sm, r, V, ids);
             scan_hist(sh.h, sm);
+            // (double precision is scarce on this part: thread 0 takes the
+            // scalar decisions in double and shares them)
             const bool big = (sm.hflag & 2) != 0;
-            double kl0 = (sm.hflag & 1) ? HUGE_VAL : (double)sm.ltot * 0x1p-46;
-            if (big) kl0 = sort_pass<E>(sm, r, V, k0, i0, A);
-            if (kl0 <= (double)p.kl_bound) {
+            if (tid == 0)
+                sm.bi[6] = !big && !(sm.hflag & 1) && (double)sm.ltot * (double)kLS <= (double)p.kl_bound;
+            __syncthreads();
+            bool shortcut = sm.bi[6] != 0;
+            if (big) shortcut = sort_pass<E>(sm, r, V, k0, i0, A) <= (double)p.kl_bound;
+            if (shortcut) {
                 state = kPosAccepted;
                 alpha = 0.f;
             } else {
                 double a = 1.0;
                 beta = 1.f;
-                if (p.kl_bound > 0.f && (big || !solve_hist<E>(sh, sm, p, r, &a, &beta))) {
+                if (p.kl_bound > 0.f && (big || !solve_hist<E>(sh, sm, p, r, ids, &a, &beta))) {
                     if (!big) sort_pass<E>(sm, r, V, k0, i0, A);
                     __threadfence_block();
                     __syncthreads();
                     solve<E>(s, sm, coarse, p, r, k0, i0, k1, i1, A, &a, &beta);
                 }
-                alpha = (float)a;
-                // alpha = 1 is the standard test, which failed
-                if (a < 1.0) {
-                    const double rho = pd > 0.f ? (double)q / (double)pd : (q > 0.f ? HUGE_VAL : 0.0);
-                    state = (double)u < fmin(1.0, rho / a) ? kPosAccepted : kPosRejectedScaled;
+                if (tid == 0) {
+                    alpha = (float)a;
+                    // alpha = 1 is the standard test, which failed
+                    if (a < 1.0) {
+                        const double rho = pd > 0.f ? (double)q / (double)pd : (q > 0.f ? HUGE_VAL : 0.0);
+                        state = (double)u < fmin(1.0, rho / a) ? kPosAccepted : kPosRejectedScaled;
+                    }
                 }
             }
         }
