@@ -695,32 +695,6 @@ SV_DEV void block_exscan3(SmallM& t, long long (&v)[3], long long (&tot)[3]) {
     for (int k = 0; k < 3; ++k) v[k] = wt[k] + inc[k] - v[k];
 }
 
-// Exclusive prefix in thread order of one int; the total lands in t.scan_total.
-SV_DEV int block_exscan_int(SmallM& t, int v) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int inc = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-        if (lane >= o) inc += y;
-    }
-    if (lane == 31) t.iw[warp] = inc;
-    __syncthreads();
-    if (warp == 0) {
-        const int w0 = t.iw[lane];
-        int w = w0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xFFFFFFFFu, w, o);
-            if (lane >= o) w += y;
-        }
-        t.iw[lane] = w - w0;
-        if (lane == 31) t.scan_total = w;
-    }
-    __syncthreads();
-    return t.iw[warp] + inc - v;
-}
-
 // One index of pass 1: its bucket sums and its bucket id (alpha: 0..kNA-1,
 // beta: kNA + bucket, kDead when q = p = 0).
 template <typename E>
@@ -1058,40 +1032,66 @@ SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<
         const uint32_t A0 = (uint32_t)t.a_b0, A1 = (uint32_t)t.a_b1;
         const uint32_t B0 = (uint32_t)(kNA + t.b_lo), B1 = (uint32_t)(kNA + t.b_hi);
         const auto sel = [&](uint32_t id) { return id < (uint32_t)kNA ? (id >= A0 && id < A1) : (id >= B0 && id <= B1); };
-        // instantiated for shared-memory and for global ids, so that each
-        // access uses its own address space
+        // one walk over the ids: each warp appends its candidates to a private
+        // buffer (ballot ranks, no atomics; warp order, then index order), a
+        // scan of the 32 warp counts places the buffers. The buffers live in
+        // `skey`, which is free until the sort and lies below the ids.
+        constexpr int kWarpBuf = kCap * 2 / NW;  // 32-bit entries per warp
+        uint32_t* wb = reinterpret_cast<uint32_t*>(w.skey) + warp * kWarpBuf;
+        const unsigned lt = (1u << lane) - 1u;
         const auto collect = [&](const uint16_t* idp) {
             const bool vec = (reinterpret_cast<uintptr_t>(idp) & 15u) == 0;
             const int n8 = vec ? V / 8 : 0;
             const uint4* iv = reinterpret_cast<const uint4*>(idp);
-            int cnt = 0;
-            for (int v = tid; v < n8; v += NT) {
-                const uint4 x = iv[v];
-                const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                for (int c = 0; c < 4; ++c) cnt += (int)sel(wd[c] & 0xFFFFu) + (int)sel(wd[c] >> 16);
-            }
-            for (int idx = n8 * 8 + tid; idx < V; idx += NT) cnt += (int)sel(idp[idx]);
-            int off = block_exscan_int(t, cnt);
-            for (int v = tid; cnt && v < n8; v += NT) {
-                const uint4 x = iv[v];
+            int wc = 0;
+            for (int v0 = warp * 32; v0 < n8; v0 += NT) {  // warp-uniform trip count
+                const int v = v0 + lane;
+                const bool ok = v < n8;
+                const uint4 x = ok ? iv[v] : make_uint4(kDead | (kDead << 16), kDead | (kDead << 16),
+                                                        kDead | (kDead << 16), kDead | (kDead << 16));
                 const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
-                    if (sel(c & 1 ? wd[c >> 1] >> 16 : wd[c >> 1] & 0xFFFFu)) {
-                        if (off < kCap) w.key[off] = (unsigned)(v * 8 + c);
-                        ++off;
+                    const bool pr = sel(c & 1 ? wd[c >> 1] >> 16 : wd[c >> 1] & 0xFFFFu);
+                    const unsigned bal = __ballot_sync(0xFFFFFFFFu, pr);
+                    if (pr) {
+                        const int pos = wc + __popc(bal & lt);
+                        if (pos < kWarpBuf) wb[pos] = (uint32_t)(v * 8 + c);
                     }
+                    wc += __popc(bal);
                 }
             }
-            for (int idx = n8 * 8 + tid; cnt && idx < V; idx += NT) {
-                if (sel(idp[idx])) {
-                    if (off < kCap) w.key[off] = (unsigned)idx;
-                    ++off;
+            for (int i0 = n8 * 8 + warp * 32; i0 < V; i0 += NT) {
+                const int idx = i0 + lane;
+                const bool pr = idx < V && sel(idp[idx]);
+                const unsigned bal = __ballot_sync(0xFFFFFFFFu, pr);
+                if (pr) {
+                    const int pos = wc + __popc(bal & lt);
+                    if (pos < kWarpBuf) wb[pos] = (uint32_t)idx;
                 }
+                wc += __popc(bal);
             }
+            return wc;
         };
-        if (V <= kIdsSmem) collect(sh.h.ids); else collect(ids);
+        const int wc = V <= kIdsSmem ? collect(sh.h.ids) : collect(ids);
+        if (lane == 0) t.iw[warp] = wc;
+        __syncthreads();
+        if (warp == 0) {
+            const int c0 = t.iw[lane];
+            int c = c0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, c, o);
+                if (lane >= o) c += y;
+            }
+            t.iw[lane] = c - c0;
+            const bool over = __any_sync(0xFFFFFFFFu, c0 > kWarpBuf);
+            if (lane == 31) t.scan_total = over ? kCap + 1 : c;
+        }
+        __syncthreads();
+        const int off = t.iw[warp];
+        for (int i = lane; i < wc && i < kWarpBuf; i += 32)
+            if (off + i < kCap) w.key[off + i] = wb[i];
     }
     __syncthreads();
     const int n = t.scan_total;
@@ -1116,7 +1116,7 @@ SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<
         // are placed directly
         int n2 = 32;
         while (n2 < n) n2 <<= 1;
-        const bool act = tid < n2;
+        const bool act = tid < n2;  // whole warps (n2 is a multiple of 32)
         unsigned long long x = tid < n ? w.key[tid] : ~0ull;
         int slot = tid;
         __syncthreads();
@@ -1135,7 +1135,7 @@ SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<
                         ys = __float_as_int(w.lw[tid ^ j]);
                     }
                     __syncthreads();
-                } else {
+                } else if (act) {
                     y = __shfl_xor_sync(0xFFFFFFFFu, x, j);
                     ys = __shfl_xor_sync(0xFFFFFFFFu, slot, j);
                 }
