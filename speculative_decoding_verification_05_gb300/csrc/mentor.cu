@@ -19,13 +19,15 @@
 // CTA per SM) solves (sequence, position) jobs independently, skipping a job
 // once an earlier position of its sequence is known to be rejected; the
 // resolve kernel then finds each sequence's first rejection and makes its one
-// draw. The sort is a stable LSD radix sort (four 8-bit digit passes) of the
-// fp32 keys of ln(rho) in global scratch. The bisection's result (the smallest
-// dyadic alpha = j 2^-iters with KL(alpha) <= D) is found by a multiway
-// search: each round evaluates KL at up to 1023 interior grid points of the
-// current interval in parallel, ten bisection steps at a time. Rejections with
-// alpha = 1 (beta = 1) and the bonus token use the verification path's own
-// draw, so D = 0 reproduces spec_verify bit for bit.
+// draw. The bisection's result is the smallest dyadic alpha = j 2^-iters with
+// KL(alpha) <= D. The sums above are needed only at the bisection's points, so
+// a row is solved without sorting it (solve_hist: histograms of rho whose
+// edges are the first ten levels, then exact sums over the few indices near
+// alpha and beta); rows outside that scheme's limits take the sorting solve
+// (solve: a stable LSD radix sort of ln(rho) in global scratch, the six
+// running sums, and a multiway search evaluating up to 1023 grid points at a
+// time). Rejections with alpha = 1 (beta = 1) and the bonus token use the
+// verification path's own draw, so D = 0 reproduces spec_verify bit for bit.
 
 #include "common.cuh"
 #include "draw.cuh"
