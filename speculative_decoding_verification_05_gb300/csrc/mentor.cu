@@ -381,7 +381,7 @@ SV_DEV void solve(SharedM& s, SmallM& t, float* coarse, const MentorParams& p, c
             const int j = jb + lane;
             const bool ok = j < w1;
             float q = ok ? __ldcg(SQ + j) : 0.f, pp = ok ? __ldcg(SP + j) : 0.f;
-            float ql = ok ? q * __ldcg(L + j) : 0.f;
+            float ql = (ok && q > 0.f) ? q * __ldcg(L + j) : 0.f;  // q = 0 contributes 0 (ln rho may be -inf)
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const float a1 = __shfl_up_sync(0xFFFFFFFFu, q, o), a2 = __shfl_up_sync(0xFFFFFFFFu, pp, o),
@@ -1285,6 +1285,7 @@ SV_DEV double sort_pass(SmallM& t, const Row<E>& r, int V, uint32_t* k0, uint32_
     for (int i = threadIdx.x; i < V; i += NT) {
         float qq, pp, l;
         qpl(r, i, qq, pp, l);
+        if (!(qq > 0.f) && !(pp > 0.f)) l = -INFINITY;  // q = p = 0: rho = 0 (ln rho would be NaN)
         if (qq > 0.f) acc_kl += qq * l;
         k0[i] = f32_key(l);
         i0[i] = (uint32_t)i;

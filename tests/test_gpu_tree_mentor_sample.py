@@ -68,10 +68,11 @@ def test_tree_malformed_and_bad_rows():
 # -------------------------------------------------------------- mentor ----
 
 def _mentor(zt, zd, D, seed=0, iters=30, label=""):
-    drafts = oracle.sample(zd, 1.0, seed=seed + 11)["tokens"]
+    zt_o, zd_o = zt.float().numpy(), zd.float().numpy()  # the oracle reads the same values in fp64
+    drafts = oracle.sample(zd_o, 1.0, seed=seed + 11)["tokens"]
     g = sv.verify_mentor(zt.cuda(), zd.cuda(), torch.from_numpy(drafts).int().cuda(), 1.0, D, iters,
                          seed, 0, debug=True)
-    r = oracle.verify_mentor(zt, zd, drafts, 1.0, D, iters, seed, 0)
+    r = oracle.verify_mentor(zt_o, zd_o, drafts, 1.0, D, iters, seed, 0)
     assert_linear_parity(g, r, max_near_frac=0.15, label=label)
     assert_probs(g["probs"], r, label)
     # alpha at the decided positions (k <= accepted) of rows without near-ties:
@@ -110,10 +111,41 @@ def test_mentor_bound_zero_equals_standard_verification():
         np.testing.assert_array_equal(np_(m[k]), np_(v[k]))
 
 
-@pytest.mark.parametrize("V,iters", [(3, 30), (100, 30), (5000, 12), (40001, 30)])
+@pytest.mark.parametrize("V,iters", [(3, 30), (100, 30), (5000, 12), (40001, 30), (40000, 30)])
 def test_mentor_shapes(V, iters):
+    """Small and odd vocabularies; above 32768 entries the pass-1 bucket ids
+    live in global scratch (40001: scalar accesses, 40000: 16-byte ones)."""
     zt, zd = workloads.linear_logits(12, 3, V, V, sd_t=2.0, sd_d=1.2)
     _mentor(zt, zd, 0.05, seed=V, iters=iters, label=f"mentor V={V}")
+
+
+@pytest.mark.parametrize("iters", [1, 5, 10, 40, 64])
+def test_mentor_bisection_depths(iters):
+    """Up to ten levels the first round alone decides; beyond 2^-60 levels
+    change alpha by less than any tolerance and are not taken."""
+    zt, zd = workloads.linear_logits(10, 3, 4099, 7 + iters, sd_t=2.0, sd_d=1.2)
+    _mentor(zt, zd, 0.05, seed=iters, iters=iters, label=f"iters={iters}")
+
+
+def test_mentor_loose_bound_and_extreme_rows():
+    """A loose bound on far-apart rows (results below 2^-10 with levels left:
+    the sorting solve takes those rows), then peaked targets with
+    zero-probability logits on either side (q > 0 = p makes KL(q || p)
+    infinite and rho infinite)."""
+    zt, zd = workloads.linear_logits(12, 3, 3000, 21, sd_t=2.0, sd_d=4.0)
+    _, r, _ = _mentor(zt, zd, 2.0, seed=3, label="loose bound")
+    assert ((r["alpha"] > 0) & (r["alpha"] < 2.0 ** -10)).any(), "no row took a result below 2^-10"
+    zt2, zd2 = workloads.linear_logits(12, 3, 3000, 22, sd_t=6.0, sd_d=1.0)
+    zt2[:, :, 5] += 12.0
+    zd2[:, :, 3::7] = float("-inf")
+    zt2[:, :, 1::11] = float("-inf")
+    _mentor(zt2, zd2, 0.1, seed=4, label="extremes")
+
+
+def test_mentor_bf16():
+    zt, zd = workloads.linear_logits(10, 3, 32000, 31, dtype="bf16", sd_t=2.0, sd_d=1.2)
+    _, r, _ = _mentor(zt, zd, 0.1, seed=1, label="mentor bf16")
+    assert ((r["alpha"] > 0) & (r["alpha"] < 1)).any()
 
 
 # -------------------------------------------------------------- sample ----
