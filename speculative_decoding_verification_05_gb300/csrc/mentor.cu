@@ -639,12 +639,6 @@ SV_DEV int beta_bucket(float l) {   // l >= 0, possibly +inf
     return l >= (float)kNB / kBScale ? kNB - 1 : (int)__fmul_rn(l, kBScale);
 }
 
-// ln rho of one index (the same rounding as qpl_of).
-template <typename E>
-SV_DEV float l_of(const Row<E>& r, float zt, float zd) {
-    return __fmaf_rn(__fsub_rn(zt, zd), r.inv_t, r.lnr0);
-}
-
 // Exclusive prefix over the 32 warps (in warp order) of three 64-bit warp
 // totals, given on every lane; tot = the block totals.
 SV_DEV void warp_offsets3(SmallM& t, long long (&v)[3], long long (&tot)[3]) {
@@ -1248,7 +1242,7 @@ SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<
     }
     __syncthreads();
     // hi = J 2^-K; each level adds bits to K. Levels beyond 2^-60 move alpha
-    // by less than any tolerance and are not taken.
+    // by less than its double-precision resolution near 1/2 and are not taken.
     uint64_t J = (uint64_t)(t.inf * stp);
     int K = 10;
     for (int left = min(p.iters, 60) - bits0; left > 0;) {
