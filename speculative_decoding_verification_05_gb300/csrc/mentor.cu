@@ -1106,49 +1106,46 @@ SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<
     }
     __syncthreads();
     if (n <= NT) {
-        // bitonic sort of one key per thread (keys are distinct: the index is
-        // part of the key), strides below 32 by shuffles, the rest through
-        // shared memory; each key carries its collection slot, so the values
-        // are placed directly
+        // keys (ordered ln rho) << 32 | collection slot (the collection order
+        // is deterministic, so ties in ln rho are too). Each warp sorts a run
+        // of 32 keys in registers; a key's rank is its place in its run plus
+        // the count of smaller keys in every other run (binary searches), and
+        // its values are placed from its slot.
         int n2 = 32;
         while (n2 < n) n2 <<= 1;
-        const bool act = tid < n2;  // whole warps (n2 is a multiple of 32)
-        unsigned long long x = tid < n ? w.key[tid] : ~0ull;
-        int slot = tid;
-        __syncthreads();
-        for (int k = 2; k <= n2; k <<= 1) {
-            for (int j = k >> 1; j > 0; j >>= 1) {
-                unsigned long long y;
-                int ys;
-                if (j >= 32) {
-                    if (act) {
-                        w.skey[tid] = x;
-                        w.lw[tid] = __int_as_float(slot);
-                    }
-                    __syncthreads();
-                    if (act) {
-                        y = w.skey[tid ^ j];
-                        ys = __float_as_int(w.lw[tid ^ j]);
-                    }
-                    __syncthreads();
-                } else if (act) {
-                    y = __shfl_xor_sync(0xFFFFFFFFu, x, j);
-                    ys = __shfl_xor_sync(0xFFFFFFFFu, slot, j);
-                }
-                if (act) {
-                    const bool keep_min = ((tid & j) == 0) == ((tid & k) == 0);
-                    if ((y < x) == keep_min) {
-                        x = y;
-                        slot = ys;
-                    }
+        const int runs = n2 / 32;
+        const bool wact = warp < runs;
+        unsigned long long x = ~0ull;
+        if (tid < n) x = (w.key[tid] & 0xFFFFFFFF00000000ull) | (unsigned)tid;
+        if (wact) {
+#pragma unroll
+            for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+                for (int j = k >> 1; j > 0; j >>= 1) {
+                    const unsigned long long y = __shfl_xor_sync(0xFFFFFFFFu, x, j);
+                    const bool keep_min = ((lane & j) == 0) == ((lane & k) == 0);
+                    if ((y < x) == keep_min) x = y;
                 }
             }
+            w.skey[tid] = x;  // run `warp`, ascending
         }
-        if (tid < n) {
-            w.skey[tid] = x;
+        __syncthreads();
+        if (wact && x != ~0ull) {
+            int rank = lane;
+            for (int rr = 0; rr < runs; ++rr) {
+                if (rr == warp) continue;
+                const unsigned long long* run = w.skey + rr * 32;
+                int pos = 0;
 #pragma unroll
-            for (int k = 0; k < 3; ++k) w.c[k][tid] = w.cu[k][slot];
-            w.lw[tid] = w.lwu[slot];
+                for (int st = 16; st; st >>= 1)
+                    if (run[pos + st - 1] < x) pos += st;
+                pos += run[pos] < x ? 1 : 0;
+                rank += pos;
+            }
+            const int slot = (int)(uint32_t)x;
+#pragma unroll
+            for (int k = 0; k < 3; ++k) w.c[k][rank] = w.cu[k][slot];
+            w.lw[rank] = w.lwu[slot];
             if ((uint32_t)(x >> 32) < 0x80000000u) atomicAdd(&t.nA, 1);
         }
     } else {
@@ -1178,8 +1175,8 @@ SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<
     }
     if (tid == 0) t.n = n;
     __syncthreads();
-    // the window's values in sorted order (already placed by the register
-    // sort; after the shared-memory sort, recomputed exactly as in pass 1)
+    // the window's values in sorted order (already placed by the run sort;
+    // after the shared-memory sort, recomputed exactly as in pass 1)
     for (int s = tid; n > NT && s < n; s += NT) {
         const int idx = (int)(uint32_t)w.skey[s];
         float q, pp, l;
