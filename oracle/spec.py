@@ -4,7 +4,7 @@ TEST INFRASTRUCTURE (see the package docstring): a plain, slow CPU oracle.
 Every function cites the passage it follows. Vectorised over the batch with
 numpy; loops run over draft positions, tree nodes and mentor rows only.
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
 
 * q is the target distribution, p the draft one ([SpS], [Mentor]); the
   [SD] write-up swaps the letters and is rewritten into this notation.

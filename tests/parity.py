@@ -1,6 +1,6 @@
 """Comparison helpers for the GPU parity tests (no verification arithmetic here).
 
-The spec bar: integer outputs (accepted counts, emitted tokens, tree
+The bar: integer outputs (accepted counts, emitted tokens, tree
 paths, argmax indices) match the oracle exactly, except decisions the oracle
 flags as near-ties (a uniform within 1e-5 of the acceptance ratio or of a CDF
 boundary, a top-p mass within 1e-5 of top_p, a mentor KL within 1e-5 * D of
