@@ -111,10 +111,11 @@ def test_mentor_bound_zero_equals_standard_verification():
         np.testing.assert_array_equal(np_(m[k]), np_(v[k]))
 
 
-@pytest.mark.parametrize("V,iters", [(3, 30), (100, 30), (5000, 12), (40001, 30), (40000, 30)])
+@pytest.mark.parametrize("V,iters", [(3, 30), (100, 30), (5000, 12), (40001, 30), (40000, 30), (262144, 30)])
 def test_mentor_shapes(V, iters):
     """Small and odd vocabularies; above 32768 entries the pass-1 bucket ids
-    live in global scratch (40001: scalar accesses, 40000: 16-byte ones)."""
+    live in global scratch (40001: scalar accesses, 40000: 16-byte ones);
+    262144 is the largest vocabulary the boundary accepts."""
     zt, zd = workloads.linear_logits(12, 3, V, V, sd_t=2.0, sd_d=1.2)
     _mentor(zt, zd, 0.05, seed=V, iters=iters, label=f"mentor V={V}")
 
