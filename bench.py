@@ -434,7 +434,9 @@ def main():
         acc_mean = float(out["accepted"].float().mean().item())
     elif "accept_len" in out:
         acc_mean = float(out["accept_len"].float().mean().item())
-    alpha_est = float(out["beta"].float().mean().item()) if "beta" in out else None
+    # alpha = E(beta) for the acceptance-rate workload only (the mentor's
+    # "beta" output is its resampling constant, NaN at undecided positions)
+    alpha_est = float(out["beta"].float().mean().item()) if inp.get("op") == "alpha" else None
 
     e2e = None
     if not args.no_e2e:
