@@ -340,10 +340,17 @@ spec_status spec_philox_uniform(uint64_t seed, uint64_t row0, uint32_t position,
  * than that (spec_verify_workspace_size(B, gamma, V, dtype) >
  * SPEC_NOALLOC_SCRATCH_BYTES). It never calls cudaMalloc, cudaFree or any
  * allocating routine. The first call on a device looks the array's device
- * address up (cudaGetSymbolAddress) and should be made before any stream
- * capture. All calls share the array and it keeps the last call's contents
- * (each call clears what must start at zero); calls that overlap on the GPU
- * race on it.
+ * address up (cudaGetSymbolAddress) and caches it for that device. With
+ * CUDA's lazy module loading (the default since CUDA 12.2) that first call is
+ * also the moment the array's module is loaded and its
+ * SPEC_NOALLOC_SCRATCH_BYTES of device memory are committed, so a caller with
+ * a fixed device budget should make one call per device at start-up, before
+ * any stream capture; later calls take no device memory. The cached address
+ * belongs to the device's current context: resetting the device
+ * (cudaDeviceReset, or destroying the primary context) after the first call
+ * is not supported. All calls share the array and it keeps the last call's
+ * contents (each call clears what must start at zero); calls that overlap on
+ * the GPU race on it.
  * ---------------------------------------------------------------------- */
 enum { SPEC_NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024 };
 

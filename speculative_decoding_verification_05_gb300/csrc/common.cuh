@@ -151,52 +151,6 @@ SV_DEV uint4 ld_stream_v4(const uint4* p) {
 }
 
 // ---------------------------------------------------------------------------
-// mbarrier + bulk asynchronous copy (TMA engine, non-tensor form).
-// ---------------------------------------------------------------------------
-SV_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-SV_DEV void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
-                 : "memory");
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-SV_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-SV_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait for phase `parity`; returns false if it gave up after `limit` polls.
-SV_DEV bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t limit) {
-    for (uint32_t it = 0; it < limit; ++it)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
-}
-
-// global -> own shared memory, `bytes` a multiple of 16, both addresses 16-byte aligned.
-SV_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// ---------------------------------------------------------------------------
 // Warp reductions.
 // ---------------------------------------------------------------------------
 SV_DEV float warp_max(float v) {
@@ -333,6 +287,7 @@ struct MentorParams {
     unsigned int* rejmark;  // [B]: max over rejected positions k of gamma - k (zero at launch)
     int32_t* pos_state;   // [B, gamma]: outcome of each solved position
     float* pos_beta;      // [B, gamma]: beta of each solved position
+    float* pos_scale;     // [B, gamma, 2]: the solve's normalised 1/S_t and 1/S_d
     int32_t* accepted;
     int32_t* tokens;
     int32_t* next_token;

@@ -38,7 +38,11 @@ void* g_scratch_ptr[kMaxDevices] = {nullptr};
 
 // Device address of the scratch array on the current device, looked up once
 // per device with that device current. In host code the array's name is only
-// a host-side stand-in; the kernels must be given this address.
+// a host-side stand-in; the kernels must be given this address. Under lazy
+// module loading the lookup is also what loads this file's module and commits
+// the array's memory, so the first call belongs at start-up. The address is
+// cached for the life of the process: a device reset after the first call
+// would leave it stale, and is not supported.
 spec_status scratch_address(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -59,8 +59,8 @@ def test_nucleus_config(sigma):
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("T,top_p,top_k", [(1.0, 1.0, 0), (0.7, 1.0, 50), (1.0, 0.9, 0),
                                            (1.0, 0.8, 200), (0.5, 0.5, 3), (1.0, 1.0, 1)])
-def test_transforms_ragged_vocab_across_a_cluster(dtype, T, top_p, top_k):
-    """V=40001 (odd: rows start off the 16-byte grid; the vocab splits over a cluster)."""
+def test_transforms_ragged_vocab(dtype, T, top_p, top_k):
+    """V=40001 (odd: rows start off the 16-byte grid and end in a ragged tail)."""
     zt, zd = workloads.linear_logits(24, 3, 40001, 11, dtype=dtype, sd_t=3.0, sd_d=0.8)
     run(zt, zd, T, top_p, top_k, seed=5, offset=1000, label=f"{dtype} T={T} p={top_p} k={top_k}",
         max_near=0.5)

@@ -27,15 +27,20 @@ pytestmark = pytest.mark.gpu
 SCRATCH_BYTES = 4 * 1024 * 1024
 
 
-def _noalloc(lib, zt, zd, drafts, T, top_p, top_k, seed, offset):
+def _outputs(B, gamma, dev):
+    return {"accepted": torch.full((B,), -7, dtype=torch.int32, device=dev),
+            "tokens": torch.full((B, gamma + 1), -7, dtype=torch.int32, device=dev),
+            "next_token": torch.full((B,), -7, dtype=torch.int32, device=dev),
+            "status": torch.full((B,), -7, dtype=torch.int32, device=dev),
+            "probs": torch.full((B, gamma, 2), -7.0, dtype=torch.float32, device=dev)}
+
+
+def _noalloc(lib, zt, zd, drafts, T, top_p, top_k, seed, offset, out=None):
     B, G1, V = zt.shape
     gamma = G1 - 1
     dev = zt.device
-    out = {"accepted": torch.full((B,), -7, dtype=torch.int32, device=dev),
-           "tokens": torch.full((B, G1), -7, dtype=torch.int32, device=dev),
-           "next_token": torch.full((B,), -7, dtype=torch.int32, device=dev),
-           "status": torch.full((B,), -7, dtype=torch.int32, device=dev),
-           "probs": torch.full((B, gamma, 2), -7.0, dtype=torch.float32, device=dev)}
+    if out is None:
+        out = _outputs(B, gamma, dev)
     p = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
     dt = sv.SPEC_F32 if zt.dtype == torch.float32 else sv.SPEC_BF16
     stream = torch.cuda.current_stream(dev)
@@ -63,6 +68,23 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(dtype, V, T, top_p, 
         for k in ("accepted", "tokens", "next_token", "status"):
             np.testing.assert_array_equal(got[k].cpu().numpy(), ref[k].cpu().numpy(), err_msg=k)
         np.testing.assert_allclose(got["probs"].cpu().numpy(), ref["probs"].cpu().numpy(), rtol=1e-5, atol=0)
+
+
+def test_noalloc_takes_no_device_memory_after_its_first_call():
+    """The first call on a device may load the scratch array's module (and
+    commit its memory); every later call must leave the device's free memory
+    unchanged. Outputs are allocated before the calls, so nothing else
+    allocates in between."""
+    lib = sv.load_library()
+    zt, zd = workloads.linear_logits(8, 4, 32000, 77, dtype="bf16", sd_t=3.0, sd_d=0.8)
+    drafts = torch.from_numpy(oracle.sample(zd, 0.8, 0.95, 0, seed=3)["tokens"]).int().cuda()
+    zt, zd = zt.cuda(), zd.cuda()
+    out = _outputs(8, 4, zt.device)
+    _noalloc(lib, zt, zd, drafts, 0.8, 0.95, 0, 1, 0, out)
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        _noalloc(lib, zt, zd, drafts, 0.8, 0.95, 0, 1, 0, out)
+        assert torch.cuda.mem_get_info()[0] == free0
 
 
 def test_noalloc_rejects_calls_beyond_its_scratch():
