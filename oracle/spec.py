@@ -38,10 +38,6 @@ NEAR_TIE = 1e-5
 # accurate to a few 1e-7; a 1e-5 band would flag most rows of a large flat
 # nucleus, where single tokens carry ~1e-5 of the mass.
 THRESH_NEAR = 2e-6
-# Absolute floor of the KL comparison band in the mentor bisection: the fp32
-# rounding of a prefix sum of ~3e4 terms q ln(q/p) of size <= 1 (hierarchical
-# summation, about 1e-6) with margin.
-KL_ABS_TOL = 2e-6
 STATUS_OK = 0
 STATUS_EDATA = 4
 
@@ -453,16 +449,18 @@ def mentor_solve(q, p, kl_bound, iters=30):
     Returns dict(alpha, beta, alpha_lo, beta_lo, alpha_hi, beta_hi, kl0,
     shortcut, near): shortcut when KL(q || p) <= D (fast path of the same
     section: accept directly); near when KL(q||p) lies within
-    band = NEAR_TIE * D + KL_ABS_TOL of D. [alpha_lo, alpha_hi] are the
-    bisection results for the bounds D + band and D - band: every result a
-    bisection can reach when each KL evaluation is off by at most band (the
-    last steps of a bisection always sit inside the band, so the admissible
-    answers form this range rather than one value).
+    band = NEAR_TIE * D of D. [alpha_lo, alpha_hi] are the bisection results
+    for the bounds D + band and D - band: every result a bisection can reach
+    when each KL evaluation is off by at most band (the last steps of a
+    bisection always sit inside the band, so the admissible answers form this
+    range rather than one value). Where the range is narrower than
+    NEAR_TIE * alpha, alpha itself is decided to that relative tolerance;
+    where it is wider (KL nearly flat at the crossing), alpha is a near-tie.
     """
     q = np.asarray(q, dtype=np.float64)
     p = np.asarray(p, dtype=np.float64)
     D = float(kl_bound)
-    band = NEAR_TIE * D + KL_ABS_TOL
+    band = NEAR_TIE * D
     with np.errstate(divide="ignore", invalid="ignore"):
         rho = np.where(p > 0, q / np.where(p > 0, p, 1.0), np.where(q > 0, np.inf, 0.0))
         qlr = np.where(q > 0, q * np.log(np.where(q > 0, rho, 1.0)), 0.0)

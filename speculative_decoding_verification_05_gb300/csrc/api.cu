@@ -121,7 +121,7 @@ constexpr int kMentorSlots = 152;
 
 struct MentorWs {
     Ws lin;
-    size_t keys, idx, arr, pos_state, pos_beta, total;
+    size_t keys, idx, arr, pos_state, pos_beta, pos_scale, total;
     int slots;
 };
 
@@ -140,6 +140,8 @@ MentorWs mentor_ws(int B, int gamma, int V) {
     o = al(o + (size_t)B * gamma * 4);
     w.pos_beta = o;
     o = al(o + (size_t)B * gamma * 4);
+    w.pos_scale = o;
+    o = al(o + (size_t)B * gamma * 8);
     w.total = o;
     return w;
 }
@@ -480,6 +482,7 @@ spec_status spec_verify_mentor(const void* target, const void* draft, spec_dtype
     m.rejmark = at<unsigned int>(workspace, w.lin.seq_cnt);
     m.pos_state = at<int32_t>(workspace, w.pos_state);
     m.pos_beta = at<float>(workspace, w.pos_beta);
+    m.pos_scale = at<float>(workspace, w.pos_scale);
     m.accepted = accepted;
     m.tokens = tokens;
     m.next_token = next_token;

@@ -90,17 +90,23 @@ struct Row {
     const E* rd;
     float mtc, mdc;    // m * c2
     float c2, inv_t;
-    float iSt, iSd;    // 1 / S
-    float lnr0;        // -(m_t - m_d)/T - ln S_t + ln S_d
+    float iSt, iSd;    // 1 / S, then corrected by the normalisation pass
+    float lnr0, lnr0_lo;  // ln(iSt / iSd) as a sum of two floats
 };
 
-// q, p and ln(q/p) of one index from its two logits. The rounding of every
-// step is pinned, so that the passes that recompute an index agree bit for bit.
+constexpr float kLn2 = 0.69314718055994531f;
+
+// q, p and ln(q/p) of one index from its two logits: with a = z c2 - m c2
+// (octaves below the maximum) q = 2^a_t iSt, p = 2^a_d iSd and
+// ln(q/p) = ln 2 (a_t - a_d) + ln(iSt / iSd), so ln(q/p) is formed from the
+// same exponents as q and p. The rounding of every step is pinned, so that
+// the passes that recompute an index agree bit for bit.
 template <typename E>
 SV_DEV void qpl_of(const Row<E>& r, float zt, float zd, float& q, float& p, float& l) {
-    q = __fmul_rn(ex2(__fmaf_rn(zt, r.c2, -r.mtc)), r.iSt);
-    p = __fmul_rn(ex2(__fmaf_rn(zd, r.c2, -r.mdc)), r.iSd);
-    l = __fmaf_rn(__fsub_rn(zt, zd), r.inv_t, r.lnr0);
+    const float at = __fmaf_rn(zt, r.c2, -r.mtc), ad = __fmaf_rn(zd, r.c2, -r.mdc);
+    q = __fmul_rn(ex2(at), r.iSt);
+    p = __fmul_rn(ex2(ad), r.iSd);
+    l = __fadd_rn(__fmaf_rn(__fsub_rn(at, ad), kLn2, r.lnr0), r.lnr0_lo);
 }
 
 template <typename E>
@@ -1287,6 +1293,90 @@ SV_DEV double sort_pass(SmallM& t, const Row<E>& r, int V, uint32_t* k0, uint32_
     return block_sum_d(t, (double)acc_kl);
 }
 
+// Normalisation pass over the row pair, before a solve: the exact
+// fixed-point totals of q and p as every later pass computes them (q, p in
+// units of 2^-44, the histogram's units), then iSt and iSd are rescaled so
+// that both totals are one, and ln(iSt / iSd) is formed in double from the
+// rescaled floats. The rows' normalisers S come from fp32 sums and the
+// rounding of m c2, which leave a common relative error of order 1e-7 to
+// 1e-6 in every q and p; the bisection's alpha moves with such an error
+// about ten times as much (the KL bound is met at a slope of order D), so
+// the solve works with sums that are exact for the values it uses.
+template <typename E>
+SV_DEV void normalise(SmallM& t, Row<E>& r, int V) {
+    constexpr int kN = VecTraits<E>::kN;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    unsigned long long sq = 0ull, sp = 0ull;
+    const auto add = [&](float zt, float zd) {
+        const float q = __fmul_rn(ex2(__fmaf_rn(zt, r.c2, -r.mtc)), r.iSt);
+        const float p = __fmul_rn(ex2(__fmaf_rn(zd, r.c2, -r.mdc)), r.iSd);
+        if (q > 0.f) {
+            const Fix2 f = fix2(q, kQF);
+            sq += ((unsigned long long)f.hi << 32) | f.lo;
+        }
+        if (p > 0.f) {
+            const Fix2 f = fix2(p, kQF);
+            sp += ((unsigned long long)f.hi << 32) | f.lo;
+        }
+    };
+    int tail = 0;
+    if (((reinterpret_cast<uintptr_t>(r.rt) | reinterpret_cast<uintptr_t>(r.rd)) & 15u) == 0) {
+        const int nv = V / kN;
+        const uint4* vt = reinterpret_cast<const uint4*>(r.rt);
+        const uint4* vd = reinterpret_cast<const uint4*>(r.rd);
+        for (int v = tid; v < nv; v += 2 * NT) {
+            const bool two = v + NT < nv;
+            const uint4 a0 = __ldg(vt + v), b0 = __ldg(vd + v);
+            const uint4 a1 = two ? __ldg(vt + v + NT) : a0, b1 = two ? __ldg(vd + v + NT) : b0;
+            float x[kN], y[kN];
+            VecTraits<E>::unpack(a0, x);
+            VecTraits<E>::unpack(b0, y);
+#pragma unroll
+            for (int u = 0; u < kN; ++u) add(x[u], y[u]);
+            if (two) {
+                VecTraits<E>::unpack(a1, x);
+                VecTraits<E>::unpack(b1, y);
+#pragma unroll
+                for (int u = 0; u < kN; ++u) add(x[u], y[u]);
+            }
+        }
+        tail = nv * kN;
+    }
+    for (int i = tail + tid; i < V; i += NT) add(VecTraits<E>::load1(r.rt + i), VecTraits<E>::load1(r.rd + i));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
+        sp += __shfl_xor_sync(0xFFFFFFFFu, sp, o);
+    }
+    if (lane == 0) {
+        t.wtot[0][warp] = (long long)sq;
+        t.wtot[1][warp] = (long long)sp;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        unsigned long long Q = 0ull, P = 0ull;
+        for (int w = 0; w < NW; ++w) {
+            Q += (unsigned long long)t.wtot[0][w];
+            P += (unsigned long long)t.wtot[1][w];
+        }
+        // both totals are positive (the row maximum has q = 1/S > 0)
+        const float ist = Q ? (float)((double)r.iSt * 0x1p44 / (double)Q) : r.iSt;
+        const float isd = P ? (float)((double)r.iSd * 0x1p44 / (double)P) : r.iSd;
+        const double l0 = log((double)ist) - log((double)isd);
+        const float hi = (float)l0;
+        t.bd[0] = (double)ist;
+        t.bd[1] = (double)isd;
+        t.bd[2] = (double)hi;
+        t.bd[3] = (double)(float)(l0 - (double)hi);
+    }
+    __syncthreads();
+    r.iSt = (float)t.bd[0];
+    r.iSd = (float)t.bd[1];
+    r.lnr0 = (float)t.bd[2];
+    r.lnr0_lo = (float)t.bd[3];
+    __syncthreads();
+}
+
 // Position states left for the resolve kernel.
 constexpr int kPosAccepted = 1;
 constexpr int kPosRejected = 0;        // rejected by the standard test (alpha = 1, beta = 1)
@@ -1349,6 +1439,7 @@ __global__ void __launch_bounds__(NT, 1) mentor_kernel(const __grid_constant__ M
         const float u = uniform01(p.seed, p.offset + (uint64_t)b, (uint32_t)k, kPurposeAccept);
         float alpha = -1.f, beta = 0.f;
         int state = accept_test(u, q, pd) ? kPosAccepted : kPosRejected;
+        float iS[2] = {1.f / t.S, 1.f / d.S};
         if (state != kPosAccepted) {
             Row<E> r;
             r.rt = tgt + ((size_t)b * G1 + k) * V;
@@ -1359,7 +1450,9 @@ __global__ void __launch_bounds__(NT, 1) mentor_kernel(const __grid_constant__ M
             r.mdc = d.m * c2;
             r.iSt = 1.f / t.S;
             r.iSd = 1.f / d.S;
-            r.lnr0 = -(t.m - d.m) * p.inv_t - logf(t.S) + logf(d.S);
+            normalise<E>(sm, r, V);
+            iS[0] = r.iSt;
+            iS[1] = r.iSd;
             // KL(q || p) from the histogram pass (exact sum of the fp32 terms)
             if (V <= kIdsSmem) hist_pass<E>(sh.h, sm, r, V, sh.h.ids); else hist_pass<E>(sh.h, sm, r, V, ids);
             scan_hist(sh.h, sm);
@@ -1397,6 +1490,8 @@ __global__ void __launch_bounds__(NT, 1) mentor_kernel(const __grid_constant__ M
             if (p.alpha_out) p.alpha_out[pos] = alpha;
             if (p.beta_out) p.beta_out[pos] = beta;
             p.pos_beta[pos] = beta;
+            p.pos_scale[2 * pos] = iS[0];
+            p.pos_scale[2 * pos + 1] = iS[1];
             p.pos_state[pos] = state;
             if (state != kPosAccepted) atomicMax(p.rejmark + b, (unsigned)(G - k));
         }
@@ -1448,9 +1543,12 @@ __global__ void __launch_bounds__(kDrawNT) mentor_resolve_kernel(const __grid_co
                 if (st == kPosRejected) {
                     tok = draw_residual<E, draw_vec<E>()>(ds, rt, rd, V, t, d, c2, u2);
                 } else {
+                    // max(0, q/beta - p) with the q and p the solve normalised
                     const float beta = __ldcg(p.pos_beta + (size_t)b * G + n);
-                    const ResidualW w{KeptExp{t.thr, c2, t.m * c2, (1.f / t.S) * (1.f / beta)},
-                                      KeptExp{d.thr, c2, d.m * c2, 1.f / d.S}};
+                    const float ist = __ldcg(p.pos_scale + 2 * ((size_t)b * G + n));
+                    const float isd = __ldcg(p.pos_scale + 2 * ((size_t)b * G + n) + 1);
+                    const ResidualW w{KeptExp{t.thr, c2, t.m * c2, ist * (1.f / beta)},
+                                      KeptExp{d.thr, c2, d.m * c2, isd}};
                     float W;
                     tok = block_draw<E, ResidualW, draw_vec<E>()>(ds, rt, rd, V, u2, w, &W);
                     if (!(W > 0.f)) tok = draw_q<E, draw_vec<E>()>(ds, rt, V, t, c2, u2);

@@ -12,6 +12,18 @@ import numpy as np
 import torch
 
 PROB_RTOL = 1e-5
+ALPHA_RTOL = 1e-5   # mentor alpha, relative
+BETA_RTOL = 1e-5    # acceptance probabilities beta = sum min(q, p), relative
+
+# Counts of the decisions each parity test excluded or accepted as equally
+# valid, by test label (reported at the end of the session by conftest.py).
+NEAR_TIES = {}
+
+
+def record(label, **counts):
+    e = NEAR_TIES.setdefault(label, {})
+    for k, v in counts.items():
+        e[k] = e.get(k, 0) + int(v)
 
 
 def np_(t):
@@ -43,8 +55,37 @@ def assert_linear_parity(g, r, max_near_frac=0.05, label=""):
             f"gpu acc {acc[i].tolist()} ref {r['accepted'][i].tolist()}, "
             f"gpu next {nxt[i].tolist()} ref {r['next_token'][i].tolist()} alt {alt[i].tolist()}")
     near = int(r["near_tie"].sum())
+    record(label, sequences=len(acc), near_ties=near, alt_tokens=int(use_alt[ok].sum()),
+           threshold_near=int(r["prob_near"].any(axis=1).sum()) if "prob_near" in r else 0)
     assert near <= max(2, max_near_frac * len(acc)), f"{label}: {near} near-ties of {len(acc)}"
     return near
+
+
+def assert_mentor_alpha(g_alpha, r, label=""):
+    """Mentor alpha at the decided positions (k <= accepted) of rows without a
+    near-tie: the standard-test (-1) and shortcut (0) codes exactly; every
+    bisection result within ALPHA_RTOL of the oracle's, except where the
+    oracle's admissible range [alpha_lo, alpha_hi] (bisections whose KL
+    evaluations are all off by 1e-5 D) is itself wider than ALPHA_RTOL: such
+    an alpha is a near-tie, counted and held to that range (widened by
+    ALPHA_RTOL)."""
+    ga = np_(g_alpha).astype(np.float64)
+    gamma = ga.shape[1]
+    dec = (np.arange(gamma)[None, :] <= np.minimum(r["accepted"], gamma - 1)[:, None])
+    dec &= ~r["near_tie"][:, None] & (r["status"][:, None] == 0) & ~np.isnan(r["alpha"])
+    code = dec & (r["alpha"] <= 0)
+    np.testing.assert_array_equal(ga[code], r["alpha"][code], err_msg=f"{label} alpha codes")
+    sol = dec & (r["alpha"] > 0)
+    a, ra, lo, hi = ga[sol], r["alpha"][sol], r["alpha_lo"][sol], r["alpha_hi"][sol]
+    wide = (hi - lo) > ALPHA_RTOL * ra
+    rel = np.abs(a - ra) / ra
+    bad = ~wide & (rel > ALPHA_RTOL)
+    assert not bad.any(), (f"{label}: {bad.sum()} of {sol.sum()} alphas off by more than {ALPHA_RTOL} relative "
+                           f"(worst {rel[~wide].max():.3g})")
+    inside = (a >= lo * (1 - ALPHA_RTOL)) & (a <= hi * (1 + ALPHA_RTOL))
+    assert inside[wide].all(), f"{label}: alpha near-ties outside their admissible range"
+    record(label, alphas_solved=int(sol.sum()), alpha_near_ties=int(wide.sum()))
+    return float(rel[~wide].max()) if (~wide).any() else 0.0
 
 
 def assert_probs(g_probs, r, label=""):

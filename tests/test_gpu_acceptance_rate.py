@@ -2,11 +2,12 @@
 every target / draft row pair under the verification transforms.
 
 [SD] "Fast Inference from Transformers via Speculative Decoding", section
-"方法细节" (接受率精确刻画). fp32 sums of at most V terms in [0, 1]: the
-tolerance is 2e-5 absolute (the kernel's exponentials are within 2^-21 of the
-exact ones; the sums add up to V rounding errors of about 2^-24 each). Rows
-whose top-p crossing is a near-tie (the oracle's flag) are left out, as in the
-verification parity tests.
+"方法细节" (接受率精确刻画). beta is a probability, held to the parity
+tolerance of probabilities: 1e-5 relative (fp32 sums of at most V terms in
+[0, 1]; the kernel's exponentials are within about 2^-22 of the exact ones and
+the sums' rounding errors partly cancel). Rows whose top-p crossing is a
+near-tie (the oracle's flag) are left out and counted, as in the verification
+parity tests.
 """
 
 import numpy as np
@@ -16,9 +17,10 @@ import torch
 import oracle
 import speculative_decoding_verification_05_gb300 as sv
 import workloads
+from parity import BETA_RTOL, record
 
 pytestmark = pytest.mark.gpu
-TOL = 2e-5
+RTOL = BETA_RTOL
 
 
 def _oracle_beta(zt, zd, T, top_k, top_p):
@@ -46,10 +48,12 @@ def test_beta_matches_oracle(case):
     got = r["beta"].cpu().numpy()
     assert (r["status"].cpu().numpy() == 0).all()
     ok = ~near
+    record(f"beta {case['dtype']} V={case['V']} T={case['T']} k={case['k']} p={case['p']}",
+           positions=near.size, near_ties=int(near.sum()))
     assert ok.mean() > 0.8
-    np.testing.assert_allclose(got[ok], want[ok], rtol=0, atol=TOL)
+    np.testing.assert_allclose(got[ok], want[ok], rtol=RTOL, atol=0)
     # alpha as the mean of beta
-    assert abs(got[ok].mean() - oracle.estimate_alpha(want[ok])) < TOL
+    assert abs(got[ok].mean() - oracle.estimate_alpha(want[ok])) <= RTOL * oracle.estimate_alpha(want[ok])
 
 
 def test_full_size_batch_sampled_and_properties():
@@ -59,15 +63,16 @@ def test_full_size_batch_sampled_and_properties():
     r = sv.acceptance_rate(zt, zd, 0.8, 0.95, 0)
     beta = r["beta"].cpu().numpy()
     assert beta.shape == (8000, 4) and (r["status"].cpu().numpy() == 0).all()
-    assert np.isfinite(beta).all() and (beta >= -TOL).all() and (beta <= 1 + TOL).all()
+    assert np.isfinite(beta).all() and (beta >= 0).all() and (beta <= 1 + RTOL).all()
     rng = np.random.default_rng(1)
     for b in rng.choice(8000, 6, replace=False):
         want, near = _oracle_beta(zt[b:b + 1].float().cpu().numpy(), zd[b:b + 1].float().cpu().numpy(),
                                   0.8, 0, 0.95)
         ok = ~near[0]
-        np.testing.assert_allclose(beta[b][ok], want[0][ok], rtol=0, atol=TOL)
+        record("beta nucleus x1000 (sampled)", positions=near[0].size, near_ties=int(near[0].sum()))
+        np.testing.assert_allclose(beta[b][ok], want[0][ok], rtol=RTOL, atol=0)
     same = sv.acceptance_rate(zt[:64], zt[:64, :4].contiguous(), 0.8, 0.95, 0)["beta"]
-    np.testing.assert_allclose(same.cpu().numpy(), 1.0, rtol=0, atol=TOL)
+    np.testing.assert_allclose(same.cpu().numpy(), 1.0, rtol=RTOL, atol=0)
 
 
 def test_bad_rows_and_host_buffers():
@@ -79,4 +84,4 @@ def test_bad_rows_and_host_buffers():
     beta = r["beta"].numpy()
     assert np.isnan(beta[1, 0]) and np.isfinite(beta[1, 1])
     want, _ = _oracle_beta(zt.numpy()[[0, 2]], zd.numpy()[[0, 2]], 1.0, 0, 1.0)
-    np.testing.assert_allclose(beta[[0, 2]], want, rtol=0, atol=TOL)
+    np.testing.assert_allclose(beta[[0, 2]], want, rtol=RTOL, atol=0)

@@ -11,7 +11,7 @@ import torch
 import oracle
 import speculative_decoding_verification_05_gb300 as sv
 import workloads
-from parity import assert_linear_parity, assert_probs, np_
+from parity import assert_linear_parity, assert_mentor_alpha, assert_probs, np_
 
 pytestmark = pytest.mark.gpu
 
@@ -65,6 +65,7 @@ def test_mentor_12_steps_in_one_call():
     gs = _take(g, idx)
     assert_linear_parity(gs, r, max_near_frac=0.25, label="mentor x12")
     assert_probs(gs["probs"], r, "mentor x12")
+    assert_mentor_alpha(gs["alpha"], r, "mentor x12")
     assert ((r["alpha"] > 0) & (r["alpha"] < 1)).any(), "no sampled position reached the solver"
 
 
