@@ -2,22 +2,28 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
-One bench step is one pass of the whole verification path over one batch:
-for the default workload ("nucleus": B=8, gamma=4, V=32000, bf16, T=0.8,
-top_p=0.95, 1000 steps) the 1000 verification steps are issued as one call
-over 8000 sequences (offset = step * B, so every Philox counter is the one a
-step-by-step loop would use). Inputs (4.6 GB) are resident in HBM and larger
-than L2, so no flush is needed between timed steps; workloads smaller than
-twice L2 (tiny) overwrite a 256 MB buffer before each timed step, outside
-the timed events. ``--stack S`` overrides the number of stacked steps (a
-smaller case of the same workload, used for ncu captures).
+One bench step is one pass of the whole verification path over one batch. The
+default workload is the large-vocabulary configuration (B=64, gamma=7,
+V=128256, f32 logits, temperature 1): 20 of its 200 steps are stacked into
+one call over 1280 sequences (offset = step * B, so every Philox counter is
+the one a step-by-step loop would use), 9.85 GB of logits resident in HBM,
+larger than L2, so no flush is needed between timed steps. Workloads smaller
+than twice L2 (tiny) overwrite a 256 MB buffer before each timed step,
+outside the timed events. ``--stack S`` overrides the number of stacked
+steps (a smaller case of the same workload, used for ncu captures).
+
+The same run also times the other V >= 32k workloads (nucleus x1000 steps,
+large-vocab at temperature 0, the tree workload, the mentor workload) and
+reports each under ``per_workload`` with its own roofline and clocks
+(``--no-extra`` skips them).
 
 Prints one JSON line: verified positions/s (whole job), the roofline of the
-dominant kernel (algorithmic bytes / CUDA-event time against the measured HBM
-copy bandwidth), the CPU oracle baseline, the end-to-end figure through the
-public API with host buffers, launch count and SM clocks during the run.
-Under torchrun (N > 1) every rank runs an independent replica (the path
-shards by sequence with no exchange), and rank 0 reports the aggregate.
+timed call (algorithmic bytes / CUDA-event time against the measured HBM copy
+bandwidth), the CPU oracle baseline (one core and every host core), the
+end-to-end figure through the public API with host buffers, launch count and
+SM clocks during the run. Under torchrun (N > 1) every rank runs an
+independent replica (the path shards by sequence with no exchange), and rank 0
+reports the aggregate.
 """
 
 import argparse
@@ -42,16 +48,19 @@ UNIT = "positions/s"
 
 WORKLOADS = {
     # name: (config, steps stacked into one call, temperature override)
+    "large_vocab": ("large_vocab", 20, 1.0),
+    "large_vocab_t0": ("large_vocab", 20, 0.0),
     "nucleus": ("nucleus", 1000, None),
+    "tree": ("tree", 32, None),
+    "mentor": ("mentor", 250, None),
     "tiny": ("tiny", 64, None),
-    "large_vocab": ("large_vocab", 1, 1.0),
-    "large_vocab_t0": ("large_vocab", 1, 0.0),
-    "tree": ("tree", 4, None),
-    "mentor": ("mentor", 12, None),
     "rest": ("rest", 4, None),
     "nucleus_lenient": ("nucleus", 1000, None),
     "nucleus_alpha": ("nucleus", 1000, None),
 }
+DEFAULT = "large_vocab"
+# the other V >= 32k workloads, timed in the same run as the default one
+EXTRA = ("nucleus", "large_vocab_t0", "tree", "mentor")
 LENIENCE = {"nucleus_lenient": 0.5}   # lenient verification (l < 1); others are exact
 OPS = {"nucleus_alpha": "alpha"}      # measured acceptance probabilities instead of verification
 
@@ -105,15 +114,32 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def recorded_traffic(workload):
-    """Per-launch DRAM bytes of the dominant kernel from the committed ncu summary."""
+def kernel_sources_sha():
+    """Hash of the library's CUDA sources: a recorded ncu traffic figure holds
+    only for the kernels it was taken on."""
+    import hashlib
+
+    h = hashlib.sha256()
+    src = os.path.join(ROOT, "speculative_decoding_verification_05_gb300", "csrc")
+    for f in sorted(os.listdir(src)):
+        with open(os.path.join(src, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload, stacked):
+    """Per-launch DRAM bytes (read + write) of the timed call from the committed
+    ncu summary, or None: none recorded, another stacking, or kernels changed
+    since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     e = d.get(workload)
-    return None if e is None else e.get("bytes_per_launch")
+    if e is None or e.get("stacked") != stacked or e.get("csrc_sha16") != kernel_sources_sha():
+        return None
+    return e.get("bytes_per_launch")
 
 
 class ClockSampler:
@@ -266,94 +292,178 @@ def launches_per_step(inp):
     return 2
 
 
-def cpu_baseline(name, temperature, budget_s=12.0, lenience=1.0, op="verify"):
-    """The oracle, as it stands, on a bounded sample of the workload (host cores)."""
+def oracle_job(name, temperature, lenience=1.0, op="verify", seed=99):
+    """A bounded sample of the workload for the oracle: one step of the
+    configuration (two of its 64 sequences for the large vocabulary, whose
+    rows are 4x longer), as numpy arrays."""
     import oracle
 
     c = dict(workloads.CONFIGS[name])
     if op == "alpha":
-        B, G, V = c["B"], c["gamma"], c["V"]
-        zt, zd = workloads.config_logits(name, 99, steps=1)
-        zt, zd = zt.float().numpy(), zd.float().numpy()
-        T, tp = c["temperature"], c.get("top_p", 1.0)
-        t0 = time.perf_counter()
-        n = 0
-        while time.perf_counter() - t0 < budget_s:
-            q, _ = oracle.transformed_probs(zt[:, :G].reshape(-1, V), T, 0, tp)
-            p, _ = oracle.transformed_probs(zd.reshape(-1, V), T, 0, tp)
-            oracle.acceptance_rate(q, p)
-            n += 1
-        dt = time.perf_counter() - t0
-        return {"value": n * B * G / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-                "sample": f"{n} steps of B={B} ({n * B * G} positions' beta, V={V}) in {dt:.1f} s"}
+        zt, zd = workloads.config_logits(name, seed, steps=1)
+        return dict(kind="alpha", zt=zt.float().numpy(), zd=zd.float().numpy(), T=c["temperature"],
+                    top_p=c.get("top_p", 1.0)), f"beta of one step (B={c['B']}, V={c['V']})"
     if c["kind"] == "rest":
         B = c["B"]
-        cand = workloads.rest_candidates(B, c["C"], c["L"], c["V"], 99, bases=c["bases"], diverge=c["diverge"])
+        cand = workloads.rest_candidates(B, c["C"], c["L"], c["V"], seed, bases=c["bases"], diverge=c["diverge"])
         root = np.arange(B, dtype=np.int32)
         tr = oracle.rest_tree_batch(cand, None, root, c["N"], c["V"])
-        z = workloads.forced_tree_logits(tr["tokens"], tr["parent"], tr["n_nodes"], c["V"], 99, sd=c["sd"],
+        z = workloads.forced_tree_logits(tr["tokens"], tr["parent"], tr["n_nodes"], c["V"], seed, sd=c["sd"],
                                          force_p=c["force_p"])
-        t0 = time.perf_counter()
-        n = 0
-        while time.perf_counter() - t0 < budget_s:
-            t = oracle.rest_tree_batch(cand, None, root, c["N"], c["V"])
-            oracle.verify_tree(z, t["tokens"], t["parent"], t["depth"], c["L"])
-            n += 1
-        dt = time.perf_counter() - t0
-        return {"value": n * B * (c["N"] - 1) / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-                "sample": f"{n} REST steps of {B} sequences (C={c['C']}, L={c['L']}, N={c['N']}, "
-                          f"V={c['V']}) in {dt:.1f} s"}
-    T = c.get("temperature", 0.0) if temperature is None else temperature
+        return (dict(kind="rest", cand=cand, root=root, z=z.numpy() if hasattr(z, "numpy") else z, N=c["N"],
+                     V=c["V"], max_depth=c["L"]),
+                f"one REST step: {B} trees built (C={c['C']}, L={c['L']}, N={c['N']}) and verified (V={c['V']})")
     if c["kind"] == "tree":
-        B = c["B"]
-        z, tok, par, dep = workloads.tree_inputs(B, c["N"], c["V"], 99)
-        t0 = time.perf_counter()
-        n = 0
-        while time.perf_counter() - t0 < budget_s:
-            oracle.verify_tree(z, tok, par, dep, c["max_depth"])
-            n += 1
-        dt = time.perf_counter() - t0
-        pos = n * B * (c["N"] - 1)
-        return {"value": pos / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-                "sample": f"{n} calls of {B} trees (N={c['N']}, V={c['V']}) in {dt:.1f} s"}
-    B = c["B"]
-    zt, zd = workloads.config_logits(name, 99, steps=1)
+        z, tok, par, dep = workloads.tree_inputs(c["B"], c["N"], c["V"], seed)
+        return (dict(kind="tree", z=z.numpy(), tok=tok.numpy(), par=par.numpy(), dep=dep.numpy(),
+                     max_depth=c["max_depth"]), f"one step: {c['B']} trees (N={c['N']}, V={c['V']})")
+    T = c.get("temperature", 0.0) if temperature is None else temperature
+    B = 2 if name == "large_vocab" else c["B"]
+    zt, zd = workloads.linear_logits(B, c["gamma"], c["V"], seed, dtype=c["dtype"], sd_t=c["sd_t"],
+                                     sd_d=c["sd_d"], boost=c.get("boost", 0.0), boost_p=c.get("boost_p", 0.0),
+                                     zipf=c.get("zipf", 0.0))
     top_p = c.get("top_p", 1.0)
-    drafts = oracle.sample(zd, T, top_p, 0, seed=99)["tokens"]
-    t0 = time.perf_counter()
-    n = 0
-    while time.perf_counter() - t0 < budget_s:
-        if c["kind"] == "mentor":
-            oracle.verify_mentor(zt, zd, drafts, T, c["kl_bound"], c["iters"], seed=n, offset=n * B)
-        else:
-            oracle.verify(zt, zd if T > 0 else None, drafts, T, top_p, 0, seed=n, offset=n * B, lenience=lenience)
-        n += 1
-    dt = time.perf_counter() - t0
-    return {"value": n * B * c["gamma"] / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n} steps of B={B} ({n * B * c['gamma']} positions, V={c['V']}) in {dt:.1f} s"}
+    drafts = oracle.sample(zd, T, top_p, 0, seed=seed)["tokens"]
+    job = dict(kind="mentor" if c["kind"] == "mentor" else "verify", zt=zt.float().numpy(), zd=zd.float().numpy(),
+               drafts=drafts, T=T, top_p=top_p, lenience=lenience, kl_bound=c.get("kl_bound", 0.0),
+               iters=c.get("iters", 30))
+    return job, f"{B} sequences of one step (gamma={c['gamma']}, V={c['V']}, T={T})"
+
+
+def cpu_baseline(name, temperature, budget_s=6.0, lenience=1.0, op="verify"):
+    """The oracle, as it stands, on a bounded sample of the workload: one host
+    core, then every host core at once (one spawned process per core)."""
+    from oracle import timing
+
+    job, what = oracle_job(name, temperature, lenience, op)
+    one, n1, dt1 = timing.time_one_core(job, budget_s)
+    rates, cores, calls = timing.time_all_cores(job, budget_s)
+    return {"value": rates[0], "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{what}; {calls} oracle calls over {cores} concurrent processes in {budget_s:.0f} s",
+            "single_core": {"value": one, "cores": 1, "sample": f"{n1} oracle calls in {dt1:.1f} s"}}
 
 
 def reference_arm(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
+    from oracle import timing
+
     cfg, _, temp = WORKLOADS[args.workload]
     lv = LENIENCE.get(args.workload, 1.0)
-    budget = args.ref_budget if args.ref_budget > 0 else max(2.0, 60.0 / max(1, args.steps))
-    for _ in range(args.warmup):
-        cpu_baseline(cfg, temp, budget_s=min(1.0, budget), lenience=lv, op=OPS.get(args.workload, "verify"))
-    vals = [cpu_baseline(cfg, temp, budget_s=budget, lenience=lv,
-                         op=OPS.get(args.workload, "verify"))
-            for _ in range(args.steps)]
-    v = statistics.median(x["value"] for x in vals)
+    budget = args.ref_budget if args.ref_budget > 0 else max(1.5, 60.0 / max(1, args.steps + args.warmup))
+    job, what = oracle_job(cfg, temp, lv, OPS.get(args.workload, "verify"))
+    rates, cores, calls = timing.time_all_cores(job, budget, rounds=args.warmup + args.steps)
+    timed = rates[args.warmup:]
+    v = statistics.median(timed)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload},
-            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": vals[0]["sample"]},
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": describe(args.workload, WORKLOADS[args.workload][1])},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{what}; each step {budget:.1f} s on {cores} concurrent processes "
+                                       f"(median of {args.steps} steps after {args.warmup} warm-up)"},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
+
+
+def describe(name, stacked):
+    """The workload as the JSON line names it: configuration, sizes, stacking."""
+    cfg, _, temp = WORKLOADS[name]
+    c = workloads.CONFIGS[cfg]
+    T = c.get("temperature") if temp is None else temp
+    desc = {"large_vocab": f"B={c['B']}, gamma={c.get('gamma')}, V={c['V']}, f32, T={T}",
+            "nucleus": f"B={c['B']}, gamma={c.get('gamma')}, V={c['V']}, bf16, T={T}, top_p={c.get('top_p')}",
+            "tree": f"B={c['B']}, N={c.get('N')}, V={c['V']}, f32",
+            "mentor": f"B={c['B']}, gamma={c.get('gamma')}, V={c['V']}, f32, T=1, D={c.get('kl_bound')}, "
+                      f"{c.get('iters')} bisection steps"}.get(cfg, f"B={c['B']}, V={c['V']}")
+    extra = f", lenience {LENIENCE[name]}" if name in LENIENCE else ""
+    extra += ", acceptance rates (beta) only" if name in OPS else ""
+    return f"{name}: {cfg} ({desc}{extra}), {stacked} steps stacked in one call of B={c['B'] * stacked} sequences"
+
+
+def measure(args, name, stacked, steps, warmup, device, ws, rank, local):
+    """Times `steps` calls of one workload (after `warmup`); returns its figures."""
+    cfg, _, temp = WORKLOADS[name]
+    inp = make_inputs(cfg, stacked, temp, device, seed=2024 + rank, lenience=LENIENCE.get(name, 1.0), rank=rank)
+    inp["op"] = OPS.get(name, "verify")
+    nbytes, npos = algorithmic(inp)
+    stream = torch.cuda.current_stream(device)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(device)
+
+    l2_bytes = 129 * 2**20
+    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=device) if nbytes < 2 * l2_bytes else None
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    # clocks are sampled from the warm-up through the timed steps; a short
+    # timed region is followed by untimed steps until 0.3 s of load is sampled
+    with ClockSampler(local) as clk:
+        t_load0 = time.perf_counter()
+        for _ in range(warmup):
+            if flush is not None:
+                flush.fill_(1)
+            run_step(inp)
+        barrier()
+        for i in range(steps):
+            if flush is not None:
+                flush.fill_(i & 255)  # evicts the previous step's inputs from L2 (untimed)
+            starts[i].record(stream)
+            run_step(inp)
+            ends[i].record(stream)
+        barrier()
+        while time.perf_counter() - t_load0 < 0.3:
+            run_step(inp)
+            torch.cuda.synchronize(device)
+    per_launch_ms = [st.elapsed_time(en) for st, en in zip(starts, ends)]
+    total_ms = max_over_ranks(sum(per_launch_ms), device)
+    # acceptance statistics of one step (a property of the synthetic inputs)
+    out = run_step(inp)
+    torch.cuda.synchronize(device)
+    acc_mean = None
+    if "accepted" in out:
+        acc_mean = float(out["accepted"].float().mean().item())
+    elif "accept_len" in out:
+        acc_mean = float(out["accept_len"].float().mean().item())
+    alpha_est = float(out["beta"].float().mean().item()) if inp.get("op") == "alpha" else None
+    peak, peak_kind = measured_peaks()
+    avg_launch_ms = statistics.mean(per_launch_ms)
+    achieved = nbytes / (avg_launch_ms / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": recorded_traffic(name, stacked), "kernel": KERNEL_OF[name],
+            "algorithmic_bytes_per_launch": nbytes, "peak_source": f"{peak_kind} hbm_gbs (copy)",
+            "frac_of_nominal_8TBps": achieved / 8000.0}
+    return dict(inp=inp, nbytes=nbytes, npos=npos, total_ms=total_ms, ms_per_step=total_ms / steps,
+                value=job_value(ws, npos, steps, total_ms), roofline=roof,
+                clocks=dict(clk.summary(), window="warm-up + timed steps (+ untimed steps up to 0.3 s)"),
+                mean_accepted=acc_mean, alpha=alpha_est, cfg=cfg, stacked=stacked, flush=flush is not None,
+                batch=inp["B"], launches=launches_per_step(inp),
+                workload=describe(name, stacked))
+
+
+def e2e_figure(inp, steps, device, ws, npos):
+    """The same metric through the public API with pinned host buffers: the
+    inputs' host-to-device copies and the outputs' device-to-host copies are
+    inside the timed region."""
+    host = {k: v.to("cpu").pin_memory() for k, v in inp.items() if isinstance(v, torch.Tensor)}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    for _ in range(2):
+        run_step_host(inp, host)
+    torch.cuda.synchronize(device)
+    n_e2e = max(3, min(steps, 10))
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        r = run_step_host(inp, host)
+    dt = max_over_ranks((time.perf_counter() - t0) * 1e3, device) / 1e3
+    d2h = sum(v.numel() * v.element_size() for v in r.values() if isinstance(v, torch.Tensor))
+    return {"value": ws * npos * n_e2e / dt, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": n_e2e, "ms_per_step": dt * 1e3 / n_e2e,
+            "h2d_gbs": h2d / (dt / n_e2e) / 1e9}
 
 
 def main():
@@ -361,10 +471,11 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="nucleus", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other V >= 32k workloads")
     ap.add_argument("--stack", type=int, default=0, help="stacked steps per call (default: the workload's)")
     ap.add_argument("--ref-budget", type=float, default=0.0,
                     help="reference arm: seconds of oracle work per step (default: about 60 s over all steps)")
@@ -383,106 +494,41 @@ def main():
     import speculative_decoding_verification_05_gb300 as sv
 
     sv.load_library()
-    cfg, stacked, temp = WORKLOADS[args.workload]
-    if args.stack > 0:
-        stacked = args.stack
-    inp = make_inputs(cfg, stacked, temp, device, seed=2024 + rank, lenience=LENIENCE.get(args.workload, 1.0),
-                      rank=rank)
-    inp["op"] = OPS.get(args.workload, "verify")
-    nbytes, npos = algorithmic(inp)
-    stream = torch.cuda.current_stream(device)
-
-    def barrier():
-        if ws > 1:
-            import torch.distributed as dist
-            dist.barrier()
-        torch.cuda.synchronize(device)
-
-    l2_bytes = 129 * 2**20
-    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device=device) if nbytes < 2 * l2_bytes else None
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    # clocks are sampled from the warm-up through the timed steps; a short
-    # timed region is followed by untimed steps until 0.3 s of load is sampled
-    with ClockSampler(local) as clk:
-        t_load0 = time.perf_counter()
-        for _ in range(args.warmup):
-            if flush is not None:
-                flush.fill_(1)
-            run_step(inp)
-        barrier()
-        for i in range(args.steps):
-            if flush is not None:
-                flush.fill_(i & 255)  # evicts the previous step's inputs from L2 (untimed)
-            starts[i].record(stream)
-            run_step(inp)
-            ends[i].record(stream)
-        barrier()
-        while time.perf_counter() - t_load0 < 0.3:
-            run_step(inp)
-            torch.cuda.synchronize(device)
-    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = max_over_ranks(sum(per_launch_ms), device)
-    ms_per_step = total_ms / args.steps
-    value = job_value(ws, npos, args.steps, total_ms)
-
-    # acceptance statistics of one step (a property of the synthetic inputs)
-    out = run_step(inp)
-    torch.cuda.synchronize(device)
-    acc_mean = None
-    if "accepted" in out:
-        acc_mean = float(out["accepted"].float().mean().item())
-    elif "accept_len" in out:
-        acc_mean = float(out["accept_len"].float().mean().item())
-    # alpha = E(beta) for the acceptance-rate workload only (the mentor's
-    # "beta" output is its resampling constant, NaN at undecided positions)
-    alpha_est = float(out["beta"].float().mean().item()) if inp.get("op") == "alpha" else None
-
-    e2e = None
-    if not args.no_e2e:
-        host = {k: v.to("cpu").pin_memory() for k, v in inp.items() if isinstance(v, torch.Tensor)}
-        h2d = sum(v.numel() * v.element_size() for v in host.values())
-        for _ in range(2):
-            run_step_host(inp, host)
-        torch.cuda.synchronize(device)
-        n_e2e = max(3, min(args.steps, 10))
-        t0 = time.perf_counter()
-        for _ in range(n_e2e):
-            r = run_step_host(inp, host)
-        dt = max_over_ranks((time.perf_counter() - t0) * 1e3, device) / 1e3
-        d2h = sum(v.numel() * v.element_size() for v in r.values() if isinstance(v, torch.Tensor))
-        e2e = {"value": ws * npos * n_e2e / dt, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "steps": n_e2e}
-        del host
-
+    stacked = args.stack if args.stack > 0 else WORKLOADS[args.workload][1]
+    m = measure(args, args.workload, stacked, args.steps, args.warmup, device, ws, rank, local)
+    inp = m["inp"]
+    e2e = None if args.no_e2e else e2e_figure(inp, args.steps, device, ws, m["npos"])
+    del inp, m["inp"]
+    extra = {}
+    if not args.no_extra and args.workload == DEFAULT and args.stack == 0:
+        for name in EXTRA:
+            torch.cuda.empty_cache()
+            x = measure(args, name, WORKLOADS[name][1], max(3, min(args.steps, 10)), 3, device, ws, rank, local)
+            del x["inp"]
+            extra[name] = {"workload": x["workload"], "value": x["value"], "unit": UNIT,
+                           "ms_per_step": x["ms_per_step"], "steps": max(3, min(args.steps, 10)),
+                           "roofline": x["roofline"], "clocks": x["clocks"], "mean_accepted": x["mean_accepted"],
+                           "bytes_per_step": x["nbytes"], "positions_per_step": x["npos"]}
     if rank != 0:
         return 0
-    peak, peak_kind = measured_peaks()
-    avg_launch_ms = statistics.mean(per_launch_ms)
-    achieved = nbytes / (avg_launch_ms / 1e3) / 1e9
-    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-            "frac": achieved / peak,
-            "traffic": recorded_traffic(args.workload) if args.stack in (0, WORKLOADS[args.workload][1]) else None,
-            "kernel": KERNEL_OF[args.workload], "algorithmic_bytes_per_launch": nbytes,
-            "peak_source": f"{peak_kind} hbm_gbs (copy)", "frac_of_nominal_8TBps": achieved / 8000.0}
-    cpu = None if args.no_cpu else cpu_baseline(cfg, temp, lenience=LENIENCE.get(args.workload, 1.0),
+    cfg = m["cfg"]
+    cpu = None if args.no_cpu else cpu_baseline(cfg, WORKLOADS[args.workload][2],
+                                                lenience=LENIENCE.get(args.workload, 1.0),
                                                 op=OPS.get(args.workload, "verify"))
-    c = workloads.CONFIGS[cfg]
+    esize = workloads.TORCH_DTYPE[workloads.CONFIGS[cfg].get("dtype", "f32")].itemsize
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if inp["esize"] == 2 else "f32", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {cfg} x {stacked} steps in one call "
-                               f"(B={inp['B']}, V={inp['V']})"
-                               + (f", lenience {LENIENCE[args.workload]}" if args.workload in LENIENCE else ""),
-                   "global_batch": inp["B"] * ws,
-                   "bytes_per_step": nbytes, "positions_per_step": npos,
-                   "l2": "L2 flushed between steps" if flush is not None else "inputs larger than 2x L2 (no flush)",
+        "metric": METRIC, "value": m["value"], "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": m["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if esize == 2 else "f32", "data": "synthetic",
+        "config": {"workload": m["workload"], "global_batch": m["batch"] * ws,
+                   "bytes_per_step": m["nbytes"], "positions_per_step": m["npos"],
+                   "l2": "L2 flushed between steps" if m["flush"] else "inputs larger than 2x L2 (no flush)",
                    "parallelism": f"replicas x{ws}"},
-        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": launches_per_step(inp) * args.steps,
-        "clocks": dict(clk.summary(), window="warm-up + timed steps (+ untimed steps up to 0.3 s)"),
-        "hbm_gbs": achieved, "mean_accepted": acc_mean, **({"alpha": alpha_est} if alpha_est is not None else {}),
+        "roofline": m["roofline"], "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": m["launches"] * args.steps,
+        "clocks": m["clocks"], "hbm_gbs": m["roofline"]["achieved"], "mean_accepted": m["mean_accepted"],
+        **({"alpha": m["alpha"]} if m["alpha"] is not None else {}),
+        **({"per_workload": extra} if extra else {}),
     }
     print(json.dumps(line))
     return 0

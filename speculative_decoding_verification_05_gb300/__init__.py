@@ -177,18 +177,36 @@ class _Staging:
         return torch.empty(shape, dtype=dtype, device=self.device)
 
     def back(self, d):
+        """Device outputs to host tensors: one asynchronous copy per output
+        into a reused pinned buffer, one synchronisation, then copies into
+        ordinary host tensors that the caller owns."""
         if not self.host:
             return d
-        res = {}
-        for k, v in d.items():
-            if isinstance(v, torch.Tensor):
-                h = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+        tens = {k: v for k, v in d.items() if isinstance(v, torch.Tensor)}
+        total = sum(_al16(v.numel() * v.element_size()) for v in tens.values())
+        with _pin_lock:
+            buf = _pinned.get(self.device.index)
+            if buf is None or buf.numel() < total:
+                buf = torch.empty(max(total, 1 << 16), dtype=torch.uint8, pin_memory=True)
+                _pinned[self.device.index] = buf
+            views, o = {}, 0
+            for k, v in tens.items():
+                n = v.numel() * v.element_size()
+                h = buf[o:o + n].view(v.dtype).view(v.shape)
                 h.copy_(v, non_blocking=True)
-                res[k] = h
-            else:
-                res[k] = v
-        torch.cuda.current_stream(self.device).synchronize()
+                views[k] = h
+                o += _al16(n)
+            torch.cuda.current_stream(self.device).synchronize()
+            res = {k: (views[k].clone() if k in views else v) for k, v in d.items()}
         return res
+
+
+def _al16(n):
+    return (n + 15) & ~15
+
+
+_pinned = {}
+_pin_lock = threading.Lock()
 
 
 def verify(target, draft, draft_tokens, temperature=1.0, top_p=1.0, top_k=0, seed=0, offset=0,
