@@ -123,7 +123,7 @@ def accept_test(u, q_x, p_x):
     return u < thr, rho, np.abs(u - thr) <= NEAR_TIE
 
 
-def inverse_cdf(u, w, with_alt=False):
+def inverse_cdf(u, w):
     """Index sampled from weights w [R, V] >= 0 with uniform u [R].
 
     The smallest i with C_i > u * W (C the inclusive prefix sum in index
@@ -131,11 +131,8 @@ def inverse_cdf(u, w, with_alt=False):
     This is the draw x ~ (f)_+ of [SpS] "改进的拒绝采样" once the weights are
     max(0, q - p), and the ordinary draw from q for the bonus token.
     Returns (index [R], near_tie [R]) with near_tie when u*W lies within
-    NEAR_TIE * W of the boundary that decided the index. With with_alt=True
-    also returns alt [R]: where exactly one of the two boundaries of the
-    chosen interval is that close, the positive-weight neighbour across it
-    (the other admissible answer); -1 where there is no near boundary, -2
-    where both are near (ambiguous beyond one neighbour).
+    NEAR_TIE * W of the boundary that decided the index (``admissible_draws``
+    lists every index such a draw may return).
     """
     w = np.asarray(w, dtype=np.float64)
     u = np.asarray(u, dtype=np.float64)
@@ -152,18 +149,55 @@ def inverse_cdf(u, w, with_alt=False):
     lower = np.where(i > 0, C[rows, np.maximum(i - 1, 0)], -np.inf)
     near_hi = (C[rows, i] - t) <= NEAR_TIE * W
     near_lo = (t - lower) <= NEAR_TIE * W
-    near = near_hi | near_lo | ~has
-    if not with_alt:
-        return i, near
-    idx = np.arange(V)[None, :]
-    prev_pos = np.where(pos & (idx < i[:, None]), idx, -1).max(axis=1)
-    nxt = np.where(pos & (idx > i[:, None]), idx, V).min(axis=1)
-    alt = np.full(R, -1, dtype=np.int64)
-    alt = np.where(near_lo & ~near_hi & (prev_pos >= 0), prev_pos, alt)
-    alt = np.where(near_hi & ~near_lo & (nxt < V), nxt, alt)
-    alt = np.where((near_lo & near_hi) | ~has, -2, alt)
-    alt = np.where(near & (alt == -1), -2, alt)   # near, but no neighbour to offer
-    return i, near, alt
+    return i, near_hi | near_lo | ~has
+
+
+ADM_K = 16
+
+
+def admissible_draws(u, w, k=ADM_K):
+    """Every index an inverse-CDF draw (``inverse_cdf``) from weights w [R, V]
+    returns when its threshold t = u W moves by at most b = NEAR_TIE * W: the
+    positive-weight indices j with C_{j-1} <= t + b and C_j > t - b (C the
+    inclusive prefix sum, C_{-1} = 0), and the last positive-weight index
+    when t + b reaches W (the rounding fallback). A draw computed in lower
+    precision, whose prefix sums are within the band, returns one of them.
+
+    Returns (adm [R, k] ascending, -1 padded; over [R] True where more than k
+    indices qualify, which leaves the draw undecided by this check).
+    """
+    w = np.asarray(w, dtype=np.float64)
+    u = np.asarray(u, dtype=np.float64)
+    R, V = w.shape
+    C = np.cumsum(w, axis=1)
+    W = C[:, -1]
+    t = u * W
+    b = NEAR_TIE * W
+    Cm = np.concatenate([np.zeros((R, 1)), C[:, :-1]], axis=1)
+    pos = w > 0
+    ok = pos & (Cm <= (t + b)[:, None]) & (C > (t - b)[:, None])
+    last_pos = V - 1 - np.argmax(pos[:, ::-1], axis=1)
+    rows = np.arange(R)
+    fall = (t + b >= W) & pos.any(axis=1)
+    ok[rows[fall], last_pos[fall]] = True
+    cnt = ok.sum(axis=1)
+    first = np.argsort(~ok, axis=1, kind="stable")[:, :k]   # the qualifying indices, ascending
+    adm = np.where(np.take_along_axis(ok, first, axis=1), first, -1).astype(np.int64)
+    if adm.shape[1] < k:
+        adm = np.concatenate([adm, np.full((R, k - adm.shape[1]), -1, dtype=np.int64)], axis=1)
+    return adm, cnt > k
+
+
+def _merge_adm(a, b, k=ADM_K):
+    """Union of two admissible sets [R, k] (ascending, -1 padded); over where
+    the union exceeds k."""
+    out = np.full_like(a, -1)
+    over = np.zeros(a.shape[0], dtype=bool)
+    for r in range(a.shape[0]):
+        u = np.union1d(a[r][a[r] >= 0], b[r][b[r] >= 0])
+        over[r] = u.size > k
+        out[r, :min(k, u.size)] = u[:k]
+    return out, over
 
 
 def _emit(x, n, token):
@@ -216,9 +250,9 @@ def verify(target, draft, draft_tokens, temperature=1.0, top_p=1.0, top_k=0,
 
     Returns a dict: accepted [B], tokens [B, gamma+1] (-1 padded),
     next_token [B], status [B], near_tie [B] (a decision within the near-tie
-    band: the row is excluded from exact comparison), alt_token [B] (where
-    the final draw's uniform sits within the band of one CDF boundary, the
-    neighbouring token across it, equally admissible; -1 otherwise),
+    band: the row is excluded from exact comparison), adm_tokens [B, ADM_K]
+    (every token the final draw may return when its threshold moves within
+    the near-tie band, ``admissible_draws``; next_token is one of them),
     q_x / p_x [B, gamma] (the probabilities of each draft token), prob_near
     [B, gamma] (top-p threshold near-tie in either row at that position).
     """
@@ -239,7 +273,7 @@ def verify(target, draft, draft_tokens, temperature=1.0, top_p=1.0, top_k=0,
 
     n = np.full(B, gamma, dtype=np.int64)
     token = np.full(B, -1, dtype=np.int64)
-    alt = np.full(B, -1, dtype=np.int64)
+    adm = np.full((B, ADM_K), -1, dtype=np.int64)
     near = np.zeros(B, dtype=bool)
     q_x = np.full((B, gamma), np.nan)
     p_x = np.full((B, gamma), np.nan)
@@ -253,6 +287,7 @@ def verify(target, draft, draft_tokens, temperature=1.0, top_p=1.0, top_k=0,
         p_x[:] = 1.0
         n = np.where(match.all(axis=1), gamma, np.argmin(match, axis=1)) if gamma else n
         token = am[brange, n]
+        adm[:, 0] = token
     else:
         for k in range(gamma):
             q, nq = transformed_probs(zt[:, k], temperature, top_k, top_p)
@@ -268,18 +303,18 @@ def verify(target, draft, draft_tokens, temperature=1.0, top_p=1.0, top_k=0,
                 w = np.maximum(0.0, q[rej] - lenience * p[rej])
                 zero = w.sum(axis=1) == 0
                 w[zero] = q[rej][zero]
-                tok, _, a = inverse_cdf(U(rows[rej], k, PURPOSE_RESAMPLE), w, with_alt=True)
-                token[rej] = tok
-                alt[rej] = np.maximum(a, -1)
-                near[rej] |= a == -2
+                u2 = U(rows[rej], k, PURPOSE_RESAMPLE)
+                token[rej], _ = inverse_cdf(u2, w)
+                adm[rej], over = admissible_draws(u2, w)
+                near[rej] |= over
                 n[rej] = k
         allacc = n == gamma
         if allacc.any():
             q, nq = transformed_probs(zt[allacc, gamma], temperature, top_k, top_p)
-            tok, _, a = inverse_cdf(U(rows[allacc], gamma, PURPOSE_RESAMPLE), q, with_alt=True)
-            token[allacc] = tok
-            alt[allacc] = np.maximum(a, -1)
-            near[allacc] |= (a == -2) | nq
+            u2 = U(rows[allacc], gamma, PURPOSE_RESAMPLE)
+            token[allacc], _ = inverse_cdf(u2, q)
+            adm[allacc], over = admissible_draws(u2, q)
+            near[allacc] |= over | nq
 
     tokens = _emit(x, n, token)
     accepted = n.copy()
@@ -288,9 +323,9 @@ def verify(target, draft, draft_tokens, temperature=1.0, top_p=1.0, top_k=0,
     tokens[bad] = -1
     token[bad] = -1
     near[bad] = False
-    alt[bad | near] = -1
+    adm[bad] = -1
     return dict(accepted=accepted, tokens=tokens, next_token=token, status=status,
-                near_tie=near, alt_token=alt, q_x=q_x, p_x=p_x, prob_near=prob_near)
+                near_tie=near, adm_tokens=adm, q_x=q_x, p_x=p_x, prob_near=prob_near)
 
 
 def sample(logits, temperature=1.0, top_p=1.0, top_k=0, seed=0, offset=0,
@@ -302,30 +337,34 @@ def sample(logits, temperature=1.0, top_p=1.0, top_k=0, seed=0, offset=0,
     [B, P, V]; token[b, j] uses U(seed, offset+b, pos0+j, purpose) and the
     inverse CDF in index order (temperature 0: argmax). A bad row (NaN,
     +inf, all -inf) gets token -1 and marks its sequence with status 4.
-    Returns dict with tokens [B, P], near_tie [B, P], status [B].
+    Returns dict with tokens [B, P], near_tie [B, P] (top-p threshold
+    near-ties, and draws with more admissible tokens than ADM_K),
+    adm_tokens [B, P, ADM_K] (``admissible_draws``), status [B].
     """
     z = _f64(logits)
     B, P, V = z.shape
     U = _uniform_fn(seed, uniform_fn)
     rows = np.uint64(offset) + np.arange(B, dtype=np.uint64)
     tokens = np.full((B, P), -1, dtype=np.int64)
-    alt = np.full((B, P), -1, dtype=np.int64)
+    adm = np.full((B, P, ADM_K), -1, dtype=np.int64)
     near = np.zeros((B, P), dtype=bool)
     bad = _bad_rows(z)
     for j in range(P):
         q, nq = transformed_probs(z[:, j], temperature, top_k, top_p)
         if temperature == 0:
             tokens[:, j] = np.argmax(q, axis=1)
+            adm[:, j, 0] = tokens[:, j]
             continue
+        u = U(rows, pos0 + j, purpose)
         with np.errstate(invalid="ignore"):
-            tok, _, a = inverse_cdf(U(rows, pos0 + j, purpose), np.nan_to_num(q), with_alt=True)
-        tokens[:, j] = tok
-        alt[:, j] = np.maximum(a, -1)
-        near[:, j] = nq | (a == -2)
+            qq = np.nan_to_num(q)
+            tokens[:, j], _ = inverse_cdf(u, qq)
+            adm[:, j], over = admissible_draws(u, qq)
+        near[:, j] = nq | over
     tokens[bad] = -1
     near[bad] = False
-    alt[bad | near] = -1
-    return dict(tokens=tokens, near_tie=near, alt_token=alt,
+    adm[bad] = -1
+    return dict(tokens=tokens, near_tie=near, adm_tokens=adm,
                 status=np.where(bad.any(axis=1), STATUS_EDATA, STATUS_OK))
 
 
@@ -551,7 +590,7 @@ def verify_mentor(target, draft, draft_tokens, temperature=1.0, kl_bound=0.0,
     xs = np.clip(x, 0, V - 1)
     n = np.full(B, gamma, dtype=np.int64)
     token = np.full(B, -1, dtype=np.int64)
-    alt_tok = np.full(B, -1, dtype=np.int64)
+    adm = np.full((B, ADM_K), -1, dtype=np.int64)
     near = np.zeros(B, dtype=bool)
     alpha = np.full((B, gamma), np.nan)
     beta = np.full((B, gamma), np.nan)
@@ -589,33 +628,36 @@ def verify_mentor(target, draft, draft_tokens, temperature=1.0, kl_bound=0.0,
                 continue
             u2 = U(rows[b:b + 1], k, PURPOSE_RESAMPLE)
 
-            def draw(bb):
+            def weights(bb):
                 w = np.maximum(0.0, q[b] / bb - p[b])
-                if w.sum() == 0:
-                    w = q[b]
-                return inverse_cdf(u2, w[None, :], with_alt=True)
+                return (w if w.sum() > 0 else q[b])[None, :]
 
-            tok, _, a_alt = draw(be)
-            others = {int(draw(sol["beta_lo"])[0][0]), int(draw(sol["beta_hi"])[0][0])}
-            token[b] = tok[0]
-            alt_tok[b] = max(int(a_alt[0]), -1)
-            near[b] |= (a_alt[0] == -2) or bool(others - {int(tok[0]), alt_tok[b]})
+            token[b] = inverse_cdf(u2, weights(be))[0][0]
+            # admissible tokens: the band around each draw from the weights
+            # of beta and of the admissible range's ends
+            a_set, over = admissible_draws(u2, weights(be))
+            for bb in (sol["beta_lo"], sol["beta_hi"]):
+                a2, o2 = admissible_draws(u2, weights(bb))
+                a_set, o3 = _merge_adm(a_set, a2)
+                over |= o2 | o3
+            adm[b] = a_set[0]
+            near[b] |= bool(over[0])
             n[b] = k
     allacc = (n == gamma) & ~bad
     if allacc.any():
         q, _ = transformed_probs(zt[allacc, gamma], temperature)
-        tok, _, a = inverse_cdf(U(rows[allacc], gamma, PURPOSE_RESAMPLE), q, with_alt=True)
-        token[allacc] = tok
-        alt_tok[allacc] = np.maximum(a, -1)
-        near[allacc] |= a == -2
+        u2 = U(rows[allacc], gamma, PURPOSE_RESAMPLE)
+        token[allacc], _ = inverse_cdf(u2, q)
+        adm[allacc], over = admissible_draws(u2, q)
+        near[allacc] |= over
     tokens = _emit(x, n, token)
     tokens[bad] = -1
     accepted = np.where(bad, -1, n)
     token[bad] = -1
     near[bad] = False
-    alt_tok[bad | near] = -1
+    adm[bad] = -1
     return dict(accepted=accepted, tokens=tokens, next_token=token,
-                status=np.where(bad, STATUS_EDATA, STATUS_OK), near_tie=near, alt_token=alt_tok,
+                status=np.where(bad, STATUS_EDATA, STATUS_OK), near_tie=near, adm_tokens=adm,
                 alpha=alpha, beta=beta, alpha_lo=alpha_lo, alpha_hi=alpha_hi, q_x=q_x, p_x=p_x)
 
 

