@@ -74,7 +74,8 @@ typedef enum {
     SPEC_EINVAL = 1,   /* bad argument; nothing was enqueued */
     SPEC_ECUDA = 2,    /* a CUDA launch or attribute call failed */
     SPEC_ETIMEOUT = 3, /* (status[] only) a bounded device wait gave up */
-    SPEC_EDATA = 4     /* (status[] only) bad logits, tokens or tree */
+    SPEC_EDATA = 4,    /* (status[] only) bad logits, tokens or tree */
+    SPEC_EBOUNDS = 5   /* (status[] only, debug builds) an index check failed; the access was skipped */
 } spec_status;
 
 typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
@@ -366,6 +367,19 @@ const char* spec_status_string(spec_status s);
 /* The last CUDA error string recorded by a call that returned SPEC_ECUDA on
  * this host thread (static per-thread storage; "" if none). */
 const char* spec_last_cuda_error(void);
+
+/* Debug builds. The library built with -DSPEC_DEBUG (build.py's debug
+ * library, libspecverify_debug.so) checks the indices its kernels compute
+ * against the extent of the array each addresses, where a memory checker
+ * cannot be run: a failed check skips the access, counts the failure and,
+ * where the kernel knows the sequence, sets its status to SPEC_EBOUNDS
+ * (nothing traps). spec_debug_build returns 1 for that library, 0 for the
+ * release one. spec_debug_failures returns the number of failed checks on the
+ * current device since the library was loaded (0 in release builds) and, when
+ * `line` is not NULL, the source line of the first one (0 if none); it waits
+ * for the device's queued work to finish; -1 on a CUDA error. */
+int spec_debug_build(void);
+int spec_debug_failures(int* line);
 
 /* Library ABI version (major * 100 + minor). */
 int spec_version(void);

@@ -16,6 +16,7 @@ Tensors may live on the GPU (the normal case) or in (pinned) host memory; host
 inputs are copied to the current device, and outputs come back to the host.
 """
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -24,8 +25,10 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libspecverify.so")
+# the same library built with device-side index checks (build.py --debug)
+DEBUG_LIB_PATH = os.path.join(_HERE, "libspecverify_debug.so")
 
-SPEC_OK, SPEC_EINVAL, SPEC_ECUDA, SPEC_ETIMEOUT, SPEC_EDATA = 0, 1, 2, 3, 4
+SPEC_OK, SPEC_EINVAL, SPEC_ECUDA, SPEC_ETIMEOUT, SPEC_EDATA, SPEC_EBOUNDS = 0, 1, 2, 3, 4, 5
 SPEC_F32, SPEC_BF16 = 0, 1
 PURPOSE_ACCEPT, PURPOSE_RESAMPLE, PURPOSE_DRAFT = 0, 1, 2
 
@@ -36,7 +39,7 @@ EXPORTED = [
     "spec_verify_mentor_workspace_size", "spec_verify_mentor",
     "spec_sample_workspace_size", "spec_sample",
     "spec_philox_uniform", "spec_verify_noalloc", "spec_status_string", "spec_last_cuda_error",
-    "spec_version",
+    "spec_version", "spec_debug_build", "spec_debug_failures",
 ]
 
 
@@ -48,7 +51,8 @@ class SpecError(RuntimeError):
     pass
 
 
-_lib = None
+_libs = {}
+_current = [LIB_PATH]
 _lock = threading.Lock()
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -56,12 +60,14 @@ _U64 = ctypes.c_uint64
 _SZ = ctypes.c_size_t
 
 
-def load_library(path=LIB_PATH):
-    """Load libspecverify.so and declare its C signatures (no CUDA call)."""
-    global _lib
+def load_library(path=None):
+    """Load the library (default: the one ``use_library`` selected, normally
+    libspecverify.so) and declare its C signatures (no CUDA call)."""
     with _lock:
-        if _lib is not None:
-            return _lib
+        path = path or _current[0]
+        lib = _libs.get(path)
+        if lib is not None:
+            return lib
         if not os.path.exists(path):
             raise SpecError(f"{path} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
         lib = ctypes.CDLL(path)
@@ -112,8 +118,27 @@ def load_library(path=LIB_PATH):
         lib.spec_last_cuda_error.restype = ctypes.c_char_p
         lib.spec_version.argtypes = []
         lib.spec_version.restype = _I
-        _lib = lib
+        lib.spec_debug_build.argtypes = []
+        lib.spec_debug_build.restype = _I
+        lib.spec_debug_failures.argtypes = [_P]
+        lib.spec_debug_failures.restype = _I
+        _libs[path] = lib
         return lib
+
+
+@contextlib.contextmanager
+def use_library(path):
+    """Route the calls of this module to the library at `path` (for example
+    the debug build, DEBUG_LIB_PATH) inside the block."""
+    load_library(path)
+    with _lock:
+        saved = _current[0]
+        _current[0] = path
+    try:
+        yield
+    finally:
+        with _lock:
+            _current[0] = saved
 
 
 def _check(rc):
@@ -403,6 +428,6 @@ def philox_uniform(seed, row0, position, purpose, n, device=None):
     return out
 
 
-__all__ = ["philox_uniform", "verify", "verify_tree", "tree_build", "acceptance_rate", "expected_tokens",
+__all__ = ["use_library", "DEBUG_LIB_PATH", "philox_uniform", "verify", "verify_tree", "tree_build", "acceptance_rate", "expected_tokens",
            "walltime_factor", "ops_factor", "best_gamma", "verify_mentor", "sample", "load_library", "workspace",
            "SpecError", "SpecSampling", "EXPORTED", "LIB_PATH"]

@@ -16,8 +16,11 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspecverify.so")
-SOURCES = ["csrc/api.cu", "csrc/rows.cu", "csrc/argmax.cu", "csrc/mentor.cu", "csrc/noalloc.cu",
-           "csrc/tree_build.cu", "csrc/beta.cu", "csrc/planner.cu"]
+# the same sources with device-side index checks (-DSPEC_DEBUG): failed checks
+# skip the access and are counted (spec_debug_failures), nothing traps
+DEBUG_LIB = os.path.join(HERE, "libspecverify_debug.so")
+SOURCES = ["csrc/api.cu", "csrc/rows.cu", "csrc/rows_smem.cu", "csrc/argmax.cu", "csrc/mentor.cu",
+           "csrc/noalloc.cu", "csrc/tree_build.cu", "csrc/beta.cu", "csrc/planner.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
           "-Xptxas", "-v", "-I", os.path.join(ROOT, "include"), "-I", os.path.join(HERE, "csrc")]
@@ -30,32 +33,41 @@ def _nvcc():
     return nvcc
 
 
-def _compile(src):
-    obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
-    cmd = [_nvcc(), *ARCH, *CFLAGS, "-c", os.path.join(HERE, src), "-o", obj]
+def _compile(job):
+    src, debug = job
+    obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", "_debug.o" if debug else ".o"))
+    cmd = [_nvcc(), *ARCH, *CFLAGS, *(["-DSPEC_DEBUG"] if debug else []), "-c", os.path.join(HERE, src), "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
     return obj, r.stderr
 
 
-def build(verbose=False):
-    """Compile every translation unit and link libspecverify.so; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
-    with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        results = list(ex.map(_compile, SOURCES))
-    with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
-        for (obj, log), src in zip(results, SOURCES):
-            f.write(f"==== {src}\n{log}\n")
-    objs = [o for o, _ in results]
-    tmp = LIB + ".tmp"
-    cmd = [_nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
-    r = subprocess.run(cmd, capture_output=True, text=True)
+def _link(objs, lib):
+    tmp = lib + ".tmp"
+    r = subprocess.run([_nvcc(), *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
+
+
+def build(verbose=False, debug=True):
+    """Compile every translation unit and link libspecverify.so (and, with
+    `debug`, libspecverify_debug.so with device-side index checks), all
+    translation units in parallel; returns the release library's path."""
+    os.makedirs(BUILD, exist_ok=True)
+    jobs = [(src, False) for src in SOURCES] + ([(src, True) for src in SOURCES] if debug else [])
+    with concurrent.futures.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+        results = list(ex.map(_compile, jobs))
+    with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
+        for (obj, log), (src, dbg) in zip(results, jobs):
+            if not dbg:
+                f.write(f"==== {src}\n{log}\n")
+    _link([o for (o, _), (_, dbg) in zip(results, jobs) if not dbg], LIB)
+    if debug:
+        _link([o for (o, _), (_, dbg) in zip(results, jobs) if dbg], DEBUG_LIB)
     if verbose:
-        print(f"built {LIB}")
+        print(f"built {LIB}" + (f" and {DEBUG_LIB}" if debug else ""))
     return LIB
 
 

@@ -112,6 +112,42 @@ Ws ws_layout(int B, int R, int V) {
     return w;
 }
 
+// Verification workspace: the row layout, plus (for shapes the shared-memory
+// row path can take: bf16, V a multiple of 8, V <= 65536) the window list of
+// every target row, kKeptCap entries in regions (indices, raw logits, entries
+// per region), and the queue of rows whose threshold the window did not
+// decide.
+constexpr int kKeptCap = sv::kKeptRegions * sv::kKeptRegionCap;
+
+struct VerifyWs {
+    Ws lin;
+    size_t kidx, kval, kcnt, fbq, total;
+    bool kept;
+};
+
+bool smem_shape(spec_dtype dtype, int V) { return dtype == SPEC_BF16 && V % 8 == 0 && V <= 65536; }
+
+VerifyWs verify_ws(int B, int gamma, int V, spec_dtype dtype) {
+    VerifyWs w;
+    w.lin = ws_layout(B, 2 * gamma + 1, V);
+    size_t o = w.lin.total;
+    w.kept = smem_shape(dtype, V);
+    w.kidx = w.kval = w.kcnt = w.fbq = o;
+    if (w.kept) {
+        const size_t n = (size_t)B * (gamma + 1) * kKeptCap;
+        w.kidx = o;
+        o = al(o + n * sizeof(uint32_t));
+        w.kval = o;
+        o = al(o + n * sizeof(uint16_t));
+        w.kcnt = o;
+        o = al(o + (size_t)B * (gamma + 1) * sv::kKeptRegions);
+        w.fbq = o;
+        o = al(o + (size_t)B * (2 * gamma + 1) * sizeof(int32_t));
+    }
+    w.total = o;
+    return w;
+}
+
 spec_status clear(void* ws, size_t from, size_t to, cudaStream_t st) {
     const cudaError_t e = cudaMemsetAsync(reinterpret_cast<char*>(ws) + from, 0, to - from, st);
     return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
@@ -170,6 +206,32 @@ spec_status run_rows(sv::RowParams& p, int dtype, void* ws, const Ws& w, cudaStr
     return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
 }
 
+// The shared-memory row path for verification with a transform on bf16
+// rows, when the shape, the alignment and the shared memory allow it;
+// SPEC_EINVAL (nothing enqueued) when it does not apply.
+spec_status run_smem_rows(sv::RowParams& p, void* ws, const VerifyWs& w, cudaStream_t st) {
+    int nbuf = 0;
+    size_t smem = 0;
+    if (!w.kept || p.transform == 0 || p.mode != sv::kModeVerify || !aligned(p.target, 16) ||
+        !aligned(p.draft, 16) || (long long)p.B * p.rows_per_b > (1LL << 30) ||
+        !sv::smem_rows_plan(p.V, &nbuf, &smem))
+        return SPEC_EINVAL;
+    p.nseg = 1;
+    p.seg_len = p.V;
+    p.rows = at<sv::RowRec>(ws, w.lin.rows);
+    p.work = at<unsigned int>(ws, w.lin.work);
+    p.seq_n = at<int32_t>(ws, w.lin.seqn);  // the queue of sequences drawn from the rows
+    p.kept_idx = at<uint32_t>(ws, w.kidx);
+    p.kept_val = at<uint16_t>(ws, w.kval);
+    p.kept_cnt = at<uint8_t>(ws, w.kcnt);
+    p.kept_cap = kKeptCap;
+    p.fb_rows = at<int32_t>(ws, w.fbq);
+    if (spec_status c = clear(ws, 0, w.lin.work + kAlign, st)) return c;
+    cudaError_t e = sv::launch_smem_rows(p, nbuf, smem, device_sms(), st);
+    if (e == cudaSuccess) e = sv::launch_smem_draws(p, device_sms(), st);
+    return e == cudaSuccess ? SPEC_OK : cuda_fail(e);
+}
+
 spec_status launch_argmax_checked(sv::ArgmaxParams& p, int dtype, void* ws, const Ws& w, cudaStream_t st) {
     p.rowbest = at<unsigned long long>(ws, w.rowbest);
     p.rowbad = at<unsigned int>(ws, w.rowbad);
@@ -223,8 +285,9 @@ spec_status verify_impl(const void* target, const void* draft, spec_dtype dtype,
     const int es = esize(dtype);
     if (!aligned(target, es) || (draft && !aligned(draft, es)) || !aligned(workspace, kAlign))
         return SPEC_EINVAL;
-    const Ws w = ws_layout(B, 2 * gamma + 1, V);
-    if (ws_bytes < w.total) return SPEC_EINVAL;
+    const VerifyWs vw = verify_ws(B, gamma, V, dtype);
+    const Ws& w = vw.lin;
+    if (ws_bytes < vw.total) return SPEC_EINVAL;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int dt = dtype == SPEC_F32 ? 0 : 1;
 
@@ -265,6 +328,10 @@ spec_status verify_impl(const void* target, const void* draft, spec_dtype dtype,
     p.status = status;
     p.probs_dbg = probs_dbg;
     if (!std::isfinite(p.c2)) return SPEC_EINVAL;
+    if (dt == 1 && p.transform != 0) {
+        const spec_status s = run_smem_rows(p, workspace, vw, st);
+        if (s != SPEC_EINVAL) return s;
+    }
     return run_rows(p, dt, workspace, w, st);
 }
 
@@ -284,16 +351,40 @@ const char* spec_status_string(spec_status s) {
         case SPEC_ECUDA: return "SPEC_ECUDA";
         case SPEC_ETIMEOUT: return "SPEC_ETIMEOUT";
         case SPEC_EDATA: return "SPEC_EDATA";
+        case SPEC_EBOUNDS: return "SPEC_EBOUNDS";
     }
     return "SPEC_UNKNOWN";
 }
 
 const char* spec_last_cuda_error(void) { return g_cuda_err; }
 
+int spec_debug_build(void) {
+#ifdef SPEC_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+int spec_debug_failures(int* line) {
+    using Reader = cudaError_t (*)(unsigned int*, unsigned int*);
+    const Reader readers[] = {sv::debug_read_rows, sv::debug_read_rows_smem, sv::debug_read_argmax,
+                              sv::debug_read_mentor, sv::debug_read_beta, sv::debug_read_tree_build};
+    long long total = 0;
+    int first = 0;
+    for (const Reader rd : readers) {
+        unsigned int c = 0u, l = 0u;
+        if (rd(&c, &l) != cudaSuccess) return -1;
+        if (c && !first) first = (int)l;
+        total += c;
+    }
+    if (line) *line = first;
+    return total > 0x7FFFFFFF ? 0x7FFFFFFF : (int)total;
+}
+
 size_t spec_verify_workspace_size(int B, int gamma, int V, spec_dtype dtype) {
-    (void)dtype;
     if (B < 1 || gamma < 1 || V < 1) return 0;
-    return ws_layout(B, 2 * gamma + 1, V).total;
+    return verify_ws(B, gamma, V, dtype).total;
 }
 
 spec_status spec_verify(const void* target, const void* draft, spec_dtype dtype,

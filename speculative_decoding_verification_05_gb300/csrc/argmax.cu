@@ -146,9 +146,9 @@ SV_DEV void segment(const ArgmaxParams& p, long long r, int i0, int i1) {
         if (best.i >= 0) {
             const unsigned long long packed =
                 ((unsigned long long)f32_key(best.v) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)best.i);
-            atomicMax(&p.rowbest[r], packed);
+            if (SV_IN(r, (long long)p.B * p.rows_per_b)) atomicMax(&p.rowbest[r], packed);
         }
-        if (wbad) atomicOr(&p.rowbad[r], 1u);
+        if (wbad && SV_IN(r, (long long)p.B * p.rows_per_b)) atomicOr(&p.rowbad[r], 1u);
     }
 }
 
@@ -158,6 +158,7 @@ SV_DEV void resolve(const ArgmaxParams& p, SharedA& s, int b) {
     const int R = p.rows_per_b;
     const long long base = (long long)b * R;
     for (int i = tid; i < R; i += NT) {
+        if (!SV_IN(i, kMaxN)) continue;
         const unsigned long long w = __ldcg(&p.rowbest[base + i]);
         const unsigned bad = __ldcg(&p.rowbad[base + i]);
         s.am[i] = (int)(0xFFFFFFFFu - (uint32_t)(w & 0xFFFFFFFFull));
@@ -195,7 +196,7 @@ SV_DEV void resolve(const ArgmaxParams& p, SharedA& s, int b) {
         for (int j = tid; j < R; j += NT) {
             int v = -1;
             if (!anybad) v = j < n ? s.tok[j] : (j == n ? s.am[n] : -1);
-            p.out1[(size_t)b * R + j] = v;
+            if (SV_IN_SEQ((size_t)b * R + j, (long long)p.B * R, p.status, b)) p.out1[(size_t)b * R + j] = v;
         }
         if (p.probs_dbg) {  // q(x) is 1 iff x is the argmax; greedy drafts have p(x) = 1
             float* dbg = p.probs_dbg;
@@ -251,6 +252,7 @@ SV_DEV void resolve(const ArgmaxParams& p, SharedA& s, int b) {
         const int bad = s.bi[0], dstar = s.bi[1], alen = s.bi[2];
         if (tid == 0 && !bad) {
             for (int node = dstar;; node = s.par[node]) {
+                if (!SV_IN_SEQ(node, N, p.status, b) || !SV_IN_SEQ(s.dep[node], kMaxN, p.status, b)) break;
                 s.pn[s.dep[node]] = node;
                 if (node == 0) break;
             }
@@ -261,8 +263,10 @@ SV_DEV void resolve(const ArgmaxParams& p, SharedA& s, int b) {
             if (!bad && j <= alen) pn = s.pn[j];
             if (!bad && j < alen) tk = s.tok[s.pn[j + 1]];
             if (!bad && j == alen) tk = s.am[dstar];
-            p.out1[(size_t)b * W + j] = pn;
-            p.out2[(size_t)b * W + j] = tk;
+            if (SV_IN_SEQ((size_t)b * W + j, (long long)p.B * W, p.status, b)) {
+                p.out1[(size_t)b * W + j] = pn;
+                p.out2[(size_t)b * W + j] = tk;
+            }
         }
     }
 }
@@ -326,5 +330,7 @@ cudaError_t launch_argmax(const ArgmaxParams& p, int dtype, int grid, cudaStream
         argmax_kernel<bf16_t><<<grid, NT, 0, stream>>>(p);
     return cudaGetLastError();
 }
+
+SV_DEBUG_READER(argmax)
 
 }  // namespace sv

@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(BT) beta_kernel(const __grid_constant__ RowPar
         if (tid == 0) {
             float s = 0.f;
             for (int w = 0; w < BT / 32; ++w) s += red[w];
-            beta[jb] = bad ? NAN : s;
+            if (SV_IN(jb, (long long)p.B * p.gamma)) beta[jb] = bad ? NAN : s;
             if (k == 0 && p.status) {
                 int fl = 0;
                 for (int i = 0; i < R; ++i) fl |= __ldcg(&rb[i].flags);
@@ -122,5 +122,7 @@ cudaError_t launch_beta_t(const RowParams& p, float* beta, int sms, cudaStream_t
 cudaError_t launch_beta(const RowParams& p, int dtype, float* beta, int sms, cudaStream_t stream) {
     return dtype == 0 ? launch_beta_t<float>(p, beta, sms, stream) : launch_beta_t<bf16_t>(p, beta, sms, stream);
 }
+
+SV_DEBUG_READER(beta)
 
 }  // namespace sv

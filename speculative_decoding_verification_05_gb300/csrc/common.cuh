@@ -18,8 +18,66 @@ constexpr int kOk = 0;
 constexpr int kEData = 4;
 constexpr int kETimeout = 3;
 
+// ---------------------------------------------------------------------------
+// Index checks of the debug build (-DSPEC_DEBUG, build.py's debug library).
+// SV_IN(i, n) checks 0 <= i < n for an index a kernel is about to use; a
+// failed check counts the failure in the translation unit's failure words,
+// keeps the source line of the first one, and returns false so that the
+// caller skips the access (nothing traps or faults). SV_IN_SEQ also marks the
+// sequence's status with kEBounds. Release builds compile both to `true`.
+// Each translation unit keeps its own words (the library is built without
+// relocatable device code) and reads them with SV_DEBUG_READER.
+// ---------------------------------------------------------------------------
+constexpr int kEBounds = 5;
+
+#ifdef SPEC_DEBUG
+static __device__ unsigned int g_sv_debug[2];  // failed checks, line of the first
+
+SV_DEV bool sv_in(long long i, long long n, int line) {
+    if (i >= 0 && i < n) return true;
+    if (atomicAdd(&g_sv_debug[0], 1u) == 0u) g_sv_debug[1] = (unsigned)line;
+    return false;
+}
+
+SV_DEV bool sv_in_seq(long long i, long long n, int line, int32_t* status, long long b) {
+    if (sv_in(i, n, line)) return true;
+    if (status) atomicMax(reinterpret_cast<int*>(status + b), kEBounds);
+    return false;
+}
+
+#define SV_IN(i, n) ::sv::sv_in((long long)(i), (long long)(n), __LINE__)
+#define SV_IN_SEQ(i, n, status, b) ::sv::sv_in_seq((long long)(i), (long long)(n), __LINE__, (status), (long long)(b))
+// Defines sv::debug_read_<tu>(count, line): this translation unit's words.
+#define SV_DEBUG_READER(tu)                                                        \
+    cudaError_t debug_read_##tu(unsigned int* count, unsigned int* line) {        \
+        unsigned int w[2] = {0u, 0u};                                             \
+        const cudaError_t e = cudaMemcpyFromSymbol(w, g_sv_debug, sizeof(w));     \
+        *count = w[0];                                                            \
+        *line = w[1];                                                             \
+        return e;                                                                 \
+    }
+#else
+#define SV_IN(i, n) true
+#define SV_IN_SEQ(i, n, status, b) true
+#define SV_DEBUG_READER(tu)                                                        \
+    cudaError_t debug_read_##tu(unsigned int* count, unsigned int* line) {        \
+        *count = 0u;                                                              \
+        *line = 0u;                                                               \
+        return cudaSuccess;                                                       \
+    }
+#endif
+
+// The debug readers of the kernel translation units.
+cudaError_t debug_read_rows(unsigned int* count, unsigned int* line);
+cudaError_t debug_read_rows_smem(unsigned int* count, unsigned int* line);
+cudaError_t debug_read_argmax(unsigned int* count, unsigned int* line);
+cudaError_t debug_read_mentor(unsigned int* count, unsigned int* line);
+cudaError_t debug_read_beta(unsigned int* count, unsigned int* line);
+cudaError_t debug_read_tree_build(unsigned int* count, unsigned int* line);
+
 // Per-task record flags.
 constexpr int kRecEData = 2;     // bad logits in this row, or a draft token out of range
+constexpr int kRecTimeout = 4;   // the row's staging copy did not complete in time
 
 constexpr uint32_t kPurposeAccept = 0;
 constexpr uint32_t kPurposeResample = 1;
@@ -206,8 +264,8 @@ struct RowRec {
     float Sk;     // kept mass (the normaliser of the row's probabilities)
     float zx;     // the draft token's logit in this row (rows with a token)
     int32_t x;    // the draft token (rows with a token), else -1
-    int32_t flags;  // kRecEData
-    int32_t pad;
+    int32_t flags;  // kRecEData, kRecTimeout
+    int32_t nkept;  // shared-memory row path, target rows: entries of the kept list (-1: none)
 };
 
 // Partial statistics of one segment of a long row.
@@ -215,6 +273,10 @@ struct SegRec {
     float m, s, zx;
     int32_t flags;
 };
+
+// Window lists of the shared-memory row path (see RowParams::kept_idx).
+constexpr int kKeptRegions = 12;
+constexpr int kKeptRegionCap = 128;
 
 struct RowParams {
     const void* target;
@@ -242,8 +304,20 @@ struct RowParams {
     SegRec* segs;           // [B * rows_per_b * nseg] (nseg > 1)
     unsigned int* row_cnt;  // [B * rows_per_b] segment arrivals (nseg > 1)
     unsigned int* seq_cnt;  // [B] row arrivals
-    unsigned int* work;     // [2] next work unit, next sequence to draw (zero at launch)
+    unsigned int* work;     // work counters (zero at launch): [0] next work unit (row kernel) or
+                            // queued sequences, [1] next sequence to draw, [2] next queued
+                            // sequence, [3] queued rows, [4] next queued row
     int32_t* seq_n;         // [B] accepted length of each resolved sequence (-1: bad data)
+    // shared-memory row path: the window list of every target row (the
+    // logits within the window of its maximum, a superset of its kept set):
+    // kKeptRegions regions of kKeptRegionCap entries, each region in
+    // ascending index order, the regions in order; kept_cnt holds the entries
+    // of each region
+    uint32_t* kept_idx;     // [B * (gamma + 1) * kept_cap] indices
+    uint16_t* kept_val;     //                              raw logits
+    uint8_t* kept_cnt;      // [B * (gamma + 1) * kKeptRegions]
+    int kept_cap;           // kKeptRegions * kKeptRegionCap
+    int32_t* fb_rows;       // [B * rows_per_b] rows whose threshold comes from the whole row
 };
 
 enum ArgmaxMode : int { kArgVerify = 0, kArgTree = 1, kArgSample = 2 };
@@ -302,6 +376,12 @@ struct MentorParams {
 cudaError_t launch_rows(const RowParams& p, int dtype, int sms, cudaStream_t stream);
 // The one draw of every sequence the row kernel resolved (verification).
 cudaError_t launch_draws(const RowParams& p, int dtype, int sms, cudaStream_t stream);
+// Shared-memory row path (bf16 rows with a top-k / top-p transform):
+// whether a shape can take it (and the ring depth and dynamic shared memory
+// it needs), the row kernel, and the per-sequence resolve and draw.
+bool smem_rows_plan(int V, int* nbuf, size_t* smem);
+cudaError_t launch_smem_rows(const RowParams& p, int nbuf, size_t smem, int sms, cudaStream_t stream);
+cudaError_t launch_smem_draws(const RowParams& p, int sms, cudaStream_t stream);
 // Resident argmax CTAs per SM (occupancy of the kernel as built).
 int argmax_ctas_per_sm(int dtype);
 cudaError_t launch_argmax(const ArgmaxParams& p, int dtype, int grid, cudaStream_t stream);

@@ -127,7 +127,7 @@ SV_DEV int block_draw(DrawShared& ds, const E* rt, const E* rd, int V, float u, 
         // butterfly: every lane ends with the same warp total, in a fixed order
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) wsum += __shfl_xor_sync(0xFFFFFFFFu, wsum, o);
-        if (lane == 0) ds.wt[r][warp] = wsum;
+        if (lane == 0 && SV_IN(r, kDrawMaxRounds)) ds.wt[r][warp] = wsum;
     }
     __syncthreads();
     if (warp == 0) {
@@ -261,7 +261,7 @@ SV_DEV RowRec load_rec(const RowRec* src) {
     q.zx = __ldcg(&src->zx);
     q.x = __ldcg(&src->x);
     q.flags = __ldcg(&src->flags);
-    q.pad = 0;
+    q.nkept = __ldcg(&src->nkept);
     return q;
 }
 

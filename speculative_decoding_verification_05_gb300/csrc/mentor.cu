@@ -719,11 +719,13 @@ SV_DEV uint32_t hist_elem(HistArrays& h, const Row<E>& r, float zt, float zd, in
     uint32_t id;
     if (l < 0.f) {
         const int j = alpha_bucket(l);
+        if (!SV_IN(j, kNA)) return kDead;
         H = &h.A.raw[0][j];
         st = kNA;
         id = (uint32_t)j;
     } else {
         const int b = beta_bucket(l);
+        if (!SV_IN(b, kNB)) return kDead;
         H = &h.B.raw[0][b];
         st = kNB;
         id = (uint32_t)(kNA + b);
@@ -1149,9 +1151,11 @@ SV_DEV bool solve_hist(SharedH& sh, SmallM& t, const MentorParams& p, const Row<
                 rank += pos;
             }
             const int slot = (int)(uint32_t)x;
+            if (SV_IN(rank, kCap) && SV_IN(slot, kCap)) {
 #pragma unroll
-            for (int k = 0; k < 3; ++k) w.c[k][rank] = w.cu[k][slot];
-            w.lw[rank] = w.lwu[slot];
+                for (int k = 0; k < 3; ++k) w.c[k][rank] = w.cu[k][slot];
+                w.lw[rank] = w.lwu[slot];
+            }
             if ((uint32_t)(x >> 32) < 0x80000000u) atomicAdd(&t.nA, 1);
         }
     } else {
@@ -1486,7 +1490,7 @@ __global__ void __launch_bounds__(NT, 1) mentor_kernel(const __grid_constant__ M
                 }
             }
         }
-        if (tid == 0) {
+        if (tid == 0 && SV_IN_SEQ(pos, (long long)p.B * G, p.status, b)) {
             if (p.alpha_out) p.alpha_out[pos] = alpha;
             if (p.beta_out) p.beta_out[pos] = beta;
             p.pos_beta[pos] = beta;
@@ -1563,7 +1567,7 @@ __global__ void __launch_bounds__(kDrawNT) mentor_resolve_kernel(const __grid_co
         for (int j = tid; j <= G; j += kDrawNT) {
             int v = -1;
             if (!bad) v = j < n ? __ldcg(&rb[j].x) : (j == n ? tok : -1);
-            p.tokens[(size_t)b * G1 + j] = v;
+            if (SV_IN_SEQ((size_t)b * G1 + j, (long long)p.B * G1, p.status, b)) p.tokens[(size_t)b * G1 + j] = v;
         }
         for (int k = tid; k < G; k += kDrawNT) {
             if (bad || k > n) {
@@ -1595,5 +1599,7 @@ cudaError_t launch_mentor(const MentorParams& p, int grid, int resolve_grid, cud
     (p.bf16 ? mentor_resolve_kernel<bf16_t> : mentor_resolve_kernel<float>)<<<rgrid, kDrawNT, 0, stream>>>(p);
     return cudaGetLastError();
 }
+
+SV_DEBUG_READER(mentor)
 
 }  // namespace sv

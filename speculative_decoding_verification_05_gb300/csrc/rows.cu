@@ -46,9 +46,12 @@
 
 #include "common.cuh"
 #include "draw.cuh"
+#include "select.cuh"
 
 namespace sv {
 namespace {
+
+using namespace sel;
 
 constexpr int NT = kDrawNT;
 constexpr int NW = NT / 32;
@@ -58,17 +61,9 @@ constexpr int kWin = 13;               // stored keys: within 2^-kWin of the row
 constexpr int kWinB = 11;              // bf16 rows while streaming (a second, wider pass if needed)
 constexpr int kWinWide = 15;           // bf16 second pass: the ordinal histogram's reach
 constexpr int kSlotBytes = 96;         // key slots per thread, in bytes (five CTAs per SM fit)
-constexpr int kSel = 256;              // keys compared exactly inside the crossing bin
 constexpr int kOrd = 2048;             // bf16 ordinal histogram: bins
 constexpr uint32_t kPrefetchBytes = 65536;  // next units up to this size are prefetched into L2
-constexpr float kFx = 1099511627776.0f;  // 2^40: masses >= 2^-17 are exact integers
 
-struct GenSel {
-    unsigned hcnt[256];               // selection histogram: counts
-    unsigned long long hist[256];     //                      fixed-point masses
-    uint32_t skey[kSel];              // keys of the crossing bin
-    unsigned long long smass[kSel];
-};
 
 struct Shared {
     int q[3];                         // work units: this one and the next two
@@ -96,20 +91,6 @@ struct Shared {
     DrawShared draw;
 };
 
-SV_DEV float max_nan(float a, float b) {
-    float r;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
-    return r;
-}
-
-SV_DEV uint32_t bmax2(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-
-SV_DEV float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-SV_DEV float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // Online (max, sum of exp2((z - max) c)) of a segment.
 struct Online {
@@ -146,7 +127,7 @@ struct Collect {
     // Branch-free form for when at least one slot is free: the key is always
     // written to the next slot and kept only if it passes the cut.
     SV_DEV void put(float x, uint32_t raw) {
-        base[hc * NT] = (K)raw;
+        if (SV_IN(hc, kPer)) base[hc * NT] = (K)raw;
         hc += x > cut;
     }
 };
@@ -161,7 +142,7 @@ struct PairCollect {
     int hc;
     // branch-free, for when a slot is free
     SV_DEV void put(float lo, float hi, uint32_t w) {
-        base[hc * NT] = w;
+        if (SV_IN(hc, kPer)) base[hc * NT] = w;
         hc += (lo > cut) | (hi > cut);
     }
     SV_DEV void safe(float lo, float hi, uint32_t w) {
@@ -416,302 +397,6 @@ SV_DEV RowRef<E> row_ref(const RowParams& p, int b, int r) {
     return rr;
 }
 
-// --- exact thresholds ------------------------------------------------------
-
-SV_DEV unsigned long long fx_of(float a) { return __float2ull_rz(ex2(a) * kFx); }
-
-// The top-p target top_p * (kept mass) in fixed point; both paths use it.
-SV_DEV unsigned long long top_p_target(float top_p, unsigned long long kept) {
-    const unsigned long long t = (unsigned long long)(top_p * (float)kept);
-    return t ? t : 1ull;
-}
-
-// Bin of a = (z - m) log2e / T <= 0, non-increasing in z: 1/16 octave down to
-// 12 octaves, then 1 octave down to 60, then 8 octaves down to 180, then the
-// rest (and -inf).
-SV_DEV int abin(float a) {
-    const float t = -a;
-    if (t < 12.f) return max(0, (int)(t * 16.f));
-    if (t < 60.f) return 192 + (int)(t - 12.f);
-    if (t < 180.f) return 240 + (int)((t - 60.f) * 0.125f);
-    return 255;
-}
-
-SV_DEV unsigned long long block_sum_u64(Shared& s, unsigned long long v) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    if (lane == 0) s.ured[warp] = v;
-    __syncthreads();
-    unsigned long long t = 0ull;
-    for (int w = 0; w < NW; ++w) t += s.ured[w];
-    __syncthreads();
-    return t;
-}
-
-SV_DEV uint32_t block_max_u32(Shared& s, uint32_t v) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    v = __reduce_max_sync(0xFFFFFFFFu, v);
-    if (lane == 0) s.ured[warp] = v;
-    __syncthreads();
-    uint32_t t = 0u;
-    for (int w = 0; w < NW; ++w) t = max(t, (uint32_t)s.ured[w]);
-    __syncthreads();
-    return t;
-}
-
-// Histogram add with the lanes of a warp that hit the same bin combined into
-// one atomic per bin. Every lane of the warp must call it (v: item valid).
-SV_DEV void hist_add(Shared& s, bool v, int bin, unsigned long long w) {
-    const unsigned act = __ballot_sync(0xFFFFFFFFu, v);
-    if (v) {
-        const unsigned peers = __match_any_sync(act, bin);
-        const unsigned lo = __reduce_add_sync(peers, (unsigned)(w & 0x1FFFFFull));
-        const unsigned hi = __reduce_add_sync(peers, (unsigned)(w >> 21));  // w < 2^41
-        if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) {
-            atomicAdd(&s.h.g.hist[bin], ((unsigned long long)hi << 21) + lo);
-            atomicAdd(&s.h.g.hcnt[bin], (unsigned)__popc(peers));
-        }
-    }
-}
-
-struct Sel {
-    uint32_t tau;                 // selected key
-    unsigned long long cnt, mass; // count and fixed-point mass of the items with key >= tau
-    bool reach;                   // the items' total reached the target
-};
-
-// Radix selection (8-bit digits, exact integer histograms) restricted to the
-// items accepted by `keep`, starting above weight A0: the largest key tau with
-// A0 + W(key >= tau) >= target. npass = 2 suffices for keys of bf16 values.
-template <typename Each, typename Keep>
-SV_DEV uint32_t radix_select(Shared& s, const Each& each, const Keep& keep, int npass, bool by_count,
-                             unsigned long long A0, unsigned long long target) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t prefix = 0;
-    unsigned long long A = A0;
-    for (int pass = 0; pass < npass; ++pass) {
-        const int shift = 24 - 8 * pass;
-        if (threadIdx.x == 0) s.odirty = 1;
-        for (int i = threadIdx.x; i < 256; i += NT) {
-            s.h.g.hist[i] = 0ull;
-            s.h.g.hcnt[i] = 0u;
-        }
-        __syncthreads();
-        each([&](bool v, uint32_t key, float a) {
-            v = v && keep(key, a) && (pass == 0 || (key >> (shift + 8)) == (prefix >> (shift + 8)));
-            hist_add(s, v, v ? (int)((key >> shift) & 255u) : 0, v && !by_count ? fx_of(a) : 0ull);
-        });
-        __syncthreads();
-        if (warp == 0) {
-            // lane l owns digits 255 - 8l .. 248 - 8l (descending keys)
-            unsigned long long h[8], L = 0ull;
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const int d = 255 - 8 * lane - t;
-                h[t] = by_count ? (unsigned long long)s.h.g.hcnt[d] : s.h.g.hist[d];
-                L += h[t];
-            }
-            unsigned long long P = L;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, P, d);
-                if (lane >= d) P += y;
-            }
-            unsigned long long cum = A + (P - L), above = 0ull;
-            int dl = -1, lastnz = -1;
-            unsigned long long above_last = 0ull;
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                if (dl < 0 && h[t] > 0ull && cum + h[t] >= target) {
-                    dl = t;
-                    above = cum;
-                }
-                if (h[t] > 0ull) {
-                    lastnz = t;
-                    above_last = cum;
-                }
-                cum += h[t];
-            }
-            const unsigned mf = __ballot_sync(0xFFFFFFFFu, dl >= 0);
-            const unsigned ml = __ballot_sync(0xFFFFFFFFu, lastnz >= 0);
-            // the crossing digit, else (target not reached) the lowest non-empty digit
-            const int src = mf ? __ffs(mf) - 1 : (ml ? 31 - __clz(ml) : 0);
-            if (lane == src) {
-                const int t = mf ? dl : lastnz;
-                s.bi[1] = t >= 0 ? 255 - 8 * lane - t : 0;
-                s.ured[NW] = t >= 0 ? (mf ? above : above_last) : A;
-            }
-        }
-        __syncthreads();
-        prefix |= (uint32_t)s.bi[1] << shift;
-        A = s.ured[NW];
-        __syncthreads();
-    }
-    if (npass == 2) prefix |= (prefix & 0x80000000u) ? 0u : 0xFFFFu;
-    return prefix;
-}
-
-// Exact weighted selection over the items of `each` with key >= floor_key:
-// tau = the largest key with W(key >= tau) >= target, W a count (by_count) or
-// the fixed-point mass. Every thread returns the same result. Unreached
-// targets return reach = false (tau and the sums are then unspecified).
-template <typename Each>
-SV_DEV Sel select(Shared& s, const Each& each, int npass, bool by_count, uint32_t floor_key,
-                  unsigned long long target) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < 256; i += NT) {
-        s.h.g.hist[i] = 0ull;
-        s.h.g.hcnt[i] = 0u;
-    }
-    if (tid == 0) {
-        s.nsel = 0;
-        s.odirty = 1;
-    }
-    __syncthreads();
-    each([&](bool v, uint32_t key, float a) {
-        v = v && key >= floor_key;
-        hist_add(s, v, v ? abin(a) : 0, v ? fx_of(a) : 0ull);
-    });
-    __syncthreads();
-    if (warp == 0) {
-        // lane l owns bins 8l .. 8l + 7 (descending keys)
-        unsigned long long h[8], L = 0ull;
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            h[t] = by_count ? (unsigned long long)s.h.g.hcnt[8 * lane + t] : s.h.g.hist[8 * lane + t];
-            L += h[t];
-        }
-        unsigned long long P = L;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const unsigned long long y = __shfl_up_sync(0xFFFFFFFFu, P, d);
-            if (lane >= d) P += y;
-        }
-        const bool reach = __shfl_sync(0xFFFFFFFFu, P, 31) >= target;
-        unsigned long long cum = P - L;
-        int dl = -1;
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            if (dl < 0 && h[t] > 0ull && cum + h[t] >= target) dl = t;
-            cum += h[t];
-        }
-        const unsigned mf = __ballot_sync(0xFFFFFFFFu, dl >= 0);
-        const int c = mf ? 8 * (__ffs(mf) - 1) + __shfl_sync(0xFFFFFFFFu, dl, __ffs(mf) - 1) : 0;
-        // weights of the bins above c: count, mass
-        unsigned long long ac = 0ull, am = 0ull;
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            if (8 * lane + t < c) {
-                ac += s.h.g.hcnt[8 * lane + t];
-                am += s.h.g.hist[8 * lane + t];
-            }
-        }
-        for (int o = 16; o; o >>= 1) {
-            ac += __shfl_xor_sync(0xFFFFFFFFu, ac, o);
-            am += __shfl_xor_sync(0xFFFFFFFFu, am, o);
-        }
-        if (lane == 0) {
-            s.bi[0] = reach && mf;
-            s.bi[1] = c;
-            s.ured[NW] = ac;
-            s.ured[NW + 1] = am;
-        }
-    }
-    __syncthreads();
-    Sel r;
-    r.reach = s.bi[0] != 0;
-    const int c = s.bi[1];
-    const unsigned long long ac = s.ured[NW], am = s.ured[NW + 1];
-    const int nc = (int)s.h.g.hcnt[c];
-    __syncthreads();
-    if (!r.reach) return r;
-    const unsigned long long above = by_count ? ac : am;
-    if (nc <= kSel) {
-        // the crossing bin's keys, compared exactly
-        each([&](bool v, uint32_t key, float a) {
-            if (v && key >= floor_key && abin(a) == c) {
-                const int slot = atomicAdd(&s.nsel, 1);
-                s.h.g.skey[slot] = key;
-                s.h.g.smass[slot] = fx_of(a);
-            }
-        });
-        __syncthreads();
-        const int n = s.nsel;
-        uint32_t cand = 0u;
-        for (int i = tid; i < n; i += NT) {
-            const uint32_t ki = s.h.g.skey[i];
-            unsigned long long W = above;
-            for (int j = 0; j < n; ++j) W += s.h.g.skey[j] >= ki ? (by_count ? 1ull : s.h.g.smass[j]) : 0ull;
-            if (W >= target) cand = max(cand, ki);
-        }
-        r.tau = block_max_u32(s, cand);
-        unsigned long long pc = 0ull, pm = 0ull;
-        for (int i = tid; i < n; i += NT) {
-            if (s.h.g.skey[i] >= r.tau) {
-                pc += 1ull;
-                pm += s.h.g.smass[i];
-            }
-        }
-        r.cnt = ac + block_sum_u64(s, pc);
-        r.mass = am + block_sum_u64(s, pm);
-    } else {
-        auto keep = [&](uint32_t key, float a) { return key >= floor_key && abin(a) == c; };
-        r.tau = radix_select(s, each, keep, npass, by_count, above, target);
-        unsigned long long pc = 0ull, pm = 0ull;
-        each([&](bool v, uint32_t key, float a) {
-            if (v && key >= r.tau) {
-                pc += 1ull;
-                pm += fx_of(a);
-            }
-        });
-        r.cnt = block_sum_u64(s, pc);
-        r.mass = block_sum_u64(s, pm);
-    }
-    return r;
-}
-
-// Top-k then top-p over the items of `each`. Returns false (head keys only)
-// when they do not decide the threshold; the row path always decides.
-template <typename Each>
-SV_DEV bool threshold_from(Shared& s, const RowParams& p, const Each& each, int npass, bool head, float S,
-                           float* thr, float* sk) {
-    unsigned long long kept = (unsigned long long)(S * kFx);
-    float t = -INFINITY;
-    uint32_t floor_key = 0u;
-    if (p.transform & kXfTopK) {
-        const Sel r = select(s, each, npass, true, 0u, (unsigned long long)p.top_k);
-        if (!r.reach) {
-            if (head) return false;
-        } else {
-            floor_key = r.tau;
-            t = key_to_f32(r.tau);
-            kept = r.mass;
-        }
-    }
-    if (p.transform & kXfTopP) {
-        const Sel r = select(s, each, npass, false, floor_key, top_p_target(p.top_p, kept));
-        if (!r.reach) {
-            if (head) return false;
-        } else {
-            t = key_to_f32(r.tau);
-            kept = r.mass;
-        }
-    }
-    *thr = t;
-    *sk = (float)kept * (1.0f / kFx);
-    return true;
-}
-
-// bf16 ordinal: order-preserving 16-bit key of a bf16 value (-0 folded onto +0).
-SV_DEV uint32_t ord16(uint32_t raw) {
-    raw = raw == 0x8000u ? 0u : raw;
-    return (raw & 0x8000u) ? (~raw & 0xFFFFu) : (raw | 0x8000u);
-}
-
-SV_DEV float ord16_value(uint32_t k) {
-    const uint32_t raw = (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
-    return __uint_as_float(raw << 16);
-}
 
 // Threshold of a bf16 row from its stored keys counted per distinct value
 // (bin j holds the values of ordinal ord16(m) - j, largest first; the cut was
@@ -924,7 +609,7 @@ __device__ __noinline__ void row_threshold(Shared& s, const RowParams& p, const 
                 f(v0 && a > -(float)kWin, f32_key(z), a);
             }
         };
-        if (threshold_from(s, p, each, npass, true, S, thr, sk)) return;
+        if (threshold_from<true>(s, p, each, npass, true, S, thr, sk)) return;
     }
     const int V = p.V;
     auto each = [&](auto f) {
@@ -935,7 +620,7 @@ __device__ __noinline__ void row_threshold(Shared& s, const RowParams& p, const 
             f(v, f32_key(z), fmaf(z, c2, -mc));
         }
     };
-    threshold_from(s, p, each, npass, false, S, thr, sk);
+    threshold_from<false>(s, p, each, npass, false, S, thr, sk);
 }
 
 // --- per-row draw (sampling) and per-sequence resolve (verification) --------
@@ -951,7 +636,7 @@ __device__ __noinline__ void sample_row(Shared& s, const RowParams& p, const E* 
         tok = draw_q<E>(s.draw, row, p.V, rec, p.c2, u);
     }
     if (threadIdx.x == 0) {
-        p.sample_out[rowid] = tok;
+        if (SV_IN(rowid, (long long)p.B * p.rows_per_b)) p.sample_out[rowid] = tok;
         if (tok < 0 && p.status) atomicMax(&p.status[b], kEData);
     }
 }
@@ -968,7 +653,8 @@ __device__ __noinline__ void resolve_sequence(Shared& s, const RowParams& p, int
     const int tid = threadIdx.x;
     const int R = p.rows_per_b, G = p.gamma;
     __threadfence();
-    for (int i = tid; i < R; i += NT) s.u.rec[i] = load_rec(p.rows + (size_t)b * R + i);
+    for (int i = tid; i < R; i += NT)
+        if (SV_IN(i, kMaxRows)) s.u.rec[i] = load_rec(p.rows + (size_t)b * R + i);
     __syncthreads();
     if (tid == 0) {
         int flags = 0;
@@ -999,7 +685,8 @@ __device__ __noinline__ void resolve_sequence(Shared& s, const RowParams& p, int
     __syncthreads();
     const int n = s.bi[2], stt = s.bi[3];
     for (int j = tid; j <= G; j += NT)
-        if (stt || j != n) p.tokens[(size_t)b * (G + 1) + j] = (!stt && j < n) ? s.u.rec[j].x : -1;
+        if ((stt || j != n) && SV_IN_SEQ((size_t)b * (G + 1) + j, (long long)p.B * (G + 1), p.status, b))
+            p.tokens[(size_t)b * (G + 1) + j] = (!stt && j < n) ? s.u.rec[j].x : -1;
 }
 
 // One draw per resolved sequence: the residual max(0, q_n - l p_n) after a
@@ -1020,7 +707,7 @@ __global__ void __launch_bounds__(NT, sizeof(E) == 4 ? 4 : 6) draw_kernel(const 
         const int b = job;
         if (b >= p.B) break;
         const int n = p.seq_n[b];
-        if (n >= 0) {
+        if (n >= 0 && SV_IN_SEQ(n, G + 1, p.status, b)) {
             if (tid == 0) rec[0] = load_rec(p.rows + (size_t)b * R + n);
             if (tid == 1 && n < G) rec[1] = load_rec(p.rows + (size_t)b * R + G + 1 + n);
             __syncthreads();
@@ -1101,7 +788,7 @@ __global__ void __launch_bounds__(NT, 5) row_kernel(const __grid_constant__ RowP
         int x = -1;
         float zx = 0.f;
         if (tid == 0 && rr.has_x) {
-            x = p.draft_tokens[(size_t)b * p.gamma + rr.k];
+            if (SV_IN((size_t)b * p.gamma + rr.k, (long long)p.B * p.gamma)) x = p.draft_tokens[(size_t)b * p.gamma + rr.k];
             if (x >= i0 && x < i1) zx = VecTraits<E>::load1(rr.ptr + x);
         }
 
@@ -1122,7 +809,7 @@ __global__ void __launch_bounds__(NT, 5) row_kernel(const __grid_constant__ RowP
                 sr.s = S;
                 sr.zx = zx;
                 sr.flags = 0;
-                p.segs[unit] = sr;
+                if (SV_IN(unit, nunits)) p.segs[unit] = sr;
                 __threadfence();
                 const unsigned old = atomicAdd(&p.row_cnt[rowid], 1u);
                 s.last = old == (unsigned)(p.nseg - 1);
@@ -1161,8 +848,8 @@ __global__ void __launch_bounds__(NT, 5) row_kernel(const __grid_constant__ RowP
                 rec.zx = zx;
                 rec.x = x;
                 rec.flags = (bad || (rr.has_x && (x < 0 || x >= p.V))) ? kRecEData : 0;
-                rec.pad = 0;
-                p.rows[rowid] = rec;
+                rec.nkept = -1;
+                if (SV_IN(rowid, (long long)p.B * R)) p.rows[rowid] = rec;
                 s.u.rec[0] = rec;
                 s.ovf = 0;
             }
@@ -1226,5 +913,7 @@ cudaError_t launch_rows(const RowParams& p, int dtype, int sms, cudaStream_t str
 cudaError_t launch_draws(const RowParams& p, int dtype, int sms, cudaStream_t stream) {
     return dtype == 0 ? launch_draws_t<float>(p, sms, stream) : launch_draws_t<bf16_t>(p, sms, stream);
 }
+
+SV_DEBUG_READER(rows)
 
 }  // namespace sv

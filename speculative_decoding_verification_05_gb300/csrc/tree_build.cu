@@ -421,9 +421,11 @@ __global__ void __launch_bounds__(TB) tree_build_kernel(const __grid_constant__ 
                 s.u.pos.e[q] = e;
             }
             const size_t o = (size_t)b * N + q;
-            p.tokens[o] = tk;
-            p.parent[o] = pa;
-            p.depth[o] = de;
+            if (SV_IN_SEQ(o, (long long)p.B * p.N, p.status, b)) {
+                p.tokens[o] = tk;
+                p.parent[o] = pa;
+                p.depth[o] = de;
+            }
         }
         if (tid == 0) {
             p.n_nodes[b] = S + 1;
@@ -499,5 +501,7 @@ cudaError_t launch_tree_build(const int32_t* cand, const int32_t* counts, const 
     tree_build_kernel<<<B, TB, smem, stream>>>(p);
     return cudaGetLastError();
 }
+
+SV_DEBUG_READER(tree_build)
 
 }  // namespace sv

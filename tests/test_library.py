@@ -48,7 +48,12 @@ def test_version_and_status_strings(lib):
 def test_workspace_sizes_are_positive_and_grow(lib):
     a = lib.spec_verify_workspace_size(8, 4, 32000, 1)
     b = lib.spec_verify_workspace_size(64, 7, 128256, 0)
-    assert 0 < a < b and a % 256 == 0
+    assert 0 < a and 0 < b and a % 256 == 0 and b % 256 == 0
+    assert lib.spec_verify_workspace_size(16, 4, 32000, 1) > a
+    # bf16 shapes the shared-memory row path can take also hold the kept list
+    # of every target row (1024 entries of a 4-byte index and a 2-byte logit)
+    assert a - lib.spec_verify_workspace_size(8, 4, 32000, 0) >= 8 * 5 * 1024 * 6
+    assert lib.spec_verify_workspace_size(8, 4, 32001, 1) == lib.spec_verify_workspace_size(8, 4, 32001, 0)
     assert lib.spec_verify_workspace_size(0, 4, 10, 0) == 0
     assert lib.spec_verify_tree_workspace_size(16, 64, 32016, 0) > 0
     m = lib.spec_verify_mentor_workspace_size(32, 5, 32128, 0)
