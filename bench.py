@@ -66,11 +66,12 @@ OPS = {"nucleus_alpha": "alpha"}      # measured acceptance probabilities instea
 
 # The timed unit is one library call; where a call launches several kernels the
 # label names them all (the row or argmax kernel reads every logit byte).
-KERNEL_OF = {"nucleus": "row_kernel<bf16,transform> + draw_kernel", "tiny": "row_kernel<f32> + draw_kernel",
+SMEM_PATH = "smem_row_kernel + smem_fallback_kernel + smem_draw_kernel + smem_fulldraw_kernel"
+KERNEL_OF = {"nucleus": SMEM_PATH, "tiny": "row_kernel<f32> + draw_kernel",
              "large_vocab": "row_kernel<f32> + draw_kernel", "large_vocab_t0": "argmax_kernel<f32>",
              "tree": "argmax_kernel<f32>",
              "mentor": "row_kernel<f32> + mentor_kernel + mentor_resolve_kernel",
-             "nucleus_lenient": "row_kernel<bf16,transform> + draw_kernel",
+             "nucleus_lenient": SMEM_PATH,
              "rest": "tree_build_kernel + argmax_kernel<f32>",
              "nucleus_alpha": "row_kernel<bf16,transform> (records) + beta_kernel"}
 

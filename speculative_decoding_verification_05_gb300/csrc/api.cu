@@ -114,14 +114,14 @@ Ws ws_layout(int B, int R, int V) {
 
 // Verification workspace: the row layout, plus (for shapes the shared-memory
 // row path can take: bf16, V a multiple of 8, V <= 65536) the window list of
-// every target row, kKeptCap entries in regions (indices, raw logits, entries
-// per region), and the queue of rows whose threshold the window did not
-// decide.
+// every target row, kKeptCap entries in regions (index and raw logit packed
+// in 32 bits; entries per region), and the queue of rows whose threshold the
+// window did not decide.
 constexpr int kKeptCap = sv::kKeptRegions * sv::kKeptRegionCap;
 
 struct VerifyWs {
     Ws lin;
-    size_t kidx, kval, kcnt, fbq, total;
+    size_t kidx, kcnt, fbq, total;
     bool kept;
 };
 
@@ -132,13 +132,11 @@ VerifyWs verify_ws(int B, int gamma, int V, spec_dtype dtype) {
     w.lin = ws_layout(B, 2 * gamma + 1, V);
     size_t o = w.lin.total;
     w.kept = smem_shape(dtype, V);
-    w.kidx = w.kval = w.kcnt = w.fbq = o;
+    w.kidx = w.kcnt = w.fbq = o;
     if (w.kept) {
         const size_t n = (size_t)B * (gamma + 1) * kKeptCap;
         w.kidx = o;
         o = al(o + n * sizeof(uint32_t));
-        w.kval = o;
-        o = al(o + n * sizeof(uint16_t));
         w.kcnt = o;
         o = al(o + (size_t)B * (gamma + 1) * sv::kKeptRegions);
         w.fbq = o;
@@ -221,8 +219,7 @@ spec_status run_smem_rows(sv::RowParams& p, void* ws, const VerifyWs& w, cudaStr
     p.rows = at<sv::RowRec>(ws, w.lin.rows);
     p.work = at<unsigned int>(ws, w.lin.work);
     p.seq_n = at<int32_t>(ws, w.lin.seqn);  // the queue of sequences drawn from the rows
-    p.kept_idx = at<uint32_t>(ws, w.kidx);
-    p.kept_val = at<uint16_t>(ws, w.kval);
+    p.kept = at<uint32_t>(ws, w.kidx);
     p.kept_cnt = at<uint8_t>(ws, w.kcnt);
     p.kept_cap = kKeptCap;
     p.fb_rows = at<int32_t>(ws, w.fbq);

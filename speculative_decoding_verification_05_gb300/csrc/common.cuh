@@ -310,11 +310,10 @@ struct RowParams {
     int32_t* seq_n;         // [B] accepted length of each resolved sequence (-1: bad data)
     // shared-memory row path: the window list of every target row (the
     // logits within the window of its maximum, a superset of its kept set):
-    // kKeptRegions regions of kKeptRegionCap entries, each region in
-    // ascending index order, the regions in order; kept_cnt holds the entries
-    // of each region
-    uint32_t* kept_idx;     // [B * (gamma + 1) * kept_cap] indices
-    uint16_t* kept_val;     //                              raw logits
+    // kKeptRegions regions of kKeptRegionCap entries (index << 16 | raw bf16),
+    // each region in ascending index order, the regions in order; kept_cnt
+    // holds the entries of each region
+    uint32_t* kept;         // [B * (gamma + 1) * kept_cap]
     uint8_t* kept_cnt;      // [B * (gamma + 1) * kKeptRegions]
     int kept_cap;           // kKeptRegions * kKeptRegionCap
     int32_t* fb_rows;       // [B * rows_per_b] rows whose threshold comes from the whole row

@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) smem_row_kernel(const __grid_c
                     const float cutf = bf_lo(cut2);
                     const int top = (int)ord16(__float_as_uint(m) >> 16);
                     const int b = w.b, r = w.r;
-                    const bool tgt = r <= G && p.kept_idx != nullptr;
+                    const bool tgt = r <= G && p.kept != nullptr;
                     const size_t rg = ((size_t)b * (G + 1) + (tgt ? r : 0)) * (size_t)p.kept_cap + gw * kElemCap;
                     uint32_t* const bins = st.set[u & 1u].bins;
                     for (int c0 = 0; c0 < nv; c0 += 32) {
@@ -475,8 +475,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) smem_row_kernel(const __grid_c
                             jm = max(jm, jb);
                             if (jb < kOrdBins) atomicAdd(&bins[jb >> 1], 1u << ((jb & 1) * 16));
                             if (tgt && o < kElemCap && SV_IN(rg + o, (long long)p.B * (G + 1) * p.kept_cap)) {
-                                p.kept_idx[rg + o] = (uint32_t)(v * 8 + e);
-                                p.kept_val[rg + o] = (uint16_t)raw;
+                                p.kept[rg + o] = (uint32_t)(v * 8 + e) << 16 | raw;
                             }
                         }
                     }
@@ -607,7 +606,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) smem_row_kernel(const __grid_c
             if (fit && warp_threshold(ss.bins, jm + 1, top, p, m * c2, S, &thr, &sk, &jt)) {
                 decided = true;
                 // a target row's window list (written by the sum warps) holds its kept set
-                if (target && p.kept_idx != nullptr && !__any_sync(0xFFFFFFFFu, wcn > kElemCap))
+                if (target && p.kept != nullptr && !__any_sync(0xFFFFFFFFu, wcn > kElemCap))
                     nkept = __reduce_add_sync(0xFFFFFFFFu, (unsigned)wcn);
             }
             if (lane == 0) {
@@ -855,10 +854,9 @@ __global__ void __launch_bounds__(NT) smem_draw_kernel(const __grid_constant__ R
         }
         const float u2 = uniform01(p.seed, p.offset + (uint64_t)b, (uint32_t)n, kPurposeResample);
         const size_t lb = trow * (size_t)p.kept_cap;
-        const uint32_t* li = p.kept_idx + lb;
-        const uint16_t* lv = p.kept_val + lb;
+        const uint32_t* le = p.kept + lb;  // (index << 16) | raw
         const KeptExp q1{t.thr, c2, t.m * c2, 1.f};
-        const auto wq = [&](int e) { return q1(__uint_as_float((uint32_t)__ldcg(lv + e) << 16)); };
+        const auto wq = [&](int e) { return q1(__uint_as_float(__ldcg(le + e) << 16)); };
         float W = 0.f;
         int jj = -1;
         if (n < G) {
@@ -866,9 +864,10 @@ __global__ void __launch_bounds__(NT) smem_draw_kernel(const __grid_constant__ R
             const unsigned short* rd = reinterpret_cast<const unsigned short*>(p.draft) + ((size_t)b * G + n) * p.V;
             const ResidualW rw = residual_weight(t, d, c2, p.lenience);
             const auto wr = [&](int e) {
-                const float zt = __uint_as_float((uint32_t)__ldcg(lv + e) << 16);
+                const uint32_t en = __ldcg(le + e);
+                const float zt = __uint_as_float(en << 16);
                 if (!(zt >= t.thr)) return 0.f;  // q = 0 (the draft logit is not needed)
-                const uint32_t i = __ldcg(li + e);
+                const uint32_t i = en >> 16;
                 const float zd = SV_IN_SEQ(i, p.V, p.status, b) ? __uint_as_float((uint32_t)__ldg(rd + i) << 16) : 0.f;
                 return rw(zt, zd);
             };
@@ -877,7 +876,7 @@ __global__ void __launch_bounds__(NT) smem_draw_kernel(const __grid_constant__ R
         if (!(W > 0.f)) jj = warp_list_draw(t.nkept, rcnt[warp], roff[warp], u2, wq, &W);  // bonus, or a vanished residual
         __syncwarp();  // the region table is read before the warp's next sequence rewrites it
         if (lane == 0) {
-            const int tok = jj >= 0 ? (int)__ldcg(li + jj) : -1;
+            const int tok = jj >= 0 ? (int)(__ldcg(le + jj) >> 16) : -1;
             p.next_token[b] = tok;
             p.tokens[(size_t)b * (G + 1) + n] = tok;
         }
