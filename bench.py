@@ -281,15 +281,29 @@ def algorithmic(inp):
             workloads.verified_positions("linear", inp["B"], gamma=inp["gamma"]))
 
 
+def smem_path(inp):
+    """Whether spec_verify takes the shared-memory row path for these inputs:
+    bf16 logits with a top-k / top-p transform, V a multiple of 8 and at
+    most about 54000 (a ring of two rows fits), both tensors on 16 bytes."""
+    zt, zd = inp.get("zt"), inp.get("zd")
+    return (inp["kind"] == "linear" and inp.get("op", "verify") == "verify" and inp["T"] > 0
+            and inp["esize"] == 2 and inp["top_p"] < 1.0 and inp["V"] % 8 == 0 and inp["V"] <= 54000
+            and zt is not None and zd is not None and zt.data_ptr() % 16 == 0 and zd.data_ptr() % 16 == 0)
+
+
 def launches_per_step(inp):
     """Kernels one library call launches: rows, position solve and resolve
-    (mentor); the argmax kernel (tree, T = 0); rows and draws otherwise."""
+    (mentor); the argmax kernel (tree, T = 0); on the shared-memory row path
+    the row, fallback, draw and full-row draw kernels; rows and draws
+    otherwise."""
     if inp["kind"] == "mentor":
         return 3
     if inp["kind"] == "rest" or inp.get("op") == "alpha":
         return 2
     if inp["kind"] == "tree" or inp["T"] == 0:
         return 1
+    if smem_path(inp):
+        return 4
     return 2
 
 

@@ -571,9 +571,8 @@ __global__ void __launch_bounds__(kRowThreads, 1) smem_row_kernel(const __grid_c
                 }
                 break;
             }
-            const int b = w.b, r = w.r;
+            const int r = w.r;
             const bool target = r <= G;
-            const int k = target ? r : r - G - 1;
             const bool has_x = (!target || r < G) && p.draft_tokens != nullptr;
             const float m = key_max(st.mkey);
             const bool bad = !(m > -INFINITY && m < INFINITY);
@@ -602,7 +601,6 @@ __global__ void __launch_bounds__(kRowThreads, 1) smem_row_kernel(const __grid_c
             bool decided = bad;
             const int top = (int)ord16(__float_as_uint(m) >> 16);
             int jt = 0;
-            (void)k;
             if (fit && warp_threshold(ss.bins, jm + 1, top, p, m * c2, S, &thr, &sk, &jt)) {
                 decided = true;
                 // a target row's window list (written by the sum warps) holds its kept set
@@ -668,30 +666,68 @@ __global__ void __launch_bounds__(kRowThreads, 1) smem_row_kernel(const __grid_c
     __syncthreads();
 }
 
-// The queued rows: one CTA per row (taken from a counter) stages the row in
-// shared memory (16-byte loads, all in flight at once), runs the selection
-// of select.cuh over it and completes the row's record (threshold and kept
-// mass; no window list, so a draw from it reads the rows).
+// The queued rows: one CTA per row (taken from a counter) counts the row's
+// logits per distinct bf16 value (a 16-bit counter for every bf16 ordinal,
+// 128 KB of shared memory; one pass of 16-byte loads), then scans the counts
+// from the largest value down. A value's mass is its count times the
+// fixed-point mass of the value (the integers select.cuh sums element by
+// element), so the threshold is the one of select.cuh's selection over the
+// row. Thread t owns the 256 values of descending rank [256 t, 256 t + 256);
+// a block scan of the threads' totals places them, and the thread holding the
+// crossing is found; then every thread takes one value of that range and a
+// second block scan finds the value itself. Completes the row's record (threshold and kept
+// mass; no window list, so a draw from it reads the rows). Rows here are
+// shorter than 65536, so no count reaches 2^16.
+constexpr int kFbValues = 65536;
+constexpr int kFbPer = kFbValues / NT;  // values per thread (== NT: the walk takes one per thread)
+static_assert(kFbPer == NT, "one value of a thread's range per thread");
+
 struct FallbackShared {
-    struct {
-        GenSel g;
-    } h;
-    int bi[8];
-    unsigned long long ured[NW + 2];
-    int nsel, odirty;
+    unsigned long long wc[NW], ww[NW];  // block scans: per-warp totals
+    int hit;                            // the thread (then the value) holding the crossing
+    unsigned long long hc, hw;          // the weights before that thread's range
+    unsigned long long hw2;             // the mass through the crossing
     int job;
 };
 
+// Inclusive scan of two 64-bit values in thread order over the CTA.
+SV_DEV void block_scan2(FallbackShared& s, unsigned long long& a, unsigned long long& b) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long ya = __shfl_up_sync(0xFFFFFFFFu, a, o);
+        const unsigned long long yb = __shfl_up_sync(0xFFFFFFFFu, b, o);
+        if (lane >= o) {
+            a += ya;
+            b += yb;
+        }
+    }
+    __syncthreads();  // the previous scan's totals are read
+    if (lane == 31) {
+        s.wc[warp] = a;
+        s.ww[warp] = b;
+    }
+    __syncthreads();
+    for (int w = 0; w < warp; ++w) {
+        a += s.wc[w];
+        b += s.ww[w];
+    }
+}
+
 __global__ void __launch_bounds__(NT) smem_fallback_kernel(const __grid_constant__ RowParams p) {
-    extern __shared__ __align__(16) unsigned char fbuf[];
+    extern __shared__ __align__(16) uint32_t fcnt[];  // two 16-bit counts a word, by ordinal
     __shared__ FallbackShared s;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31;
     const int V = p.V, nvec = V >> 3;
     const float c2 = p.c2;
     const long long nrows = (long long)p.B * p.rows_per_b;
     (void)nrows;  // bounds of the debug build's checks
-    const unsigned short* zs = reinterpret_cast<const unsigned short*>(fbuf);
     const unsigned nq = __ldcg(p.work + 3);
+    // rank d = kFbValues - 1 - ordinal: descending values
+    const auto count_of = [&](int d) {
+        const int o = kFbValues - 1 - d;
+        return (fcnt[o >> 1] >> ((o & 1) * 16)) & 0xFFFFu;
+    };
     for (;;) {
         if (tid == 0) s.job = (int)atomicAdd(p.work + 4, 1u);
         __syncthreads();
@@ -701,24 +737,107 @@ __global__ void __launch_bounds__(NT) smem_fallback_kernel(const __grid_constant
         RowRec* rec = p.rows + row;
         const float m = __ldcg(&rec->m), S = __ldcg(&rec->S);
         const float mc = m * c2;
-        const uint4* src = reinterpret_cast<const uint4*>(row_src(p, row / p.rows_per_b, row % p.rows_per_b));
-        for (int v = tid; v < nvec; v += NT) reinterpret_cast<uint4*>(fbuf)[v] = __ldg(src + v);
+        for (int i = tid; i < kFbValues / 8; i += NT) reinterpret_cast<uint4*>(fcnt)[i] = make_uint4(0u, 0u, 0u, 0u);
         __syncthreads();
-        auto each = [&](auto f) {
-            for (int i0 = 0; i0 < V; i0 += NT) {
-                const int i = i0 + tid;
-                const bool v = i < V;
-                const float z = v ? bf_raw(zs[i]) : -INFINITY;
-                f(v, f32_key(z), fmaf(z, c2, -mc));
-            }
+        const uint4* src = reinterpret_cast<const uint4*>(row_src(p, row / p.rows_per_b, row % p.rows_per_b));
+        const auto add = [&](uint32_t raw) {
+            const uint32_t o = ord16(raw);
+            atomicAdd(&fcnt[o >> 1], 1u << ((o & 1u) * 16));
         };
-        float thr = -INFINITY, sk = S;
-        threshold_from<true>(s, p, each, 2, false, S, &thr, &sk);
+#pragma unroll 4
+        for (int v = tid; v < nvec; v += NT) {
+            const uint4 x = __ldg(src + v);
+            add(x.x & 0xFFFFu);
+            add(x.x >> 16);
+            add(x.y & 0xFFFFu);
+            add(x.y >> 16);
+            add(x.z & 0xFFFFu);
+            add(x.z >> 16);
+            add(x.w & 0xFFFFu);
+            add(x.w >> 16);
+        }
+        __syncthreads();
+        // this thread's values: totals of count and mass (each lane starts
+        // at its own offset in its range, so the warp's reads fall in
+        // different banks), then the threads' places by a block scan
+        const int d0 = tid * kFbPer;
+        const auto mass_of = [&](int d, unsigned c) {
+            return (unsigned long long)c *
+                   fx_of(fmaf(ord16_value((uint32_t)(kFbValues - 1 - d)), c2, -mc));
+        };
+        unsigned long long tc = 0ull, tw = 0ull;
+        for (int i = 0; i < kFbPer; ++i) {
+            const int d = d0 + ((i + 2 * lane) & (kFbPer - 1));
+            const unsigned c = count_of(d);
+            if (c) {
+                tc += c;
+                tw += mass_of(d, c);
+            }
+        }
+        unsigned long long ec = tc, ew = tw;
+        block_scan2(s, ec, ew);  // inclusive, thread order
+        ec -= tc;
+        ew -= tw;
+        // the first rank d <= dlim whose running weight reaches the target,
+        // and the mass through it (-1 if none): the thread whose range holds
+        // it is found first, then all threads take one value of that range
+        // each (a block scan in rank order) and the first that reaches the
+        // target reports it
+        const auto find = [&](bool by_count, unsigned long long target, int dlim, unsigned long long* wo) {
+            if (tid == 0) s.hit = -1;
+            __syncthreads();
+            if ((by_count ? ec : ew) < target && (by_count ? ec + tc : ew + tw) >= target && d0 <= dlim) {
+                s.hit = tid;
+                s.hc = ec;
+                s.hw = ew;
+            }
+            __syncthreads();
+            const int t = s.hit;
+            if (t < 0) return -1;
+            const int d = t * kFbPer + tid;  // kFbPer == NT: one value per thread
+            const unsigned k = d <= dlim ? count_of(d) : 0u;
+            unsigned long long c = k, w = k ? mass_of(d, k) : 0ull;
+            const unsigned long long c1 = c, w1 = w;
+            block_scan2(s, c, w);
+            c += s.hc;
+            w += s.hw;
+            if (tid == 0) s.hit = NT;
+            __syncthreads();
+            if (k && (by_count ? c : w) >= target && (by_count ? c - c1 : w - w1) < target) {
+                s.hit = tid;  // the one value where the running weight first reaches the target
+                s.hw2 = w;
+            }
+            __syncthreads();
+            const int j = s.hit;
+            *wo = s.hw2;
+            __syncthreads();
+            return j < NT ? t * kFbPer + j : -1;
+        };
+        unsigned long long kept = (unsigned long long)(S * kFx);
+        float thr = -INFINITY;
+        int dk = kFbValues - 1;
+        if (p.transform & kXfTopK) {
+            unsigned long long w;
+            const int d = find(true, (unsigned long long)p.top_k, dk, &w);
+            if (d >= 0) {  // (k beyond the row: every logit is kept)
+                dk = d;
+                thr = ord16_value((uint32_t)(kFbValues - 1 - d));
+                kept = w;
+            }
+        }
+        if (p.transform & kXfTopP) {
+            unsigned long long w;
+            const int d = find(false, top_p_target(p.top_p, kept), dk, &w);
+            if (d >= 0) {
+                thr = ord16_value((uint32_t)(kFbValues - 1 - d));
+                kept = w;
+            }
+        }
         if (tid == 0) {
             rec->thr = thr;
-            rec->Sk = sk;
+            rec->Sk = (float)kept * (1.0f / kFx);
         }
-        __syncthreads();  // the row and the shared state are free for the next row
+        __syncthreads();  // the counts and the shared state are free for the next row
     }
 }
 
@@ -854,9 +973,11 @@ __global__ void __launch_bounds__(NT) smem_draw_kernel(const __grid_constant__ R
         }
         const float u2 = uniform01(p.seed, p.offset + (uint64_t)b, (uint32_t)n, kPurposeResample);
         const size_t lb = trow * (size_t)p.kept_cap;
+        // (the list was written by the previous kernel: read-only loads through
+        // L1, so the crossing lane's second walk over its entries hits L1)
         const uint32_t* le = p.kept + lb;  // (index << 16) | raw
         const KeptExp q1{t.thr, c2, t.m * c2, 1.f};
-        const auto wq = [&](int e) { return q1(__uint_as_float(__ldcg(le + e) << 16)); };
+        const auto wq = [&](int e) { return q1(__uint_as_float(__ldg(le + e) << 16)); };
         float W = 0.f;
         int jj = -1;
         if (n < G) {
@@ -864,7 +985,7 @@ __global__ void __launch_bounds__(NT) smem_draw_kernel(const __grid_constant__ R
             const unsigned short* rd = reinterpret_cast<const unsigned short*>(p.draft) + ((size_t)b * G + n) * p.V;
             const ResidualW rw = residual_weight(t, d, c2, p.lenience);
             const auto wr = [&](int e) {
-                const uint32_t en = __ldcg(le + e);
+                const uint32_t en = __ldg(le + e);
                 const float zt = __uint_as_float(en << 16);
                 if (!(zt >= t.thr)) return 0.f;  // q = 0 (the draft logit is not needed)
                 const uint32_t i = en >> 16;
@@ -876,7 +997,7 @@ __global__ void __launch_bounds__(NT) smem_draw_kernel(const __grid_constant__ R
         if (!(W > 0.f)) jj = warp_list_draw(t.nkept, rcnt[warp], roff[warp], u2, wq, &W);  // bonus, or a vanished residual
         __syncwarp();  // the region table is read before the warp's next sequence rewrites it
         if (lane == 0) {
-            const int tok = jj >= 0 ? (int)(__ldcg(le + jj) >> 16) : -1;
+            const int tok = jj >= 0 ? (int)(__ldg(le + jj) >> 16) : -1;
             p.next_token[b] = tok;
             p.tokens[(size_t)b * (G + 1) + n] = tok;
         }
@@ -951,7 +1072,7 @@ cudaError_t launch_smem_rows(const RowParams& p, int nbuf, size_t smem, int sms,
     smem_row_kernel<<<grid, kRowThreads, smem, stream>>>(p, nbuf);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // the queued rows (usually none: the CTAs find the queue empty and exit)
-    const size_t fb = (size_t)p.V * 2;
+    const size_t fb = (size_t)kFbValues * 2;  // a 16-bit count per bf16 value
     if ((e = cudaFuncSetAttribute(smem_fallback_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fb)) !=
         cudaSuccess)
         return e;
