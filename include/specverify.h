@@ -37,10 +37,12 @@
  *    `status[b]` (when `status` is not NULL): SPEC_EDATA for a logit row that
  *    holds NaN or +inf or only -inf, a draft token outside [0, V), or a
  *    malformed tree; that sequence's outputs are then all -1. -inf alone is
- *    an ordinary zero-probability logit. SPEC_ETIMEOUT is reserved for a
- *    device wait that gives up; the current kernels never wait on one
- *    another (every hand-off is a last-arriver counter), so it is not
- *    reported.
+ *    an ordinary zero-probability logit. SPEC_ETIMEOUT: a bounded device
+ *    wait gave up. Kernels never wait on other CTAs (every hand-off between
+ *    CTAs is a last-arriver counter); only the warps of one CTA of the
+ *    shared-memory row path wait on one another (bounded, about a second),
+ *    and when one such wait gives up, the rows that CTA had left are
+ *    reported with SPEC_ETIMEOUT (outputs -1).
  *  - Workspace: a device buffer of at least the size the matching
  *    *_workspace_size() function returns, 256-byte aligned, owned by the
  *    caller. Its content on entry does not matter: each call clears the small
@@ -380,6 +382,16 @@ const char* spec_last_cuda_error(void);
  * for the device's queued work to finish; -1 on a CUDA error. */
 int spec_debug_build(void);
 int spec_debug_failures(int* line);
+
+/* Debug builds only: the shared-memory row kernel of later calls on the
+ * current device withholds the bulk copy of the j-th row its first CTA takes
+ * (j < 0: none, the default). Nothing then completes that buffer's
+ * barrier: the CTA's bounded waits give up (within about a second), its rows
+ * from that one on are reported SPEC_ETIMEOUT in status[] (outputs -1), the
+ * other CTAs' rows are verified as usual, and the device stays usable. It
+ * exercises the timeout path without a fault. Returns 0; -1 in release
+ * builds (nothing is changed) or on a CUDA error. */
+int spec_debug_withhold_copy(int j);
 
 /* Library ABI version (major * 100 + minor). */
 int spec_version(void);

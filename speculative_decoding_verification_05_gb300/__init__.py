@@ -39,7 +39,7 @@ EXPORTED = [
     "spec_verify_mentor_workspace_size", "spec_verify_mentor",
     "spec_sample_workspace_size", "spec_sample",
     "spec_philox_uniform", "spec_verify_noalloc", "spec_status_string", "spec_last_cuda_error",
-    "spec_version", "spec_debug_build", "spec_debug_failures",
+    "spec_version", "spec_debug_build", "spec_debug_failures", "spec_debug_withhold_copy",
 ]
 
 
@@ -122,6 +122,8 @@ def load_library(path=None):
         lib.spec_debug_build.restype = _I
         lib.spec_debug_failures.argtypes = [_P]
         lib.spec_debug_failures.restype = _I
+        lib.spec_debug_withhold_copy.argtypes = [_I]
+        lib.spec_debug_withhold_copy.restype = _I
         _libs[path] = lib
         return lib
 

@@ -57,6 +57,9 @@ constexpr int kElemCap = kKeptRegionCap; // window logits gathered per sum warp 
 constexpr int kOrdBins = 1024;           // distinct bf16 values below the maximum counted
 constexpr int kPrefetchAhead = 2;        // rows prefetched into L2 ahead of their copies
 constexpr uint32_t kChunk = 32768;       // bytes per bulk copy or prefetch
+#ifdef SPEC_DEBUG
+static __device__ int g_withhold = -1;   // spec_debug_withhold_copy
+#endif
 constexpr uint32_t kSuspendNs = 20000;   // longest suspension of one poll of a wait
 constexpr uint32_t kWaitPolls = 1u << 16;  // polls before a wait gives up (about a second)
 constexpr unsigned kKeyNaN = 0xFFFFu;    // row maximum key of a row holding a NaN
@@ -633,13 +636,17 @@ __global__ void __launch_bounds__(kRowThreads, 1) smem_row_kernel(const __grid_c
     } else if (warp == kCopyWarp && lane == 0) {
         // ---- copy lane ----
         uint32_t issued = 0u;  // per slot s, bits 2s and 2s + 1: a copy issued, the parity of the last
-        for (RowWalk w(0, 1, R, nbuf); w.row < nrows; w.next()) {
+        int jc = 0;
+        for (RowWalk w(0, 1, R, nbuf); w.row < nrows; w.next(), ++jc) {
             const int s = w.s;
             const uint32_t u = w.u;
             if (u > 0 && !mbar_wait(&empty[s], (u - 1u) & 1u, abort_v)) {
                 *abort_v = 1;
                 break;
             }
+#ifdef SPEC_DEBUG
+            if (blockIdx.x == 0 && jc == g_withhold) continue;  // the buffer is never filled
+#endif
             fence_proxy_async();
             mbar_expect_tx(&full[s], bytes);
             const char* src = reinterpret_cast<const char*>(row_src(p, w.b, w.r));
@@ -1099,3 +1106,12 @@ cudaError_t launch_smem_draws(const RowParams& p, int sms, cudaStream_t stream) 
 SV_DEBUG_READER(rows_smem)
 
 }  // namespace sv
+
+extern "C" int spec_debug_withhold_copy(int j) {
+#ifdef SPEC_DEBUG
+    return cudaMemcpyToSymbol(sv::g_withhold, &j, sizeof(int)) == cudaSuccess ? 0 : -1;
+#else
+    (void)j;
+    return -1;
+#endif
+}

@@ -99,3 +99,38 @@ def test_other_entry_points(dbg, V):
     root = torch.tensor([1, 2, 0], dtype=torch.int32)
     rel, deb = _both(lambda: sv.tree_build(torch.from_numpy(cand).cuda(), root.cuda(), max(V, 8), 16))
     _same(rel, deb, ("node_tokens", "parent", "depth", "mask", "n_nodes", "status"))
+
+
+def test_a_withheld_copy_times_out_and_the_device_stays_usable(dbg):
+    """The first CTA of the shared-memory row kernel withholds the copy of its
+    second row: nothing completes that buffer's barrier, the CTA's bounded
+    waits give up, the rows it had left (rows 1 x grid, 2 x grid, ...) are
+    reported as timed out, every other sequence is verified as the release
+    library verifies it, and the next call (copy no longer withheld) is
+    complete and correct."""
+    B, G, V = 60, 4, 32000
+    zt, zd = workloads.linear_logits(B, G, V, 77, dtype="bf16", sd_t=3.0, sd_d=0.5, boost=6.0, boost_p=0.01)
+    drafts = torch.from_numpy(oracle.sample(zd, 0.8, 0.95, 0, seed=3)["tokens"]).int().cuda()
+    zt, zd = zt.cuda(), zd.cuda()
+    rel = sv.verify(zt, zd, drafts, 0.8, 0.95, 0, 4, 0)
+    rows, R = B * (2 * G + 1), 2 * G + 1
+    grid = min(rows, torch.cuda.get_device_properties(0).multi_processor_count)
+    lost = sorted({r // R for r in range(grid, rows, grid)})
+    assert lost, "the first CTA must take more than one row"
+    assert dbg.spec_debug_withhold_copy(1) == 0
+    try:
+        with sv.use_library(sv.DEBUG_LIB_PATH):
+            got = sv.verify(zt, zd, drafts, 0.8, 0.95, 0, 4, 0)
+        torch.cuda.synchronize()
+    finally:
+        assert dbg.spec_debug_withhold_copy(-1) == 0
+    st = np_(got["status"])
+    assert (st[lost] == 3).all(), st[lost]  # SPEC_ETIMEOUT
+    assert (np_(got["accepted"])[lost] == -1).all()
+    keep = np.setdiff1d(np.arange(B), lost)
+    assert (st[keep] == 0).all()
+    for k in ("accepted", "tokens", "next_token"):
+        np.testing.assert_array_equal(np_(got[k])[keep], np_(rel[k])[keep], err_msg=k)
+    rel2, deb2 = _both(lambda: sv.verify(zt, zd, drafts, 0.8, 0.95, 0, 4, 0))
+    _same(rel2, deb2, ("accepted", "tokens", "next_token", "status"))
+    assert (np_(deb2["status"]) == 0).all()
