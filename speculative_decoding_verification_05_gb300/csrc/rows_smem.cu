@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(kRowThreads, 1) smem_row_kernel(const __grid_c
 
             // S against m, and the vectors holding a window logit listed in
             // ascending order (rounds of 32 consecutive vectors, lanes in
-            // order); two rounds per step
+            // order)
             float S = 0.f;
             int nv = 0, cn = 0, jm = -1;
             if (!bad) {
@@ -416,16 +416,20 @@ __global__ void __launch_bounds__(kRowThreads, 1) smem_row_kernel(const __grid_c
                     }
                 };
                 const uint4 ninf = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
-                for (int base = v0; base < v1; base += 64) {
-                    const int va = base + lane, vb = va + 32;
-                    const uint4 xa = va < v1 ? vr[va] : ninf;
-                    const uint4 xb = vb < v1 ? vr[vb] : ninf;
+                int base = v0;
+                for (; base + 32 <= v1; base += 32) {
+                    const int va = base + lane;
+                    const uint4 xa = vr[va];
                     const uint32_t ma = bmax2(bmax2(xa.x, xa.y), bmax2(xa.z, xa.w));
-                    const uint32_t mb = bmax2(bmax2(xb.x, xb.y), bmax2(xb.z, xb.w));
                     note(bmax2(ma, cut2) != cut2, va);
-                    note(bmax2(mb, cut2) != cut2, vb);
                     sum8(xa);
-                    sum8(xb);
+                }
+                if (base < v1) {  // the last, partial round: missing vectors read as -inf
+                    const int va = base + lane;
+                    const uint4 xa = va < v1 ? vr[va] : ninf;
+                    const uint32_t ma = bmax2(bmax2(xa.x, xa.y), bmax2(xa.z, xa.w));
+                    note(bmax2(ma, cut2) != cut2, va);
+                    sum8(xa);
                 }
                 const float2 t2 = __fadd2_rn(s0, s1);
                 S = t2.x + t2.y;
