@@ -32,6 +32,8 @@
 // from q_gamma) runs last, one warp per sequence, from the row records and
 // kept lists.
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "draw.cuh"
 #include "select.cuh"
@@ -677,28 +679,34 @@ __global__ void __launch_bounds__(kRowThreads, 1) smem_row_kernel(const __grid_c
     __syncthreads();
 }
 
-// The queued rows: one CTA per row (taken from a counter) counts the row's
-// logits per distinct bf16 value (a 16-bit counter for every bf16 ordinal,
-// 128 KB of shared memory; one pass of 16-byte loads), then scans the counts
-// from the largest value down. A value's mass is its count times the
-// fixed-point mass of the value (the integers select.cuh sums element by
-// element), so the threshold is the one of select.cuh's selection over the
-// row. Thread t owns the 256 values of descending rank [256 t, 256 t + 256);
-// a block scan of the threads' totals places them, and the thread holding the
-// crossing is found; then every thread takes one value of that range and a
-// second block scan finds the value itself. Completes the row's record (threshold and kept
-// mass; no window list, so a draw from it reads the rows). Rows here are
-// shorter than 65536, so no count reaches 2^16.
+// The queued rows: one thread-block cluster of kFbCluster CTAs per row
+// (taken from a counter). The row's logits are counted per distinct bf16
+// value (a 16-bit counter per value), the value range split over the
+// cluster: CTA r reads the whole row (from L2 after the first reader) and
+// counts the values of descending rank [r kFbRange, (r + 1) kFbRange). A
+// value's mass is its count times the fixed-point mass of the value (the
+// integers select.cuh sums element by element), so the threshold is the one
+// of select.cuh's selection over the row. Each CTA totals its range (thread
+// t owns kFbPer consecutive values, a block scan places the threads); the
+// CTAs read one another's totals from distributed shared memory to place
+// their ranges; the thread holding the crossing walks its values, and its
+// CTA posts the result, which every CTA reads back through distributed
+// shared memory. Completes the row's record (threshold and kept mass; no
+// window list, so a draw from it reads the rows). Rows here are shorter than
+// 65536, so no count reaches 2^16. All CTAs of a cluster take the same jobs
+// and the same branches, so every cluster barrier completes.
 constexpr int kFbValues = 65536;
-constexpr int kFbPer = kFbValues / NT;  // values per thread (== NT: the walk takes one per thread)
-static_assert(kFbPer == NT, "one value of a thread's range per thread");
+constexpr int kFbCluster = 8;
+constexpr int kFbRange = kFbValues / kFbCluster;  // values per CTA
+constexpr int kFbPer = kFbRange / NT;             // values per thread
+static_assert(kFbPer == 32, "one value per lane of a warp in the totals loop");
 
 struct FallbackShared {
-    unsigned long long wc[NW], ww[NW];  // block scans: per-warp totals
-    int hit;                            // the thread (then the value) holding the crossing
-    unsigned long long hc, hw;          // the weights before that thread's range
-    unsigned long long hw2;             // the mass through the crossing
-    int job;
+    unsigned long long wc[NW], ww[NW];  // block scan: per-warp totals
+    unsigned long long cc, cw;          // this CTA's range totals (read by the cluster)
+    int hit;                            // the crossing found in this CTA (descending rank), -1: none
+    unsigned long long hw;              // the mass through it
+    int job;                            // (rank 0) the row taken
 };
 
 // Inclusive scan of two 64-bit values in thread order over the CTA.
@@ -725,35 +733,38 @@ SV_DEV void block_scan2(FallbackShared& s, unsigned long long& a, unsigned long 
     }
 }
 
-__global__ void __launch_bounds__(NT) smem_fallback_kernel(const __grid_constant__ RowParams p) {
-    extern __shared__ __align__(16) uint32_t fcnt[];  // two 16-bit counts a word, by ordinal
+__global__ void __cluster_dims__(kFbCluster, 1, 1) __launch_bounds__(NT)
+    smem_fallback_kernel(const __grid_constant__ RowParams p) {
+    __shared__ uint32_t fcnt[kFbRange / 2];  // this CTA's values, two 16-bit counts a word
     __shared__ FallbackShared s;
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
+    const int rank = (int)cl.block_rank();
     const int tid = threadIdx.x, lane = tid & 31;
     const int V = p.V, nvec = V >> 3;
     const float c2 = p.c2;
     const long long nrows = (long long)p.B * p.rows_per_b;
     (void)nrows;  // bounds of the debug build's checks
     const unsigned nq = __ldcg(p.work + 3);
-    // rank d = kFbValues - 1 - ordinal: descending values
-    const auto count_of = [&](int d) {
-        const int o = kFbValues - 1 - d;
-        return (fcnt[o >> 1] >> ((o & 1) * 16)) & 0xFFFFu;
-    };
+    const int r0 = rank * kFbRange;  // this CTA's first descending rank
+    // local value l of this CTA: descending rank r0 + l, ordinal kFbValues - 1 - (r0 + l)
+    const auto count_of = [&](int l) { return (fcnt[l >> 1] >> ((l & 1) * 16)) & 0xFFFFu; };
     for (;;) {
-        if (tid == 0) s.job = (int)atomicAdd(p.work + 4, 1u);
-        __syncthreads();
-        const int qi = s.job;
-        if (qi >= (int)nq) break;
+        if (rank == 0 && tid == 0) s.job = (int)atomicAdd(p.work + 4, 1u);
+        cl.sync();
+        const int qi = *cl.map_shared_rank(&s.job, 0);
+        cl.sync();  // every CTA has read the job (rank 0 may now exit or take the next)
+        if (qi >= (int)nq) break;  // (the same for every CTA of the cluster)
         const int row = SV_IN(qi, nrows) ? __ldcg(p.fb_rows + qi) : 0;
         RowRec* rec = p.rows + row;
         const float m = __ldcg(&rec->m), S = __ldcg(&rec->S);
         const float mc = m * c2;
-        for (int i = tid; i < kFbValues / 8; i += NT) reinterpret_cast<uint4*>(fcnt)[i] = make_uint4(0u, 0u, 0u, 0u);
+        for (int i = tid; i < kFbRange / 8; i += NT) reinterpret_cast<uint4*>(fcnt)[i] = make_uint4(0u, 0u, 0u, 0u);
         __syncthreads();
         const uint4* src = reinterpret_cast<const uint4*>(row_src(p, row / p.rows_per_b, row % p.rows_per_b));
         const auto add = [&](uint32_t raw) {
-            const uint32_t o = ord16(raw);
-            atomicAdd(&fcnt[o >> 1], 1u << ((o & 1u) * 16));
+            const int l = kFbValues - 1 - (int)ord16(raw) - r0;
+            if ((unsigned)l < (unsigned)kFbRange) atomicAdd(&fcnt[l >> 1], 1u << ((l & 1) * 16));
         };
 #pragma unroll 4
         for (int v = tid; v < nvec; v += NT) {
@@ -768,61 +779,69 @@ __global__ void __launch_bounds__(NT) smem_fallback_kernel(const __grid_constant
             add(x.w >> 16);
         }
         __syncthreads();
-        // this thread's values: totals of count and mass (each lane starts
-        // at its own offset in its range, so the warp's reads fall in
-        // different banks), then the threads' places by a block scan
-        const int d0 = tid * kFbPer;
-        const auto mass_of = [&](int d, unsigned c) {
+        // this thread's values: totals (each lane starts at its own offset,
+        // so a warp's reads fall in different banks), the threads' places in
+        // the CTA, then the CTAs' places in the cluster
+        const int l0 = tid * kFbPer;
+        const auto mass_of = [&](int l, unsigned c) {
             return (unsigned long long)c *
-                   fx_of(fmaf(ord16_value((uint32_t)(kFbValues - 1 - d)), c2, -mc));
+                   fx_of(fmaf(ord16_value((uint32_t)(kFbValues - 1 - (r0 + l))), c2, -mc));
         };
         unsigned long long tc = 0ull, tw = 0ull;
         for (int i = 0; i < kFbPer; ++i) {
-            const int d = d0 + ((i + 2 * lane) & (kFbPer - 1));
-            const unsigned c = count_of(d);
+            const int l = l0 + ((i + lane) & (kFbPer - 1));
+            const unsigned c = count_of(l);
             if (c) {
                 tc += c;
-                tw += mass_of(d, c);
+                tw += mass_of(l, c);
             }
         }
         unsigned long long ec = tc, ew = tw;
-        block_scan2(s, ec, ew);  // inclusive, thread order
+        block_scan2(s, ec, ew);
+        if (tid == NT - 1) {
+            s.cc = ec;
+            s.cw = ew;
+        }
         ec -= tc;
         ew -= tw;
-        // the first rank d <= dlim whose running weight reaches the target,
-        // and the mass through it (-1 if none): the thread whose range holds
-        // it is found first, then all threads take one value of that range
-        // each (a block scan in rank order) and the first that reaches the
-        // target reports it
+        cl.sync();  // every CTA's totals are posted
+        for (int q = 0; q < rank; ++q) {
+            ec += *cl.map_shared_rank(&s.cc, q);
+            ew += *cl.map_shared_rank(&s.cw, q);
+        }
+        // the first descending rank d <= dlim whose running weight reaches
+        // the target, and the mass through it (-1 if none), the same in
+        // every CTA of the cluster
         const auto find = [&](bool by_count, unsigned long long target, int dlim, unsigned long long* wo) {
             if (tid == 0) s.hit = -1;
             __syncthreads();
-            if ((by_count ? ec : ew) < target && (by_count ? ec + tc : ew + tw) >= target && d0 <= dlim) {
-                s.hit = tid;
-                s.hc = ec;
-                s.hw = ew;
+            if ((by_count ? ec : ew) < target && (by_count ? ec + tc : ew + tw) >= target && r0 + l0 <= dlim) {
+                unsigned long long c = ec, w = ew;
+                for (int l = l0; l < l0 + kFbPer && r0 + l <= dlim; ++l) {
+                    const unsigned k = count_of(l);
+                    if (!k) continue;
+                    c += k;
+                    w += mass_of(l, k);
+                    if ((by_count ? c : w) >= target) {
+                        s.hit = r0 + l;
+                        s.hw = w;
+                        break;
+                    }
+                }
             }
-            __syncthreads();
-            const int t = s.hit;
-            if (t < 0) return -1;
-            const int d = t * kFbPer + tid;  // kFbPer == NT: one value per thread
-            const unsigned k = d <= dlim ? count_of(d) : 0u;
-            unsigned long long c = k, w = k ? mass_of(d, k) : 0ull;
-            const unsigned long long c1 = c, w1 = w;
-            block_scan2(s, c, w);
-            c += s.hc;
-            w += s.hw;
-            if (tid == 0) s.hit = NT;
-            __syncthreads();
-            if (k && (by_count ? c : w) >= target && (by_count ? c - c1 : w - w1) < target) {
-                s.hit = tid;  // the one value where the running weight first reaches the target
-                s.hw2 = w;
+            cl.sync();  // every CTA's result is posted
+            int d = -1;
+            unsigned long long w = 0ull;
+            for (int q = 0; q < kFbCluster; ++q) {
+                const int h = *cl.map_shared_rank(&s.hit, q);
+                if (h >= 0) {
+                    d = h;
+                    w = *cl.map_shared_rank(&s.hw, q);
+                }
             }
-            __syncthreads();
-            const int j = s.hit;
-            *wo = s.hw2;
-            __syncthreads();
-            return j < NT ? t * kFbPer + j : -1;
+            cl.sync();  // every CTA has read the results before they are reset
+            *wo = w;
+            return d;
         };
         unsigned long long kept = (unsigned long long)(S * kFx);
         float thr = -INFINITY;
@@ -844,11 +863,11 @@ __global__ void __launch_bounds__(NT) smem_fallback_kernel(const __grid_constant
                 kept = w;
             }
         }
-        if (tid == 0) {
+        if (rank == 0 && tid == 0) {
             rec->thr = thr;
             rec->Sk = (float)kept * (1.0f / kFx);
         }
-        __syncthreads();  // the counts and the shared state are free for the next row
+        cl.sync();  // the counts, the shared state and rank 0's job are free for the next row
     }
 }
 
@@ -1082,12 +1101,8 @@ cudaError_t launch_smem_rows(const RowParams& p, int nbuf, size_t smem, int sms,
     const int grid = (int)(rows < sms ? rows : sms);
     smem_row_kernel<<<grid, kRowThreads, smem, stream>>>(p, nbuf);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    // the queued rows (usually none: the CTAs find the queue empty and exit)
-    const size_t fb = (size_t)kFbValues * 2;  // a 16-bit count per bf16 value
-    if ((e = cudaFuncSetAttribute(smem_fallback_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fb)) !=
-        cudaSuccess)
-        return e;
-    smem_fallback_kernel<<<sms, NT, fb, stream>>>(p);
+    // the queued rows (usually none: the clusters find the queue empty and exit)
+    smem_fallback_kernel<<<std::max(kFbCluster, sms / kFbCluster * kFbCluster), NT, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
