@@ -257,7 +257,7 @@ enum RowMode : int { kModeVerify = 0, kModeMentor = 1, kModeSample = 2 };
 enum Transform : int { kXfTopK = 1, kXfTopP = 2 };
 
 // One record per logit row (workspace), written by the CTA that completes the row.
-struct RowRec {
+struct alignas(16) RowRec {
     float m;      // row maximum
     float S;      // sum of exp2((z - m) log2e / T) over the row
     float thr;    // kept set: z >= thr (-inf: the whole row)
@@ -265,7 +265,7 @@ struct RowRec {
     float zx;     // the draft token's logit in this row (rows with a token)
     int32_t x;    // the draft token (rows with a token), else -1
     int32_t flags;  // kRecEData, kRecTimeout
-    int32_t nkept;  // shared-memory row path, target rows: entries of the kept list (-1: none)
+    int32_t nkept;  // shared-memory row path, target rows: entries of the window list (-1: none)
 };
 
 // Partial statistics of one segment of a long row.

@@ -252,16 +252,21 @@ SV_DEV int draw_residual(DrawShared& ds, const E* rt, const E* rd, int V, const 
     return draw_q<E, kVec>(ds, rt, V, t, c2, u);
 }
 
+// Records are 32 bytes on 16-byte boundaries of the workspace: two 16-byte
+// loads (cached in L2 only: records written earlier in the same kernel).
+static_assert(sizeof(RowRec) == 32, "row records are two 16-byte words");
 SV_DEV RowRec load_rec(const RowRec* src) {
+    const uint4 a = __ldcg(reinterpret_cast<const uint4*>(src));
+    const uint4 b = __ldcg(reinterpret_cast<const uint4*>(src) + 1);
     RowRec q;
-    q.m = __ldcg(&src->m);
-    q.S = __ldcg(&src->S);
-    q.thr = __ldcg(&src->thr);
-    q.Sk = __ldcg(&src->Sk);
-    q.zx = __ldcg(&src->zx);
-    q.x = __ldcg(&src->x);
-    q.flags = __ldcg(&src->flags);
-    q.nkept = __ldcg(&src->nkept);
+    q.m = __uint_as_float(a.x);
+    q.S = __uint_as_float(a.y);
+    q.thr = __uint_as_float(a.z);
+    q.Sk = __uint_as_float(a.w);
+    q.zx = __uint_as_float(b.x);
+    q.x = (int32_t)b.y;
+    q.flags = (int32_t)b.z;
+    q.nkept = (int32_t)b.w;
     return q;
 }
 
