@@ -875,88 +875,155 @@ __global__ void __cluster_dims__(kFbCluster, 1, 1) __launch_bounds__(NT)
 
 // Inverse CDF by one warp over a window list of K entries in order: flat
 // position j lies in region r (off[r] <= j < off[r] + cnt[r]) at entry
-// e = r kKeptRegionCap + j - off[r], with weight wf(e). The result is the
-// entry of the smallest j with C_j > u W (C the inclusive prefix sum, W the
-// total), or, if rounding leaves none, of the last j with positive weight;
-// -1 when W = 0. Lane l owns positions [l per, (l + 1) per); sums run in a
-// fixed order (each lane in order, then the lanes in order). Every lane of
-// the warp calls it and gets the result.
-template <typename WF>
-SV_DEV int warp_list_draw(int K, const int* cnt, const int* off, float u, const WF& wf, float* W_out) {
+// e = r kKeptRegionCap + j - off[r] of le, which holds (index << 16) | raw
+// target logit; its weight is wf(zt, fetch(entry)), fetch giving the draft
+// logit where the weight needs one. The result is the index of the
+// smallest j with C_j > u W (C the inclusive prefix sum, W the total), or,
+// if rounding leaves none, of the last j with positive weight; -1 when
+// W = 0. The positions go in rounds of 32 (lane l takes position 32 s + l
+// of round s), kDrawBatch rounds at a time so that their list loads, and
+// then their gathers, are in flight together; the first batch stays in
+// registers for the second pass, later batches are loaded again. W adds the
+// rounds' butterfly totals in round order (the same value in every lane); C
+// adds the rounds' scans in round order. Every lane of the warp calls it
+// and gets the result.
+constexpr int kDrawBatch = 8;
+
+template <typename FETCH, typename WF>
+SV_DEV int warp_list_draw(int K, const int* off, const uint32_t* le, float u, const FETCH& fetch, const WF& wf,
+                          float* W_out) {
     const int lane = threadIdx.x & 31;
-    const int per = (K + 31) / 32;
-    const int j0 = min(K, lane * per), j1 = min(K, j0 + per);
-    // region and place of position j0; then stepping through the entries
-    int r0 = 0;
-    while (r0 < kKeptRegions - 1 && off[r0 + 1] <= j0) ++r0;
-    const int i0 = j0 - off[r0];
-    const auto step = [&](int& r, int& i) {
-        ++i;
-        while (r < kKeptRegions - 1 && i >= cnt[r]) {
-            ++r;
-            i = 0;
-        }
-    };
-    float ts = 0.f;
-    {
-        int r = r0, i = i0;
-        for (int j = j0; j < j1; ++j, step(r, i)) ts += wf(r * kKeptRegionCap + i);
-    }
-    float W;
-    const float lpre = warp_seq_exclusive(ts, &W);
-    *W_out = W;
-    const float t = u * W;
-    // the crossing lane: the last one whose range starts at or below t and holds weight
-    const unsigned mm = __ballot_sync(0xFFFFFFFFu, lpre <= t && ts > 0.f);
-    if (!mm) return -1;
-    const int ol = 31 - __clz(mm);
-    int e = -1;
-    if (lane == ol) {
-        const float tt = t - lpre;
-        float c = 0.f;
-        int last = -1, r = r0, i = i0;
-        for (int j = j0; j < j1; ++j, step(r, i)) {
-            const int ej = r * kKeptRegionCap + i;
-            const float w = wf(ej);
-            if (w > 0.f) last = ej;
-            c += w;
-            if (w > 0.f && c > tt) {
-                e = ej;
-                break;
+    const int ns = (K + 31) >> 5;
+    // weights and entries of rounds s0 .. s0 + kDrawBatch - 1 (0 past K); rg
+    // is the lane's region cursor, which only moves forward
+    const auto batch = [&](int s0, int& rg, float(&w)[kDrawBatch], uint32_t(&en)[kDrawBatch]) {
+        int e[kDrawBatch];
+#pragma unroll
+        for (int q = 0; q < kDrawBatch; ++q) {
+            const int j = (s0 + q) * 32 + lane;
+            e[q] = -1;
+            if (j < K) {
+                while (rg < kKeptRegions - 1 && off[rg + 1] <= j) ++rg;
+                e[q] = rg * kKeptRegionCap + j - off[rg];
             }
         }
-        if (e < 0) e = last;
+#pragma unroll
+        for (int q = 0; q < kDrawBatch; ++q) en[q] = e[q] >= 0 ? __ldg(le + e[q]) : 0u;
+        float zd[kDrawBatch];
+#pragma unroll
+        for (int q = 0; q < kDrawBatch; ++q) zd[q] = e[q] >= 0 ? fetch(en[q]) : 0.f;
+#pragma unroll
+        for (int q = 0; q < kDrawBatch; ++q) w[q] = e[q] >= 0 ? wf(__uint_as_float(en[q] << 16), zd[q]) : 0.f;
+    };
+    const auto round_total = [](float v) {
+        // (lanes l and l ^ o add the same two values, so every lane ends with the same total)
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+        return v;
+    };
+    float wk[kDrawBatch];
+    uint32_t ek[kDrawBatch];
+    int rg = 0;
+    batch(0, rg, wk, ek);
+    float W = 0.f;
+#pragma unroll
+    for (int q = 0; q < kDrawBatch; ++q) W += round_total(wk[q]);
+    for (int s0 = kDrawBatch; s0 < ns; s0 += kDrawBatch) {
+        float w[kDrawBatch];
+        uint32_t en[kDrawBatch];
+        batch(s0, rg, w, en);
+#pragma unroll
+        for (int q = 0; q < kDrawBatch; ++q) W += round_total(w[q]);
     }
-    return __shfl_sync(0xFFFFFFFFu, e, ol);
+    *W_out = W;
+    if (!(W > 0.f)) return -1;
+    const float t = u * W;
+    float base = 0.f;  // C before the round
+    int last = -1;     // the index of the last entry with positive weight so far
+    // the index at the crossing in a round (the same in every lane), or -1
+    const auto cross = [&](float w, uint32_t en) {
+        float c = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xFFFFFFFFu, c, o);
+            if (lane >= o) c += y;
+        }
+        c += base;
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, w > 0.f && c > t);
+        const unsigned pos = __ballot_sync(0xFFFFFFFFu, w > 0.f);
+        if (pos) last = (int)(__shfl_sync(0xFFFFFFFFu, en, 31 - __clz(pos)) >> 16);
+        base = __shfl_sync(0xFFFFFFFFu, c, 31);
+        return hit ? (int)(__shfl_sync(0xFFFFFFFFu, en, __ffs(hit) - 1) >> 16) : -1;
+    };
+#pragma unroll
+    for (int q = 0; q < kDrawBatch; ++q) {
+        const int r = cross(wk[q], ek[q]);
+        if (r >= 0) return r;
+    }
+    rg = 0;
+    for (int s0 = kDrawBatch; s0 < ns; s0 += kDrawBatch) {
+        float w[kDrawBatch];
+        uint32_t en[kDrawBatch];
+        batch(s0, rg, w, en);
+#pragma unroll
+        for (int q = 0; q < kDrawBatch; ++q) {
+            const int r = cross(w[q], en[q]);
+            if (r >= 0) return r;
+        }
+    }
+    return last;
 }
 
-// One warp per sequence (taken from a counter): the acceptance tests of all
-// positions at once (one lane each), the first rejection n, the accepted
-// prefix, and the draw from the kept list of target row n. A sequence whose
-// kept list did not fit is queued (p.seq_n, counted in p.work[0]) for
-// smem_fulldraw_kernel, which draws from the rows.
-__global__ void __launch_bounds__(NT) smem_draw_kernel(const __grid_constant__ RowParams p) {
-    __shared__ int rcnt[NW][kKeptRegions], roff[NW][kKeptRegions];
+// A lane's row record, read by every lane of the warp.
+SV_DEV RowRec shfl_rec(const RowRec& r, int src) {
+    RowRec o;
+    o.m = __shfl_sync(0xFFFFFFFFu, r.m, src);
+    o.S = __shfl_sync(0xFFFFFFFFu, r.S, src);
+    o.thr = __shfl_sync(0xFFFFFFFFu, r.thr, src);
+    o.Sk = __shfl_sync(0xFFFFFFFFu, r.Sk, src);
+    o.zx = __shfl_sync(0xFFFFFFFFu, r.zx, src);
+    o.x = __shfl_sync(0xFFFFFFFFu, r.x, src);
+    o.flags = __shfl_sync(0xFFFFFFFFu, r.flags, src);
+    o.nkept = __shfl_sync(0xFFFFFFFFu, r.nkept, src);
+    return o;
+}
+
+// One warp per sequence (warp w of the grid takes sequences w, w + warps,
+// ...): the acceptance tests of all positions at once (lane k loads target
+// record k and draft record k, 32 positions a round), the first rejection
+// n, the accepted prefix, and the draw from the window list of target row
+// n, whose record and region sizes the warp already holds (the region sizes
+// of every target row of the sequence are loaded with the records), so
+// that only the list and the draft logits it names are loaded after n is
+// known. A sequence whose target row has no usable list (a fallback row, or
+// a region of the list overflowed) is queued (p.seq_n, counted in
+// p.work[0]) for smem_fulldraw_kernel, which draws from the rows.
+__global__ void __launch_bounds__(NT, 4) smem_draw_kernel(const __grid_constant__ RowParams p) {
+    __shared__ int roff[NW][kKeptRegions];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int R = p.rows_per_b, G = p.gamma;
     const float c2 = p.c2;
-    for (;;) {
-        int b = 0;
-        if (lane == 0) b = (int)atomicAdd(p.work + 1, 1u);
-        b = __shfl_sync(0xFFFFFFFFu, b, 0);
-        if (b >= p.B) break;
+    const int cw = 3 * (G + 1);  // 4-byte words of region sizes of a sequence's target rows
+    static_assert(kKeptRegions == 12, "region sizes of a row: three 4-byte words");
+    for (long long bb = (long long)blockIdx.x * NW + warp; bb < p.B; bb += (long long)gridDim.x * NW) {
+        const int b = (int)bb;
         const RowRec* rb = p.rows + (size_t)b * R;
+        const size_t trow0 = (size_t)b * (G + 1);
+        const uint32_t* kwp = reinterpret_cast<const uint32_t*>(p.kept_cnt + trow0 * kKeptRegions);
+        const uint32_t kw =
+            (p.kept_cnt && lane < cw && SV_IN(trow0 * 3 + lane, (long long)p.B * cw)) ? __ldcg(kwp + lane) : 0u;
         // acceptance at every position (lenience l scales the draft
-        // probability; l = 1 is the exact method); n = the first rejection
-        int flags = 0;
-        for (int i = lane; i < R; i += 32) flags |= __ldcg(&rb[i].flags);
-        flags = __reduce_or_sync(0xFFFFFFFFu, flags);
-        int n = G;
-        for (int k0 = 0; k0 < G; k0 += 32) {
+        // probability; l = 1 is the exact method); n = the first rejection,
+        // tn and dn its target and draft records
+        int flags = 0, n = -1, x0 = -1;
+        RowRec tn{}, dn{};
+        for (int k0 = 0; k0 <= G; k0 += 32) {
             const int k = k0 + lane;
+            RowRec t{}, d{};
+            if (k <= G) t = load_rec(rb + k);
+            if (k < G) d = load_rec(rb + G + 1 + k);
             bool rej = false;
             if (k < G) {
-                const RowRec t = load_rec(rb + k), d = load_rec(rb + G + 1 + k);
                 const float q = KeptExp{t.thr, c2, t.m * c2, 1.f}(t.zx) / t.Sk;
                 const float pd = KeptExp{d.thr, c2, d.m * c2, 1.f}(d.zx) / d.Sk;
                 if (p.probs_dbg) {
@@ -966,9 +1033,16 @@ __global__ void __launch_bounds__(NT) smem_draw_kernel(const __grid_constant__ R
                 const float u = uniform01(p.seed, p.offset + (uint64_t)b, (uint32_t)k, kPurposeAccept);
                 rej = !accept_test(u, q, p.lenience * pd);
             }
+            flags |= t.flags | d.flags;
+            if (k0 == 0) x0 = t.x;
             const unsigned m = __ballot_sync(0xFFFFFFFFu, rej);
-            if (m && n == G) n = k0 + __ffs(m) - 1;
+            if (n < 0 && (m || k0 + 32 > G)) {
+                n = m ? k0 + __ffs(m) - 1 : G;
+                tn = shfl_rec(t, n - k0);
+                dn = shfl_rec(d, n - k0);
+            }
         }
+        flags = __reduce_or_sync(0xFFFFFFFFu, flags);
         const int stt = (flags & kRecTimeout) ? kETimeout : ((flags & kRecEData) ? kEData : kOk);
         if (lane == 0) {
             p.accepted[b] = stt ? -1 : n;
@@ -976,67 +1050,67 @@ __global__ void __launch_bounds__(NT) smem_draw_kernel(const __grid_constant__ R
             if (p.status) p.status[b] = stt;
         }
         for (int j = lane; j <= G; j += 32)
-            if ((stt || j != n) && SV_IN_SEQ((size_t)b * (G + 1) + j, (long long)p.B * (G + 1), p.status, b))
-                p.tokens[(size_t)b * (G + 1) + j] = (!stt && j < n) ? __ldcg(&rb[j].x) : -1;
+            if ((stt || j != n) && SV_IN_SEQ(trow0 + j, (long long)p.B * (G + 1), p.status, b))
+                p.tokens[trow0 + j] = (!stt && j < n) ? (j < 32 ? x0 : __ldcg(&rb[j].x)) : -1;
         if (stt) continue;
-        const RowRec t = load_rec(rb + n);
-        if (t.nkept < 0 || !SV_IN_SEQ(t.nkept, p.kept_cap + 1, p.status, b)) {
+        if (tn.nkept < 0 || !SV_IN_SEQ(tn.nkept, p.kept_cap + 1, p.status, b)) {
             if (lane == 0) p.seq_n[atomicAdd(p.work, 1u)] = b;  // drawn from the rows afterwards
             continue;
         }
         // from the window list of target row n (every index with q > 0
-        // lies in it; entries below the threshold weigh 0)
-        const size_t trow = (size_t)b * (G + 1) + n;
+        // lies in it; entries below the threshold weigh 0): its region
+        // sizes (bytes 12 n .. 12 n + 11 of the sequence's), their offsets
         {
-            const int c = lane < kKeptRegions ? (int)__ldcg(p.kept_cnt + trow * kKeptRegions + lane) : 0;
+            int c;
+            if (cw <= 32) {
+                const uint32_t wv = __shfl_sync(0xFFFFFFFFu, kw, min(3 * n + (lane >> 2), 31));
+                c = lane < kKeptRegions ? (int)((wv >> ((lane & 3) * 8)) & 0xFFu) : 0;
+            } else {
+                c = lane < kKeptRegions ? (int)__ldcg(p.kept_cnt + (trow0 + n) * kKeptRegions + lane) : 0;
+            }
             int o = c;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
                 const int y = __shfl_up_sync(0xFFFFFFFFu, o, d);
                 if (lane >= d) o += y;
             }
-            if (lane < kKeptRegions) {
-                rcnt[warp][lane] = c;
-                roff[warp][lane] = o - c;
-            }
+            if (lane < kKeptRegions) roff[warp][lane] = o - c;
             __syncwarp();
         }
         const float u2 = uniform01(p.seed, p.offset + (uint64_t)b, (uint32_t)n, kPurposeResample);
-        const size_t lb = trow * (size_t)p.kept_cap;
-        // (the list was written by the previous kernel: read-only loads through
-        // L1, so the crossing lane's second walk over its entries hits L1)
-        const uint32_t* le = p.kept + lb;  // (index << 16) | raw
+        // (the list was written by the previous kernel: read-only loads)
+        const uint32_t* le = p.kept + (trow0 + n) * (size_t)p.kept_cap;  // (index << 16) | raw
+        const RowRec& t = tn;
         const KeptExp q1{t.thr, c2, t.m * c2, 1.f};
-        const auto wq = [&](int e) { return q1(__uint_as_float(__ldg(le + e) << 16)); };
+        const auto no_draft = [](uint32_t) { return 0.f; };
+        const auto wq = [&](float zt, float) { return q1(zt); };
         float W = 0.f;
-        int jj = -1;
+        int tok = -1;
         if (n < G) {
-            const RowRec d = load_rec(rb + G + 1 + n);
             const unsigned short* rd = reinterpret_cast<const unsigned short*>(p.draft) + ((size_t)b * G + n) * p.V;
-            const ResidualW rw = residual_weight(t, d, c2, p.lenience);
-            const auto wr = [&](int e) {
-                const uint32_t en = __ldg(le + e);
-                const float zt = __uint_as_float(en << 16);
-                if (!(zt >= t.thr)) return 0.f;  // q = 0 (the draft logit is not needed)
+            const ResidualW rw = residual_weight(t, dn, c2, p.lenience);
+            const auto draft_of = [&](uint32_t en) {
+                if (!(__uint_as_float(en << 16) >= t.thr)) return 0.f;  // q = 0: the draft logit is not needed
                 const uint32_t i = en >> 16;
-                const float zd = SV_IN_SEQ(i, p.V, p.status, b) ? __uint_as_float((uint32_t)__ldg(rd + i) << 16) : 0.f;
-                return rw(zt, zd);
+                return SV_IN_SEQ(i, p.V, p.status, b) ? __uint_as_float((uint32_t)__ldg(rd + i) << 16) : 0.f;
             };
-            jj = warp_list_draw(t.nkept, rcnt[warp], roff[warp], u2, wr, &W);
+            const auto wr = [&](float zt, float zd) { return zt >= t.thr ? rw(zt, zd) : 0.f; };
+            tok = warp_list_draw(t.nkept, roff[warp], le, u2, draft_of, wr, &W);
         }
-        if (!(W > 0.f)) jj = warp_list_draw(t.nkept, rcnt[warp], roff[warp], u2, wq, &W);  // bonus, or a vanished residual
+        if (!(W > 0.f)) tok = warp_list_draw(t.nkept, roff[warp], le, u2, no_draft, wq, &W);  // bonus, or a vanished residual
         __syncwarp();  // the region table is read before the warp's next sequence rewrites it
         if (lane == 0) {
-            const int tok = jj >= 0 ? (int)(__ldg(le + jj) >> 16) : -1;
             p.next_token[b] = tok;
-            p.tokens[(size_t)b * (G + 1) + n] = tok;
+            p.tokens[trow0 + n] = tok;
         }
     }
 }
 
-// The queued sequences (kept list longer than its capacity): one CTA per
-// sequence draws from the residual row pair, or the bonus row, in global
-// memory with the CTA-wide inverse CDF of draw.cuh.
+// The queued sequences (no usable window list): one CTA per sequence draws
+// from the residual row pair, or the bonus row, in global memory with the
+// CTA-wide inverse CDF of draw.cuh, four 16-byte vectors of each row per
+// thread and round in flight (a 32000-logit row is four rounds).
+constexpr int kFullVec = 4;
 __global__ void __launch_bounds__(NT) smem_fulldraw_kernel(const __grid_constant__ RowParams p) {
     __shared__ DrawShared ds;
     __shared__ int job;
@@ -1060,9 +1134,9 @@ __global__ void __launch_bounds__(NT) smem_fulldraw_kernel(const __grid_constant
             if (n < G) {
                 const RowRec d = load_rec(rb + G + 1 + n);
                 const bf16_t* rd = reinterpret_cast<const bf16_t*>(p.draft) + ((size_t)b * G + n) * V;
-                tok = draw_residual<bf16_t, draw_vec<bf16_t>()>(ds, rt, rd, V, t, d, c2, u2, p.lenience);
+                tok = draw_residual<bf16_t, kFullVec>(ds, rt, rd, V, t, d, c2, u2, p.lenience);
             } else {
-                tok = draw_q<bf16_t, draw_vec<bf16_t>()>(ds, rt, V, t, c2, u2);
+                tok = draw_q<bf16_t, kFullVec>(ds, rt, V, t, c2, u2);
             }
             if (tid == 0) {
                 p.next_token[b] = tok;

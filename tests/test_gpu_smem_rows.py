@@ -69,6 +69,21 @@ def test_flat_rows_many_candidates_and_long_kept_lists():
     run(zt, zd, 1.0, 1.0, 3000, seed=9, label="smem flat top-k", max_near=0.2)
 
 
+@pytest.mark.parametrize("gamma", [31, 32, 40])
+def test_draft_lengths_beyond_one_warp(gamma):
+    """gamma at and beyond 32: the acceptance tests run 32 positions a round,
+    the bonus row can lie in the second round, and (gamma >= 10) the window
+    list sizes of row n are read on their own. Drafts close to the target, so
+    that sequences accept past position 32 and some take the bonus; a top-k
+    transform, so that no threshold sits on a near-tie of the kept mass (a
+    sequence has 2 gamma + 1 rows that could hold one)."""
+    zt, zd = workloads.linear_logits(6, gamma, 32000, 70 + gamma, dtype="bf16", sd_t=3.0, sd_d=0.05, boost=5.0,
+                                     boost_p=0.01)
+    g, r, _ = run(zt, zd, 0.8, 1.0, 300, seed=gamma, label=f"smem gamma={gamma}", max_near=0.0)
+    if gamma >= 32:
+        assert (r["accepted"] >= 32).any()
+
+
 def test_ties_top_k_and_top_p():
     g = torch.Generator().manual_seed(5)
     zt = (torch.randint(-6, 7, (16, 4, 3000), generator=g).float() * 0.5).bfloat16()
