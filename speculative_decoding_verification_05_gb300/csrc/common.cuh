@@ -305,8 +305,8 @@ struct RowParams {
     unsigned int* row_cnt;  // [B * rows_per_b] segment arrivals (nseg > 1)
     unsigned int* seq_cnt;  // [B] row arrivals
     unsigned int* work;     // work counters (zero at launch): [0] next work unit (row kernel) or
-                            // queued sequences, [1] next sequence to draw, [2] next queued
-                            // sequence, [3] queued rows, [4] next queued row
+                            // queued sequences, [1] next sequence to draw (streaming path),
+                            // [2] next queued sequence, [3] queued rows, [4] next queued row
     int32_t* seq_n;         // [B] accepted length of each resolved sequence (-1: bad data)
     // shared-memory row path: the window list of every target row (the
     // logits within the window of its maximum, a superset of its kept set):
