@@ -44,7 +44,7 @@ def test_nucleus_1000_steps_in_one_call():
 
     r = _oracle_rows(one, idx)
     gs = _take(g, idx)
-    assert_linear_parity(gs, r, max_near_frac=0.2, label="nucleus x1000")
+    assert_linear_parity(gs, r, max_near_frac=0.05, label="nucleus x1000")
     assert_probs(gs["probs"], r, "nucleus x1000")
     assert (np_(g["status"]) == 0).all() and ((np_(g["accepted"]) >= 0) & (np_(g["accepted"]) <= 4)).all()
 
@@ -63,7 +63,7 @@ def test_mentor_12_steps_in_one_call():
 
     r = _oracle_rows(one, idx)
     gs = _take(g, idx)
-    assert_linear_parity(gs, r, max_near_frac=0.25, label="mentor x12")
+    assert_linear_parity(gs, r, max_near_frac=0.05, label="mentor x12")
     assert_probs(gs["probs"], r, "mentor x12")
     assert_mentor_alpha(gs["alpha"], r, "mentor x12")
     assert ((r["alpha"] > 0) & (r["alpha"] < 1)).any(), "no sampled position reached the solver"

@@ -68,7 +68,7 @@ def test_verify_small_vocabularies(dbg, V, dtype):
         rel, deb = _both(lambda: sv.verify(zt.cuda(), zd.cuda() if T > 0 else None, d, T, top_p, top_k, 3, 0))
         _same(rel, deb, ("accepted", "tokens", "next_token", "status"))
         r = oracle.verify(zt, zd, drafts, T, top_p, top_k, 3, 0)
-        assert_linear_parity(deb, r, max_near_frac=0.5, label=f"debug V={V} {dtype} T={T}")
+        assert_linear_parity(deb, r, max_near_frac=0.0, label=f"debug V={V} {dtype} T={T}")
 
 
 def test_verify_shared_memory_rows_and_segments(dbg):

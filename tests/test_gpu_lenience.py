@@ -24,7 +24,7 @@ def test_lenient_matches_oracle(l, name, T, top_p, top_k):
                   debug=True, lenience=l)
     torch.cuda.synchronize()
     r = oracle.verify(zt, zd, drafts, T, top_p, top_k, 9, 2, lenience=l)
-    assert_linear_parity(g, r, max_near_frac=0.2, label=f"{name} l={l}")
+    assert_linear_parity(g, r, max_near_frac=0.05, label=f"{name} l={l}")
     assert_probs(g["probs"], r, f"{name} l={l}")
     if l <= 0.5:
         # leniency accepts more than the exact method on the same uniforms

@@ -44,8 +44,8 @@ def test_max_vocabulary_top_p_on_few_rows():
     selection over the whole row."""
     zt, zd = workloads.linear_logits(3, 4, MAX_V, seed=22, dtype="bf16", sd_t=3.0, sd_d=0.5, boost=6.0,
                                      boost_p=0.01)
-    _verify(zt, zd, 0.8, top_p=0.95, label="V max top-p", max_near=0.3)
-    _verify(zt, zd, 1.0, top_k=1000, label="V max top-k", max_near=0.3)
+    _verify(zt, zd, 0.8, top_p=0.95, label="V max top-p", max_near=0.0)
+    _verify(zt, zd, 1.0, top_k=1000, label="V max top-k", max_near=0.0)
 
 
 def test_max_sizes_at_temperature_zero():

@@ -33,7 +33,7 @@ def test_vocabularies_and_transforms(V, T, top_p, top_k):
     B = 9 if V >= 32000 else 37
     zt, zd = workloads.linear_logits(B, 3, V, 40 + V, dtype="bf16", sd_t=3.0, sd_d=0.7, boost=5.0, boost_p=0.01)
     run(zt, zd, T, top_p, top_k, seed=V % 97, offset=7, label=f"smem V={V} T={T} p={top_p} k={top_k}",
-        max_near=0.25)
+        max_near=0.05)
 
 
 def test_many_sequences_more_rows_than_sms():
@@ -48,7 +48,7 @@ def test_many_sequences_more_rows_than_sms():
         r = oracle.verify(zt[b:b + 1].float().cpu().numpy(), zd[b:b + 1].float().cpu().numpy(), dn[b:b + 1],
                           c["temperature"], c["top_p"], 0, 17, int(b))
         gs = {k: v[b:b + 1] for k, v in g.items()}
-        assert_linear_parity(gs, r, max_near_frac=1.0, label="smem x500")
+        assert_linear_parity(gs, r, max_near_frac=0.05, label="smem x500")
         assert_probs(gs["probs"], r, "smem x500")
 
 
@@ -65,8 +65,8 @@ def test_flat_rows_many_candidates_and_long_kept_lists():
     are compacted) and nuclei of thousands of tokens (longer than a kept
     list, so the draw reads the rows)."""
     zt, zd = workloads.linear_logits(12, 2, 40000, 23, dtype="bf16", sd_t=0.2, sd_d=0.3)
-    run(zt, zd, 1.0, 0.9, 0, seed=8, label="smem flat top-p", max_near=0.2)
-    run(zt, zd, 1.0, 1.0, 3000, seed=9, label="smem flat top-k", max_near=0.2)
+    run(zt, zd, 1.0, 0.9, 0, seed=8, label="smem flat top-p", max_near=0.05)
+    run(zt, zd, 1.0, 1.0, 3000, seed=9, label="smem flat top-k", max_near=0.05)
 
 
 @pytest.mark.parametrize("gamma", [31, 32, 40])
@@ -100,7 +100,7 @@ def test_lenience(lenience):
     g = sv.verify(zt.cuda(), zd.cuda(), torch.from_numpy(drafts).int().cuda(), 0.8, 0.95, 0, 2, 0, debug=True,
                   lenience=lenience)
     r = oracle.verify(zt, zd, drafts, 0.8, 0.95, 0, 2, 0, lenience=lenience)
-    assert_linear_parity(g, r, max_near_frac=0.2, label=f"smem l={lenience}")
+    assert_linear_parity(g, r, max_near_frac=0.05, label=f"smem l={lenience}")
     assert_probs(g["probs"], r, f"smem l={lenience}")
 
 
@@ -131,4 +131,4 @@ def test_unaligned_rows_take_the_streaming_path_with_the_same_results():
     d = torch.from_numpy(drafts).int().cuda()
     a = sv.verify(zt_c, zd_c, d, 0.8, 0.95, 0, 5, 0)
     r = oracle.verify(zt, zd, drafts, 0.8, 0.95, 0, 5, 0)
-    assert_linear_parity(a, r, max_near_frac=0.2, label="unaligned draft")
+    assert_linear_parity(a, r, max_near_frac=0.05, label="unaligned draft")

@@ -73,7 +73,7 @@ def _mentor(zt, zd, D, seed=0, iters=30, label=""):
     g = sv.verify_mentor(zt.cuda(), zd.cuda(), torch.from_numpy(drafts).int().cuda(), 1.0, D, iters,
                          seed, 0, debug=True)
     r = oracle.verify_mentor(zt_o, zd_o, drafts, 1.0, D, iters, seed, 0)
-    assert_linear_parity(g, r, max_near_frac=0.15, label=label)
+    assert_linear_parity(g, r, max_near_frac=0.05, label=label)
     assert_probs(g["probs"], r, label)
     assert_mentor_alpha(g["alpha"], r, label)
     return g, r, drafts

@@ -52,7 +52,7 @@ def test_nucleus_config(sigma):
     zt, zd = workloads.config_logits("nucleus", 1002, steps=8, sd_d=sigma)
     # near-ties: a top-p crossing mass within 1e-5 of top_p is a ~1% event per row (bf16 ties)
     g, r, near = run(zt, zd, c["temperature"], c["top_p"], 0, seed=3, label=f"nucleus s={sigma}",
-                     max_near=0.2)
+                     max_near=0.1)
     assert (r["accepted"] >= 0).all()
 
 
@@ -60,10 +60,12 @@ def test_nucleus_config(sigma):
 @pytest.mark.parametrize("T,top_p,top_k", [(1.0, 1.0, 0), (0.7, 1.0, 50), (1.0, 0.9, 0),
                                            (1.0, 0.8, 200), (0.5, 0.5, 3), (1.0, 1.0, 1)])
 def test_transforms_ragged_vocab(dtype, T, top_p, top_k):
-    """V=40001 (odd: rows start off the 16-byte grid and end in a ragged tail)."""
+    """V=40001 (odd: rows start off the 16-byte grid and end in a ragged tail).
+    fp32 at top_p = 0.9 has 5 near-tie sequences of the 24 on these inputs
+    (top-p crossings within 1e-5 of the target mass); the others have none."""
     zt, zd = workloads.linear_logits(24, 3, 40001, 11, dtype=dtype, sd_t=3.0, sd_d=0.8)
     run(zt, zd, T, top_p, top_k, seed=5, offset=1000, label=f"{dtype} T={T} p={top_p} k={top_k}",
-        max_near=0.5)
+        max_near=0.25)
 
 
 def deep_tie_logits(B, gamma, V, T, seed, dtype):
@@ -90,7 +92,7 @@ def test_flat_rows_overflow_the_collected_keys(dtype, T, top_p, top_k):
     """Flat rows put more keys near the maximum than each thread collects, so
     the threshold comes from the row in global memory."""
     zt, zd = workloads.linear_logits(12, 2, 40001, 23, dtype=dtype, sd_t=0.2, sd_d=0.3)
-    run(zt, zd, T, top_p, top_k, seed=8, label=f"flat {dtype} p={top_p} k={top_k}", max_near=0.2)
+    run(zt, zd, T, top_p, top_k, seed=8, label=f"flat {dtype} p={top_p} k={top_k}", max_near=0.05)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -135,7 +137,7 @@ def test_large_vocab_config_full_size():
     """large_vocab at full size: B=64, gamma=7, V=128256, f32, T=1 and T=0."""
     c = workloads.CONFIGS["large_vocab"]
     zt, zd = workloads.config_logits("large_vocab", 1003)
-    run(zt, zd, 1.0, seed=1, label="large_vocab T=1", max_near=0.15)
+    run(zt, zd, 1.0, seed=1, label="large_vocab T=1", max_near=0.1)
     drafts = zd.argmax(dim=2).numpy()
     run(zt, zd, 0.0, drafts=drafts, label="large_vocab T=0")
 
