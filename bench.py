@@ -66,7 +66,7 @@ OPS = {"nucleus_alpha": "alpha"}      # measured acceptance probabilities instea
 
 # The timed unit is one library call; where a call launches several kernels the
 # label names them all (the row or argmax kernel reads every logit byte).
-SMEM_PATH = "smem_row_kernel + smem_fallback_kernel + smem_draw_kernel + smem_fulldraw_kernel"
+SMEM_PATH = "smem_row_kernel + smem_tail_kernel + smem_fulldraw_kernel"
 KERNEL_OF = {"nucleus": SMEM_PATH, "tiny": "row_kernel<f32> + draw_kernel",
              "large_vocab": "row_kernel<f32> + draw_kernel", "large_vocab_t0": "argmax_kernel<f32>",
              "tree": "argmax_kernel<f32>",
@@ -294,8 +294,8 @@ def smem_path(inp):
 def launches_per_step(inp):
     """Kernels one library call launches: rows, position solve and resolve
     (mentor); the argmax kernel (tree, T = 0); on the shared-memory row path
-    the row, fallback, draw and full-row draw kernels; rows and draws
-    otherwise."""
+    the row kernel, the fallback-and-draw kernel and the full-row draw
+    kernel; rows and draws otherwise."""
     if inp["kind"] == "mentor":
         return 3
     if inp["kind"] == "rest" or inp.get("op") == "alpha":
@@ -303,7 +303,7 @@ def launches_per_step(inp):
     if inp["kind"] == "tree" or inp["T"] == 0:
         return 1
     if smem_path(inp):
-        return 4
+        return 3
     return 2
 
 

@@ -78,6 +78,7 @@ cudaError_t debug_read_tree_build(unsigned int* count, unsigned int* line);
 // Per-task record flags.
 constexpr int kRecEData = 2;     // bad logits in this row, or a draft token out of range
 constexpr int kRecTimeout = 4;   // the row's staging copy did not complete in time
+constexpr int kRecFallback = 8;  // shared-memory path: the row's threshold comes from the fallback selection
 
 constexpr uint32_t kPurposeAccept = 0;
 constexpr uint32_t kPurposeResample = 1;
@@ -264,7 +265,7 @@ struct alignas(16) RowRec {
     float Sk;     // kept mass (the normaliser of the row's probabilities)
     float zx;     // the draft token's logit in this row (rows with a token)
     int32_t x;    // the draft token (rows with a token), else -1
-    int32_t flags;  // kRecEData, kRecTimeout
+    int32_t flags;  // kRecEData, kRecTimeout, kRecFallback
     int32_t nkept;  // shared-memory row path, target rows: entries of the window list (-1: none)
 };
 

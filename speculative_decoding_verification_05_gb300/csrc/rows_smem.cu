@@ -624,11 +624,11 @@ __global__ void __launch_bounds__(kRowThreads, 1) smem_row_kernel(const __grid_c
                 rec.Sk = sk;
                 rec.zx = zx;
                 rec.x = x;
-                rec.flags = (bad || (has_x && (x < 0 || x >= V))) ? kRecEData : 0;
+                rec.flags = ((bad || (has_x && (x < 0 || x >= V))) ? kRecEData : 0) | (decided ? 0 : kRecFallback);
                 rec.nkept = nkept;
                 if (SV_IN(row, nrows)) p.rows[row] = rec;
                 if (!decided) {
-                    // the whole row decides it (smem_fallback_kernel)
+                    // the whole row decides it (fallback_rows, in smem_tail_kernel)
                     const unsigned qi = atomicAdd(p.work + 3, 1u);
                     if (SV_IN(qi, nrows)) p.fb_rows[qi] = row;
                 }
@@ -733,10 +733,8 @@ SV_DEV void block_scan2(FallbackShared& s, unsigned long long& a, unsigned long 
     }
 }
 
-__global__ void __cluster_dims__(kFbCluster, 1, 1) __launch_bounds__(NT)
-    smem_fallback_kernel(const __grid_constant__ RowParams p) {
-    __shared__ uint32_t fcnt[kFbRange / 2];  // this CTA's values, two 16-bit counts a word
-    __shared__ FallbackShared s;
+// fcnt: this CTA's values, two 16-bit counts a word (kFbRange / 2 words).
+SV_DEV void fallback_rows(const RowParams& p, uint32_t* fcnt, FallbackShared& s) {
     namespace cg = cooperative_groups;
     cg::cluster_group cl = cg::this_cluster();
     const int rank = (int)cl.block_rank();
@@ -988,24 +986,26 @@ SV_DEV RowRec shfl_rec(const RowRec& r, int src) {
     return o;
 }
 
-// One warp per sequence (warp w of the grid takes sequences w, w + warps,
-// ...): the acceptance tests of all positions at once (lane k loads target
-// record k and draft record k, 32 positions a round), the first rejection
-// n, the accepted prefix, and the draw from the window list of target row
-// n, whose record and region sizes the warp already holds (the region sizes
-// of every target row of the sequence are loaded with the records), so
-// that only the list and the draft logits it names are loaded after n is
-// known. A sequence whose target row has no usable list (a fallback row, or
-// a region of the list overflowed) is queued (p.seq_n, counted in
-// p.work[0]) for smem_fulldraw_kernel, which draws from the rows.
-__global__ void __launch_bounds__(NT, 4) smem_draw_kernel(const __grid_constant__ RowParams p) {
-    __shared__ int roff[NW][kKeptRegions];
+// One warp per sequence (warp w0 + i nwarps takes sequence i ... : the
+// caller numbers its warps): the acceptance tests of all positions at once
+// (lane k loads target record k and draft record k, 32 positions a round),
+// the first rejection n, the accepted prefix, and the draw from the window
+// list of target row n, whose record and region sizes the warp already
+// holds (the region sizes of every target row of the sequence are loaded
+// with the records), so that only the list and the draft logits it names
+// are loaded after n is known. A sequence is queued (p.seq_n, counted in
+// p.work[0]) for smem_fulldraw_kernel, which resolves it again from the
+// rows, when one of its rows takes its threshold from the fallback (which
+// may still be running: nothing of the sequence is written here) or when
+// its target row n has no usable list (a region of the list overflowed).
+// roff: a [NW][kKeptRegions] table in shared memory, one row per warp.
+SV_DEV void draw_sequences(const RowParams& p, int (*roff)[kKeptRegions], long long w0, long long nwarps) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int R = p.rows_per_b, G = p.gamma;
     const float c2 = p.c2;
     const int cw = 3 * (G + 1);  // 4-byte words of region sizes of a sequence's target rows
     static_assert(kKeptRegions == 12, "region sizes of a row: three 4-byte words");
-    for (long long bb = (long long)blockIdx.x * NW + warp; bb < p.B; bb += (long long)gridDim.x * NW) {
+    for (long long bb = w0; bb < p.B; bb += nwarps) {
         const int b = (int)bb;
         const RowRec* rb = p.rows + (size_t)b * R;
         const size_t trow0 = (size_t)b * (G + 1);
@@ -1043,6 +1043,10 @@ __global__ void __launch_bounds__(NT, 4) smem_draw_kernel(const __grid_constant_
             }
         }
         flags = __reduce_or_sync(0xFFFFFFFFu, flags);
+        if (flags & kRecFallback) {
+            if (lane == 0) p.seq_n[atomicAdd(p.work, 1u)] = b;  // resolved from the rows afterwards
+            continue;
+        }
         const int stt = (flags & kRecTimeout) ? kETimeout : ((flags & kRecEData) ? kEData : kOk);
         if (lane == 0) {
             p.accepted[b] = stt ? -1 : n;
@@ -1106,27 +1110,78 @@ __global__ void __launch_bounds__(NT, 4) smem_draw_kernel(const __grid_constant_
     }
 }
 
-// The queued sequences (no usable window list): one CTA per sequence draws
-// from the residual row pair, or the bonus row, in global memory with the
-// CTA-wide inverse CDF of draw.cuh, four 16-byte vectors of each row per
-// thread and round in flight (a 32000-logit row is four rounds).
+// After the row kernel: the queued rows' thresholds and every sequence's
+// acceptance and draw in one launch. The first fb_ctas CTAs (whole
+// clusters) take the queued rows (fallback_rows), the warps of the others
+// take the sequences (draw_sequences); a sequence with a queued row is left
+// to smem_fulldraw_kernel, which runs once every record is complete, so no
+// CTA waits for one outside its own cluster.
+__global__ void __cluster_dims__(kFbCluster, 1, 1) __launch_bounds__(NT, 4)
+    smem_tail_kernel(const __grid_constant__ RowParams p, const int fb_ctas) {
+    __shared__ uint32_t fcnt[kFbRange / 2];
+    __shared__ FallbackShared s;
+    __shared__ int roff[NW][kKeptRegions];
+    if ((int)blockIdx.x < fb_ctas) {
+        fallback_rows(p, fcnt, s);  // (fb_ctas is a multiple of the cluster size: whole clusters)
+        return;
+    }
+    draw_sequences(p, roff, (long long)(blockIdx.x - fb_ctas) * NW + (threadIdx.x >> 5),
+                   (long long)(gridDim.x - fb_ctas) * NW);
+}
+
+// The queued sequences: one CTA per sequence resolves it from its records,
+// all complete by now (acceptance at every position, one thread each; the
+// first rejection n; the accepted prefix), then draws from the residual row
+// pair, or the bonus row, in global memory with the CTA-wide inverse CDF of
+// draw.cuh, four 16-byte vectors of each row per thread and round in flight
+// (a 32000-logit row is four rounds). The acceptance arithmetic is
+// draw_sequences' own, so a sequence it queued after writing its outputs
+// (no usable list) gets the same n and prefix again.
 constexpr int kFullVec = 4;
 __global__ void __launch_bounds__(NT) smem_fulldraw_kernel(const __grid_constant__ RowParams p) {
     __shared__ DrawShared ds;
-    __shared__ int job;
+    __shared__ int job, sn, sfl;
     const int tid = threadIdx.x;
     const int R = p.rows_per_b, G = p.gamma, V = p.V;
     const float c2 = p.c2;
     const unsigned nq = __ldcg(p.work);
     for (;;) {
-        if (tid == 0) job = (int)atomicAdd(p.work + 2, 1u);
+        if (tid == 0) {
+            job = (int)atomicAdd(p.work + 2, 1u);
+            sn = G;
+            sfl = 0;
+        }
         __syncthreads();
         const int qi = job;
         if (qi >= (int)nq) break;
-        const int b = __ldcg(p.seq_n + qi);
-        const int n = __ldcg(p.accepted + b);
-        if (SV_IN_SEQ(n, G + 1, p.status, b)) {
-            const RowRec* rb = p.rows + (size_t)b * R;
+        const int b = SV_IN(qi, p.B) ? __ldcg(p.seq_n + qi) : 0;
+        const RowRec* rb = p.rows + (size_t)b * R;
+        int fl = 0;
+        for (int i = tid; i < R; i += NT) fl |= __ldcg(&rb[i].flags);
+        if (fl) atomicOr(&sfl, fl);
+        for (int k = tid; k < G; k += NT) {
+            const RowRec t = load_rec(rb + k), d = load_rec(rb + G + 1 + k);
+            const float q = KeptExp{t.thr, c2, t.m * c2, 1.f}(t.zx) / t.Sk;
+            const float pd = KeptExp{d.thr, c2, d.m * c2, 1.f}(d.zx) / d.Sk;
+            if (p.probs_dbg) {
+                p.probs_dbg[((size_t)b * G + k) * 2 + 0] = q;
+                p.probs_dbg[((size_t)b * G + k) * 2 + 1] = pd;
+            }
+            const float u = uniform01(p.seed, p.offset + (uint64_t)b, (uint32_t)k, kPurposeAccept);
+            if (!accept_test(u, q, p.lenience * pd)) atomicMin(&sn, k);
+        }
+        __syncthreads();
+        const int n = sn, flags = sfl;
+        const int stt = (flags & kRecTimeout) ? kETimeout : ((flags & kRecEData) ? kEData : kOk);
+        if (tid == 0) {
+            p.accepted[b] = stt ? -1 : n;
+            if (stt) p.next_token[b] = -1;
+            if (p.status) p.status[b] = stt;
+        }
+        for (int j = tid; j <= G; j += NT)
+            if ((stt || j != n) && SV_IN_SEQ((size_t)b * (G + 1) + j, (long long)p.B * (G + 1), p.status, b))
+                p.tokens[(size_t)b * (G + 1) + j] = (!stt && j < n) ? __ldcg(&rb[j].x) : -1;
+        if (!stt) {  // (the same in every thread)
             const RowRec t = load_rec(rb + n);
             const float u2 = uniform01(p.seed, p.offset + (uint64_t)b, (uint32_t)n, kPurposeResample);
             const bf16_t* rt = reinterpret_cast<const bf16_t*>(p.target) + ((size_t)b * (G + 1) + n) * V;
@@ -1143,7 +1198,7 @@ __global__ void __launch_bounds__(NT) smem_fulldraw_kernel(const __grid_constant
                 p.tokens[(size_t)b * (G + 1) + n] = tok;
             }
         }
-        __syncthreads();
+        __syncthreads();  // job, sn and sfl are read before thread 0 resets them
     }
 }
 
@@ -1174,24 +1229,24 @@ cudaError_t launch_smem_rows(const RowParams& p, int nbuf, size_t smem, int sms,
     const long long rows = (long long)p.B * p.rows_per_b;
     const int grid = (int)(rows < sms ? rows : sms);
     smem_row_kernel<<<grid, kRowThreads, smem, stream>>>(p, nbuf);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    // the queued rows (usually none: the clusters find the queue empty and exit)
-    smem_fallback_kernel<<<std::max(kFbCluster, sms / kFbCluster * kFbCluster), NT, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_smem_draws(const RowParams& p, int sms, cudaStream_t stream) {
     static const int per_sm = [] {
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, smem_draw_kernel, NT, 0) != cudaSuccess || n < 1) n = 1;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, smem_tail_kernel, NT, 0) != cudaSuccess || n < 1) n = 1;
         return n;
     }();
-    const long long warps = ((long long)p.B + NW - 1) / NW;
-    const int grid = (int)(warps < (long long)sms * per_sm ? warps : (long long)sms * per_sm);
-    smem_draw_kernel<<<grid, NT, 0, stream>>>(p);
+    // the queued rows (usually a few: the other clusters find the queue
+    // empty and exit at once), then the sequences' warps, whole clusters
+    const int fb_ctas = std::max(1, sms / kFbCluster) * kFbCluster;
+    long long dr = std::min<long long>(((long long)p.B + NW - 1) / NW, (long long)sms * per_sm);
+    dr = (dr + kFbCluster - 1) / kFbCluster * kFbCluster;
+    smem_tail_kernel<<<(unsigned)(fb_ctas + dr), NT, 0, stream>>>(p, fb_ctas);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    // the queued sequences (usually none: the CTAs find the queue empty and exit)
+    // the queued sequences (usually a few; CTAs that find the queue empty exit)
     smem_fulldraw_kernel<<<sms, NT, 0, stream>>>(p);
     return cudaGetLastError();
 }
