@@ -18,19 +18,22 @@
 //                 one group sums, the other gathers or waits); in its group
 //                 each warp owns a contiguous range of the row: S against m,
 //                 the vectors holding a logit within kWin octaves of m listed
-//                 in index order, then those logits gathered and counted per
-//                 distinct bf16 value below m;
+//                 in index order, then those logits gathered, counted per
+//                 distinct bf16 value below m and, for a target row, written
+//                 as the warp's region of the row's window list;
 //   select warps  one per ring slot: from the counts, the exact top-k /
-//                 top-p threshold; from the gathered logits, the kept list of
-//                 a target row (z >= tau, index order); the row record.
+//                 top-p threshold and kept mass; the row record.
 //
 // A row whose window does not decide the threshold (a list overflowed, or
-// the crossing lies deeper than kWin octaves) is queued; the fallback kernel
-// then runs the selection of select.cuh over the whole row in global memory.
-// The per-sequence work (acceptance left to right, "改进的拒绝采样", the first
-// rejection n, and the one draw from max(0, q_n - l p_n) or the bonus draw
-// from q_gamma) runs last, one warp per sequence, from the row records and
-// kept lists.
+// the crossing lies deeper than kWin octaves) is queued and its record
+// marked; smem_tail_kernel then counts such a row per distinct bf16 value
+// over a thread-block cluster (the same threshold as select.cuh's selection)
+// while its other warps do the per-sequence work: acceptance at every
+// position ("改进的拒绝采样"), the first rejection n, and the one draw from
+// max(0, q_n - l p_n) or the bonus draw from q_gamma, one warp per sequence
+// over the window list of target row n. A sequence with a marked row, or
+// without a usable list, is resolved last from the rows by
+// smem_fulldraw_kernel.
 
 #include <cooperative_groups.h>
 
@@ -43,7 +46,7 @@ namespace {
 
 using namespace sel;
 
-constexpr int NT = kSelNT;               // draw and fallback kernels
+constexpr int NT = kSelNT;               // tail and full-row draw kernels
 constexpr int NW = NT / 32;
 constexpr int kWin = 12;                 // candidates: logits within kWin octaves of the row maximum
 constexpr int kGroupWarps = kKeptRegions;  // sum warps per group (one window-list region each)
